@@ -1,0 +1,206 @@
+"""PyTorch-facing API over the C ABI: tensors in, tensors out.
+
+PyTorch only provides device memory, the current stream and autograd; every
+step of the computation runs in the library's CUDA kernels. Nothing here
+computes attention, and nothing falls back to another implementation: an
+unsupported call raises (FFPA docs, "Backends Overview" page, "Automatic SDPA
+fallback": unsupported dtype and similar raise NotImplementedError /
+ValueError, no silent fallback).
+
+Layouts (FFPA docs, "CuTe-DSL Backend" page): dense q [B, Hq, Nq, D],
+k/v [B, Hkv, Nkv, D]; packed varlen q [Tq, Hq, D], k/v [Tk, Hkv, D] with
+int32 cu_seqlens; LSE is fp32 [B, Hq, Nq] (dense) or [Hq, Tq] (varlen).
+Non-contiguous inputs are made contiguous first.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _ffi
+
+_DTYPES = {torch.bfloat16: _ffi.BF16, torch.float16: _ffi.FP16}
+
+
+def _dt(x: torch.Tensor) -> int:
+    if x.dtype not in _DTYPES:
+        raise NotImplementedError(f"dtype {x.dtype}: only torch.bfloat16 and torch.float16 are supported")
+    return _DTYPES[x.dtype]
+
+
+def _prep(*xs):
+    out = []
+    for x in xs:
+        if not x.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        out.append(x.contiguous())
+    dt = out[0].dtype
+    for x in out[1:]:
+        if x.dtype != dt:
+            raise ValueError(f"mixed dtypes {dt} and {x.dtype}")
+    return out
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _scale(scale, D):
+    return float(1.0 / math.sqrt(D)) if scale is None else float(scale)
+
+
+# ----------------------------------------------------------------- dense
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """Dense forward through ffpa_fwd. Returns (o, lse)."""
+    q, k, v = _prep(q, k, v)
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,Hq,Nq,D], k and v [B,Hkv,Nkv,D]")
+    B, Hq, Nq, D = q.shape
+    Bk, Hkv, Nkv, Dk = k.shape
+    if Bk != B or Dk != D:
+        raise ValueError("q and k/v disagree on B or D")
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = _ffi.ffpa_fwd(_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                       B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D), _stream())
+    _ffi.raise_for(st, "ffpa_fwd")
+    return o, l
+
+
+def bwd_workspace_bytes(q, k) -> int:
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    return int(_ffi.ffpa_bwd_workspace_bytes(_dt(q), B, Hq, Hkv, Nq, Nkv, D))
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None,
+        dq=None, dk=None, dv=None):
+    """Dense backward through ffpa_bwd. Returns (dq, dk, dv)."""
+    q, k, v, o, dout = _prep(q, k, v, o, dout)
+    lse = lse.contiguous()
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    ws_bytes = bwd_workspace_bytes(q, k)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = _ffi.ffpa_bwd(_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                       B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D), _stream())
+    _ffi.raise_for(st, "ffpa_bwd")
+    return dq, dk, dv
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale):
+        o, lse = fwd(q, k, v, causal, scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal, ctx.scale = causal, scale
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, dlse):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = bwd(q, k, v, o, lse, do, ctx.causal, ctx.scale)
+        return dq, dk, dv, None, None
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, return_lse: bool = False):
+    """O = softmax(scale * Q K^T [bottom-right causal]) V, differentiable w.r.t. q, k, v.
+
+    The gradient of the returned LSE is not propagated (it is an auxiliary output).
+    """
+    o, lse = _Attention.apply(q, k, v, bool(causal), scale)
+    return (o, lse) if return_lse else o
+
+
+# ----------------------------------------------------------------- varlen
+def _cu(cu, device):
+    if cu is None:
+        return None
+    if cu.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    return cu.to(device).contiguous()
+
+
+def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False, scale=None):
+    """Packed forward through ffpa_varlen_fwd. Returns (o [Tq,Hq,D], lse [Hq,Tq])."""
+    q, k, v = _prep(q, k, v)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    cq, ck = _cu(cu_seqlens_q, q.device), _cu(cu_seqlens_k, q.device)
+    batch = cq.numel() - 1
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    st = _ffi.ffpa_varlen_fwd(_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              cq.data_ptr(), ck.data_ptr(), batch, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k),
+                              Hq, Hkv, D, int(bool(causal)), _scale(scale, D), _stream())
+    _ffi.raise_for(st, "ffpa_varlen_fwd")
+    return o, lse
+
+
+def varlen_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False,
+               scale=None, workspace=None):
+    """Packed backward through ffpa_varlen_bwd. Returns (dq, dk, dv)."""
+    q, k, v, o, dout = _prep(q, k, v, o, dout)
+    lse = lse.contiguous()
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    cq, ck = _cu(cu_seqlens_q, q.device), _cu(cu_seqlens_k, q.device)
+    batch = cq.numel() - 1
+    ws_bytes = int(_ffi.ffpa_varlen_bwd_workspace_bytes(_dt(q), batch, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k),
+                                                        Hq, Hkv, D))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    st = _ffi.ffpa_varlen_bwd(_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cq.data_ptr(),
+                              ck.data_ptr(), batch, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D,
+                              int(bool(causal)), _scale(scale, D), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream())
+    _ffi.raise_for(st, "ffpa_varlen_bwd")
+    return dq, dk, dv
+
+
+class _VarlenAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, cq, ck, mq, mk, causal, scale):
+        o, lse = varlen_fwd(q, k, v, cq, ck, mq, mk, causal, scale)
+        ctx.save_for_backward(q, k, v, o, lse, cq, ck)
+        ctx.args = (mq, mk, causal, scale)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, dlse):
+        q, k, v, o, lse, cq, ck = ctx.saved_tensors
+        mq, mk, causal, scale = ctx.args
+        dq, dk, dv = varlen_bwd(q, k, v, o, lse, do, cq, ck, mq, mk, causal, scale)
+        return dq, dk, dv, None, None, None, None, None, None
+
+
+def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
+                     causal: bool = False, scale: float | None = None, return_lse: bool = False):
+    """Packed-THD attention (FFPA docs, "CuTe-DSL Backend" page, "Varlen (packed THD) API").
+
+    cu_seqlens_k=None means cu_seqlens_k = cu_seqlens_q. When max_seqlen_* is
+    None it is read from cu_seqlens (one device-to-host copy).
+    """
+    if cu_seqlens_k is None:
+        cu_seqlens_k = cu_seqlens_q
+    if max_seqlen_q is None:
+        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if cu_seqlens_q.numel() > 1 else 0
+    if max_seqlen_k is None:
+        max_seqlen_k = int((cu_seqlens_k[1:] - cu_seqlens_k[:-1]).max().item()) if cu_seqlens_k.numel() > 1 else 0
+    cq, ck = _cu(cu_seqlens_q, q.device), _cu(cu_seqlens_k, q.device)
+    o, lse = _VarlenAttention.apply(q, k, v, cq, ck, int(max_seqlen_q), int(max_seqlen_k), bool(causal), scale)
+    return (o, lse) if return_lse else o
+
+
+def get_status() -> None:
+    """Synchronises the current stream and raises if a kernel reported a device time-out."""
+    _ffi.raise_for(_ffi.ffpa_get_status(_stream()), "device status")

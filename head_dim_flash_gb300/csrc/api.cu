@@ -1,0 +1,340 @@
+// C ABI entry points (declared in include/ffpa.h): argument validation,
+// workspace carving, device status word, and dispatch to the kernels.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/ffpa.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<uint64_t> g_limit_ns{2000000000ull};
+
+ffpa_status fail(ffpa_status s, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
+ffpa_status ok()
+{
+    g_err.clear();
+    return FFPA_OK;
+}
+
+}  // namespace
+
+// One status word per device; kernels record the first failing wait here.
+__device__ uint32_t g_ffpa_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices];
+int g_cc_ok[kMaxDevices];  // 0 unknown, 1 yes, -1 no
+std::mutex g_dev_mu;
+
+// Device address of the status word on the current device (looked up once).
+bool device_state(uint32_t** status, bool* cc_ok)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ffpa_status_word) != cudaSuccess) return false;
+        g_status_ptr[dev] = static_cast<uint32_t*>(p);
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    *status = g_status_ptr[dev];
+    *cc_ok = g_cc_ok[dev] == 1;
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ffpa_status check_common(ffpa_dtype dt, int Hq, int Hkv, int D, float scale)
+{
+    if (dt != FFPA_BF16 && dt != FFPA_FP16) return fail(FFPA_ERR_NOT_SUPPORTED, "dtype %d: only bf16 (0) and fp16 (1)", (int)dt);
+    if (D < 64 || D > 1024 || D % 64 != 0)
+        return fail(FFPA_ERR_NOT_SUPPORTED, "head dim D=%d: supported D is a multiple of 64 in [64, 1024]", D);
+    if (Hq < 0 || Hkv < 0) return fail(FFPA_ERR_INVALID_VALUE, "negative head count Hq=%d Hkv=%d", Hq, Hkv);
+    if (Hq > 0 && (Hkv == 0 || Hq % Hkv != 0))
+        return fail(FFPA_ERR_INVALID_VALUE, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+    if (!std::isfinite(scale)) return fail(FFPA_ERR_INVALID_VALUE, "scale must be finite");
+    return FFPA_OK;
+}
+
+ffpa_status check_ptr(const void* p, bool needed, const char* name)
+{
+    if (!needed) return FFPA_OK;
+    if (!p) return fail(FFPA_ERR_INVALID_VALUE, "%s is NULL", name);
+    if (!aligned16(p)) return fail(FFPA_ERR_INVALID_VALUE, "%s is not 16-byte aligned", name);
+    return FFPA_OK;
+}
+
+ffpa_status device_ctl(ffpa::DeviceCtl* ctl)
+{
+    bool cc_ok = false;
+    uint32_t* st = nullptr;
+    if (!device_state(&st, &cc_ok)) return fail(FFPA_ERR_CUDA, "no usable CUDA device");
+    if (!cc_ok) return fail(FFPA_ERR_NOT_SUPPORTED, "device is not compute capability 10.3 (sm_103)");
+    if (!ffpa::encode_fn()) return fail(FFPA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    ctl->status = st;
+    ctl->limit_ns = g_limit_ns.load();
+    return FFPA_OK;
+}
+
+ffpa_status launch_result(cudaError_t e, const char* what)
+{
+    if (e != cudaSuccess) return fail(FFPA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t ws_bytes(long rows) { return rows <= 0 ? 0 : 2 * align256(static_cast<size_t>(rows) * sizeof(float)); }
+
+ffpa::Problem dense_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale)
+{
+    ffpa::Problem pb{};
+    pb.varlen = 0;
+    pb.B = B;
+    pb.Hq = Hq;
+    pb.Hkv = Hkv;
+    pb.Nq = Nq;
+    pb.Nkv = Nkv;
+    pb.D = D;
+    pb.causal = causal ? 1 : 0;
+    pb.scale = scale;
+    pb.scale_log2 = scale * 1.4426950408889634f;
+    return pb;
+}
+
+ffpa_status check_dense_sizes(int B, int Hq, int Nq, int Nkv)
+{
+    if (B < 0 || Nq < 0 || Nkv < 0) return fail(FFPA_ERR_INVALID_VALUE, "negative size B=%d Nq=%d Nkv=%d", B, Nq, Nkv);
+    if (static_cast<long>(B) * Hq > 65535) return fail(FFPA_ERR_NOT_SUPPORTED, "B*Hq=%ld exceeds 65535", (long)B * Hq);
+    return FFPA_OK;
+}
+
+ffpa_status check_varlen_sizes(int batch, int total_q, int total_k, int max_q, int max_k, int Hq, const int* cu_q,
+                               const int* cu_k)
+{
+    if (batch < 0 || total_q < 0 || total_k < 0 || max_q < 0 || max_k < 0)
+        return fail(FFPA_ERR_INVALID_VALUE, "negative varlen size");
+    if (static_cast<long>(batch) * Hq > 65535)
+        return fail(FFPA_ERR_NOT_SUPPORTED, "batch*Hq=%ld exceeds 65535", (long)batch * Hq);
+    if (batch > 0 && (!cu_q || !cu_k))
+        return fail(FFPA_ERR_INVALID_VALUE, "cu_seqlens_q and cu_seqlens_k are both required (varlen-one-sided)");
+    if ((reinterpret_cast<uintptr_t>(cu_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_k) & 3u))
+        return fail(FFPA_ERR_INVALID_VALUE, "cu_seqlens must be 4-byte aligned");
+    return FFPA_OK;
+}
+
+#define FFPA_TRY(x)                              \
+    do {                                         \
+        const ffpa_status s_ = (x);              \
+        if (s_ != FFPA_OK) return s_;            \
+    } while (0)
+
+ffpa_status run_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
+                    const ffpa::Problem& pb, long q_rows, long k_rows, ffpa_stream_t stream)
+{
+    FFPA_TRY(check_ptr(q, q_rows > 0, "q"));
+    FFPA_TRY(check_ptr(o, q_rows > 0, "o"));
+    FFPA_TRY(check_ptr(lse, q_rows > 0, "lse"));
+    FFPA_TRY(check_ptr(k, q_rows > 0 && k_rows > 0, "k"));
+    FFPA_TRY(check_ptr(v, q_rows > 0 && k_rows > 0, "v"));
+    if (q_rows == 0) return ok();
+    ffpa::FwdArgs a{};
+    a.pb = pb;
+    FFPA_TRY(device_ctl(&a.ctl));
+    a.bf16 = dt == FFPA_BF16;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    return launch_result(ffpa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)), "forward launch");
+}
+
+ffpa_status run_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                    const ffpa::Problem& pb, long q_rows, long k_rows, long stat_rows, ffpa_stream_t stream)
+{
+    const bool any = q_rows > 0 || k_rows > 0;
+    FFPA_TRY(check_ptr(q, q_rows > 0, "q"));
+    FFPA_TRY(check_ptr(o, q_rows > 0, "o"));
+    FFPA_TRY(check_ptr(lse, q_rows > 0, "lse"));
+    FFPA_TRY(check_ptr(dO, q_rows > 0, "dO"));
+    FFPA_TRY(check_ptr(dq, q_rows > 0, "dq"));
+    FFPA_TRY(check_ptr(k, k_rows > 0, "k"));
+    FFPA_TRY(check_ptr(v, k_rows > 0, "v"));
+    FFPA_TRY(check_ptr(dk, k_rows > 0, "dk"));
+    FFPA_TRY(check_ptr(dv, k_rows > 0, "dv"));
+    const size_t need = ws_bytes(stat_rows);
+    if (workspace_bytes < need)
+        return fail(FFPA_ERR_INVALID_VALUE, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return fail(FFPA_ERR_INVALID_VALUE, "workspace must be non-NULL and 256-byte aligned");
+    if (!any) return ok();
+    ffpa::BwdArgs a{};
+    a.pb = pb;
+    FFPA_TRY(device_ctl(&a.ctl));
+    a.bf16 = dt == FFPA_BF16;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.dO = dO;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.delta = static_cast<float*>(workspace);
+    a.lse_log2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + need / 2);
+    return launch_result(ffpa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)), "backward launch");
+}
+
+ffpa::Problem varlen_problem(int batch, int total_q, int total_k, int max_q, int max_k, int Hq, int Hkv, int D,
+                             int causal, float scale, const int* cu_q, const int* cu_k)
+{
+    ffpa::Problem pb = dense_problem(batch, Hq, Hkv, max_q, max_k, D, causal, scale);
+    pb.varlen = 1;
+    pb.total_q = total_q;
+    pb.total_k = total_k;
+    pb.cu_q = cu_q;
+    pb.cu_k = cu_k;
+    return pb;
+}
+
+__global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ffpa::mbar_init(&bar, 1);
+        abort_flag = 0;
+        ffpa::fence_barrier_init();
+        // nothing ever arrives on `bar`: the wait must give up by itself
+        ffpa::mbar_wait(&bar, 0, &abort_flag, status, limit_ns, 255);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+ffpa_status ffpa_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                     int Hkv, int Nq, int Nkv, int D, int causal, float scale, ffpa_stream_t stream)
+{
+    FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
+    FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
+    const long q_rows = static_cast<long>(B) * Hq * Nq;
+    const long k_rows = static_cast<long>(B) * Hkv * Nkv;
+    return run_fwd(dt, q, k, v, o, lse, dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, scale), q_rows, k_rows, stream);
+}
+
+size_t ffpa_bwd_workspace_bytes(ffpa_dtype, int B, int Hq, int, int Nq, int, int)
+{
+    if (B < 0 || Hq < 0 || Nq < 0) return 0;
+    return ws_bytes(static_cast<long>(B) * Hq * Nq);
+}
+
+ffpa_status ffpa_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B,
+                     int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale, ffpa_stream_t stream)
+{
+    FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
+    FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
+    const long q_rows = static_cast<long>(B) * Hq * Nq;
+    const long k_rows = static_cast<long>(B) * Hkv * Nkv;
+    return run_bwd(dt, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes,
+                   dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, scale), q_rows, k_rows, q_rows, stream);
+}
+
+ffpa_status ffpa_varlen_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int total_q, int total_k,
+                            int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D, int causal, float scale,
+                            ffpa_stream_t stream)
+{
+    FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
+    FFPA_TRY(check_varlen_sizes(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, cu_seqlens_q, cu_seqlens_k));
+    const long q_rows = batch > 0 ? static_cast<long>(total_q) * Hq : 0;
+    const long k_rows = batch > 0 ? static_cast<long>(total_k) * Hkv : 0;
+    return run_fwd(dt, q, k, v, o, lse,
+                   varlen_problem(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, causal, scale,
+                                  cu_seqlens_q, cu_seqlens_k),
+                   q_rows, k_rows, stream);
+}
+
+size_t ffpa_varlen_bwd_workspace_bytes(ffpa_dtype, int batch, int total_q, int, int, int, int Hq, int, int)
+{
+    if (batch <= 0 || total_q < 0 || Hq < 0) return 0;
+    return ws_bytes(static_cast<long>(total_q) * Hq);
+}
+
+ffpa_status ffpa_varlen_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dO, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                            const int* cu_seqlens_k, int batch, int total_q, int total_k, int max_seqlen_q,
+                            int max_seqlen_k, int Hq, int Hkv, int D, int causal, float scale, void* workspace,
+                            size_t workspace_bytes, ffpa_stream_t stream)
+{
+    FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
+    FFPA_TRY(check_varlen_sizes(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, cu_seqlens_q, cu_seqlens_k));
+    const long q_rows = batch > 0 ? static_cast<long>(total_q) * Hq : 0;
+    const long k_rows = batch > 0 ? static_cast<long>(total_k) * Hkv : 0;
+    return run_bwd(dt, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes,
+                   varlen_problem(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, causal, scale,
+                                  cu_seqlens_q, cu_seqlens_k),
+                   q_rows, k_rows, q_rows, stream);
+}
+
+ffpa_status ffpa_get_status(ffpa_stream_t stream)
+{
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(FFPA_ERR_CUDA, "stream error: %s", cudaGetErrorString(e));
+    uint32_t word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_ffpa_status_word, sizeof(word));
+    if (e != cudaSuccess) return fail(FFPA_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+    if (word == 0) return ok();
+    const uint32_t zero = 0;
+    cudaMemcpyToSymbol(g_ffpa_status_word, &zero, sizeof(zero));
+    if ((word & 0xffu) == ffpa::DEV_TIMEOUT)
+        return fail(FFPA_ERR_TIMEOUT, "a device wait timed out (site %u, block %u)", (word >> 8) & 0xffu, word >> 16);
+    return fail(FFPA_ERR_CUDA, "device status word 0x%08x", word);
+}
+
+const char* ffpa_last_error(void) { return g_err.c_str(); }
+
+void ffpa_set_wait_limit_ns(uint64_t ns) { g_limit_ns.store(ns ? ns : 2000000000ull); }
+
+ffpa_status ffpa_selftest_wait_timeout(uint64_t limit_ns, ffpa_stream_t stream)
+{
+    bool cc_ok = false;
+    uint32_t* st = nullptr;
+    if (!device_state(&st, &cc_ok)) return fail(FFPA_ERR_CUDA, "no usable CUDA device");
+    selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(st, limit_ns);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FFPA_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
+    return ffpa_get_status(stream);
+}
+
+int ffpa_num_sms(void) { return ffpa::num_sms(); }
+
+}  // extern "C"

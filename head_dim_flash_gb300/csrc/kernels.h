@@ -1,0 +1,77 @@
+// Internal interface between the C-ABI host layer (api.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace ffpa {
+
+constexpr int kBlockM = 128;   // query rows per tile (one TMEM lane each)
+constexpr int kBlockN = 128;   // keys per tile
+constexpr int kChunk = 64;     // head-dim elements per 128-byte swizzled row
+constexpr int kVKeys = 32;     // keys per V staging chunk
+constexpr int kMaxSmem = 232448;
+
+// Problem description shared by every kernel. Dense problems use B/Nq/Nkv;
+// varlen problems use cu_q/cu_k with Nq/Nkv holding the max sequence lengths.
+struct Problem {
+    int varlen;
+    int B, Hq, Hkv, Nq, Nkv, D;
+    int total_q, total_k;
+    const int* cu_q;
+    const int* cu_k;
+    int causal;
+    float scale;        // softmax scale
+    float scale_log2;   // scale * log2(e)
+};
+
+struct DeviceCtl {
+    uint32_t* status;   // device status word
+    uint64_t limit_ns;  // bound of any single device wait
+};
+
+struct FwdArgs {
+    Problem pb;
+    int bf16;
+    const void *q, *k, *v;
+    void* o;
+    float* lse;
+    DeviceCtl ctl;
+};
+
+struct BwdArgs {
+    Problem pb;
+    int bf16;
+    const void *q, *k, *v, *o, *dO;
+    const float* lse;
+    void *dq, *dk, *dv;
+    float* delta;      // workspace [rows] fp32: rowsum(dO * O)
+    float* lse_log2;   // workspace [rows] fp32: LSE * log2(e), +inf for empty rows
+    DeviceCtl ctl;
+};
+
+// Function pointer to the driver's cuTensorMapEncodeTiled (resolved once).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
+
+// Tensor map over rows of head-dim vectors: dense [BH, N, D] or packed [T, H, D].
+// Box = 64 head-dim elements x `box_rows` rows, 128-byte swizzle.
+bool make_row_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int box_rows);
+
+// True when the query side / key side of a problem has no rows at all. Such a
+// side has no storage; tensor maps for it are built over the other side's
+// tensor (never loaded from, because every tile loop is empty).
+inline bool q_side_empty(const Problem& pb) { return pb.varlen ? pb.total_q == 0 : (pb.Nq == 0 || pb.B == 0); }
+inline bool kv_side_empty(const Problem& pb) { return pb.varlen ? pb.total_k == 0 : (pb.Nkv == 0 || pb.B == 0); }
+
+int num_sms();
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
+
+}  // namespace ffpa

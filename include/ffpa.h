@@ -1,0 +1,167 @@
+/*
+ * ffpa.h — C ABI of the GB300 (sm_103a) large-head-dim exact attention library.
+ *
+ * Operation (FFPA docs, "Backends Overview" page, "Automatic SDPA fallback":
+ * the SDPA-aligned result; "CuTe-DSL Backend" page, "Hard constraints" and
+ * "Varlen (packed THD) API"):
+ *
+ *   S = scale * Q K^T, restricted to legal keys;  O = softmax(S) V;
+ *   LSE_i = ln sum_j exp(S_ij)  (fp32, natural log, of the scaled scores);
+ *   key j is legal for query i iff j < Lk and, when causal, j <= i + (Lk - Lq)
+ *   (bottom-right / tail-aligned mask; per sequence for varlen);
+ *   a row with no legal key gives O_i = 0, LSE_i = -inf and zero gradients.
+ *   GQA/MQA: query head h reads kv head h / (Hq / Hkv).
+ *   Backward for L = sum(dO * O) gives dQ, dK, dV (dK/dV summed over the
+ *   query heads of each kv group).
+ *
+ * Element types: bf16 or fp16 for q, k, v, o, dO, dq, dk, dv (one type per
+ * call); lse is fp32. Head dim D: a multiple of 64 in [64, 1024] (the FFPA
+ * tuned range 320..1024 included). The arithmetic runs on tcgen05 tensor cores
+ * with fp32 accumulation; P is rounded to the input type before P*V.
+ *
+ * Memory and ownership: every pointer argument is DEVICE memory owned by the
+ * caller, 16-byte aligned, contiguous in the layout stated per call. The
+ * library allocates nothing; backward scratch lives in a caller-provided
+ * workspace of at least *_bwd_workspace_bytes(...) bytes.
+ *
+ * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and does no host synchronisation. Outputs are fully
+ * overwritten, never accumulated into.
+ *
+ * Errors: calls validate arguments before any launch and return
+ *   FFPA_ERR_INVALID_VALUE  null pointer with a non-empty problem, misaligned
+ *                           pointer, negative size, Hq not a multiple of Hkv,
+ *                           non-finite scale, too small a workspace, bad
+ *                           cu_seqlens sizes;
+ *   FFPA_ERR_NOT_SUPPORTED  dtype other than bf16/fp16, D outside the range
+ *                           above, a device that is not compute capability 10.3;
+ *   FFPA_ERR_CUDA           a CUDA runtime/driver call failed (launch error);
+ * and nothing is launched. A problem with no work (B, H or N zero) returns
+ * FFPA_OK without a launch. Every device-side wait in the kernels is bounded;
+ * a wait that runs out records FFPA_ERR_TIMEOUT in a device status word that
+ * ffpa_get_status() reports. ffpa_last_error() gives a thread-local message
+ * for the last failing call.
+ */
+#ifndef FFPA_H_
+#define FFPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FFPA_API __attribute__((visibility("default")))
+#else
+#define FFPA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FFPA_OK = 0,
+    FFPA_ERR_INVALID_VALUE = 1,
+    FFPA_ERR_NOT_SUPPORTED = 2,
+    FFPA_ERR_CUDA = 3,
+    FFPA_ERR_TIMEOUT = 4
+} ffpa_status;
+
+typedef enum { FFPA_BF16 = 0, FFPA_FP16 = 1 } ffpa_dtype;
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* ffpa_stream_t;
+
+/*
+ * Dense forward (FFPA docs, CuTe-DSL Backend page, "Hard constraints": dense
+ * SDPA layout, causal bottom-right, MHA/GQA/MQA via zero-stride broadcast).
+ *   q, o : [B, Hq, Nq, D]  contiguous, dtype dt        (o written)
+ *   k, v : [B, Hkv, Nkv, D] contiguous, dtype dt
+ *   lse  : [B, Hq, Nq] fp32 (written)
+ *   causal: 0 or 1 (bottom-right aligned); scale: finite (usually 1/sqrt(D)).
+ */
+FFPA_API ffpa_status ffpa_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale,
+                     ffpa_stream_t stream);
+
+/* Workspace bytes ffpa_bwd needs for this problem (fp32 row statistics). */
+FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
+
+/*
+ * Dense backward (FFPA docs, CuTe-DSL Backend page, "Blackwell status": a
+ * preprocess launch followed by gradient launches; gradients are returned in
+ * the input dtype, "Configuration"). Runs three kernels in stream order:
+ * delta = rowsum(dO * O), then dK/dV, then dQ.
+ *   q, o, dO, dq : [B, Hq, Nq, D];  k, v, dk, dv : [B, Hkv, Nkv, D]
+ *   lse : [B, Hq, Nq] fp32 as written by ffpa_fwd for the same inputs.
+ *   workspace : device scratch of >= ffpa_bwd_workspace_bytes() bytes,
+ *               256-byte aligned; its contents on entry do not matter.
+ */
+FFPA_API ffpa_status ffpa_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale,
+                     ffpa_stream_t stream);
+
+/*
+ * Packed varlen forward (FFPA docs, CuTe-DSL Backend page, "Varlen (packed
+ * THD) API"): sequences are packed along T; sequence b owns query rows
+ * [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key rows
+ * [cu_seqlens_k[b], cu_seqlens_k[b+1]). Causal is bottom-right per sequence.
+ *   q, o : [total_q, Hq, D];  k, v : [total_k, Hkv, D]
+ *   lse  : [Hq, total_q] fp32
+ *   cu_seqlens_q, cu_seqlens_k : int32 [batch+1] DEVICE arrays, start at 0,
+ *     nondecreasing, last entries equal total_q / total_k (both required; pass
+ *     the same pointer twice for self-attention). Read on the device only.
+ *   max_seqlen_q / max_seqlen_k : upper bounds of the per-sequence lengths
+ *     (they size the launch grid; a sequence longer than the bound is not
+ *     fully processed).
+ */
+FFPA_API ffpa_status ffpa_varlen_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int total_q,
+                            int total_k, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                            int causal, float scale, ffpa_stream_t stream);
+
+FFPA_API size_t ffpa_varlen_bwd_workspace_bytes(ffpa_dtype dt, int batch, int total_q, int total_k, int max_seqlen_q,
+                                       int max_seqlen_k, int Hq, int Hkv, int D);
+
+/* Packed varlen backward; layouts as in ffpa_varlen_fwd, dq like q, dk/dv like k. */
+FFPA_API ffpa_status ffpa_varlen_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int total_q,
+                            int total_k, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                            int causal, float scale, void* workspace, size_t workspace_bytes,
+                            ffpa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reports and clears the device status word:
+ * FFPA_OK, FFPA_ERR_TIMEOUT (a bounded device wait ran out; the kernel
+ * returned early and its outputs are undefined) or FFPA_ERR_CUDA (the stream
+ * reported an error).
+ */
+FFPA_API ffpa_status ffpa_get_status(ffpa_stream_t stream);
+
+/* Message for the last failing call on this host thread ("" if none). */
+FFPA_API const char* ffpa_last_error(void);
+
+/*
+ * Upper bound, in nanoseconds, of any single device-side wait in later
+ * launches (default 2e9). 0 restores the default.
+ */
+FFPA_API void ffpa_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Self-test of the bounded-wait path: launches one block whose single thread
+ * waits on a barrier that nothing completes, with a limit of `limit_ns`, and
+ * returns what ffpa_get_status() then reports (FFPA_ERR_TIMEOUT when the
+ * mechanism works). Touches no user memory.
+ */
+FFPA_API ffpa_status ffpa_selftest_wait_timeout(uint64_t limit_ns, ffpa_stream_t stream);
+
+/* Number of streaming multiprocessors of the current device (0 on error). */
+FFPA_API int ffpa_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FFPA_H_ */

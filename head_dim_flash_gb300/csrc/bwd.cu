@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int i = 0; i < last; ++i) {
                 dp.retreat(stages);
                 int dummy = 0;
-                mbar_wait(&bar_full[dp.slot], dp.phase, &dummy, status, lim, BSITE_DRAIN);
+                mbar_wait(&bar_full[dp.slot], dp.phase, &dummy, status, lim, BSITE_DRAIN, false);
             }
         }
     } else if (warp == 1) {
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             umma_commit(&bar_drain);
             int dummy = 0;
-            mbar_wait(&bar_drain, 0, &dummy, status, lim, BSITE_DRAIN);
+            mbar_wait(&bar_drain, 0, &dummy, status, lim, BSITE_DRAIN, false);
         }
     } else {
         // ---------------------------------------------- elementwise (key rows)
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int i = 0; i < last; ++i) {
                 dp.retreat(stages);
                 int dummy = 0;
-                mbar_wait(&bar_full[dp.slot], dp.phase, &dummy, status, lim, BSITE_DRAIN);
+                mbar_wait(&bar_full[dp.slot], dp.phase, &dummy, status, lim, BSITE_DRAIN, false);
             }
         }
     } else if (warp == 1) {
@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             umma_commit(&bar_drain);
             int dummy = 0;
-            mbar_wait(&bar_drain, 0, &dummy, status, lim, BSITE_DRAIN);
+            mbar_wait(&bar_drain, 0, &dummy, status, lim, BSITE_DRAIN, false);
         }
     } else {
         // ------------------------------------------ elementwise (query rows)

@@ -183,11 +183,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int i = 0; i < last; ++i) {
                 dp.retreat(stages);
                 int dummy = 0;
-                mbar_wait(&bar_full[dp.slot], dp.phase, &dummy, status, lim, SITE_DRAIN);
+                mbar_wait(&bar_full[dp.slot], dp.phase, &dummy, status, lim, SITE_DRAIN, false);
             }
             if (QRES && n_kv > 0) {
                 int dummy = 0;
-                mbar_wait(&bar_q, 0, &dummy, status, lim, SITE_DRAIN);
+                mbar_wait(&bar_q, 0, &dummy, status, lim, SITE_DRAIN, false);
             }
         }
     } else if (warp == 1) {
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             // Drain: every MMA issued by this thread has completed.
             umma_commit(&bar_drain);
             int dummy = 0;
-            mbar_wait(&bar_drain, 0, &dummy, status, lim, SITE_DRAIN);
+            mbar_wait(&bar_drain, 0, &dummy, status, lim, SITE_DRAIN, false);
         }
     } else {
         // ------------------------------------------------------ softmax + epilogue

@@ -87,9 +87,12 @@ enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 4 };
 // abort flag is raised, when another block has already recorded a failure in
 // the device status word, or after `limit_ns` of wall time; on a time-out it
 // raises the abort flag and records the status word. Returns false when the
-// caller must stop its work loop.
+// caller must stop its work loop. With honor_abort = false (used to drain
+// copies and MMAs still in flight before a block exits) only the time limit
+// ends the wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status, uint64_t limit_ns, uint32_t site)
+                                          uint32_t* status, uint64_t limit_ns, uint32_t site,
+                                          bool honor_abort = true)
 {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
@@ -97,8 +100,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 63u) == 0) {
-            if (*abort_flag) return false;
-            if (*reinterpret_cast<volatile uint32_t*>(status) != 0u) {
+            if (honor_abort && *abort_flag) return false;
+            if (honor_abort && *reinterpret_cast<volatile uint32_t*>(status) != 0u) {
                 *abort_flag = 1;
                 return false;
             }

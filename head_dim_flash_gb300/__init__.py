@@ -4,7 +4,7 @@ Forward (O and fp32 LSE) and backward (dQ, dK, dV) with bottom-right causal
 masking, GQA/MQA head broadcast and packed varlen batches, computed by
 hand-written tcgen05/TMA kernels behind the C ABI of ``include/ffpa.h``.
 """
-from .attention import (attention, bwd, bwd_workspace_bytes, fwd, get_status, varlen_attention, varlen_bwd,
+from .api import (attention, bwd, bwd_workspace_bytes, fwd, get_status, varlen_attention, varlen_bwd,
                         varlen_fwd)
 
 __all__ = ["attention", "varlen_attention", "fwd", "bwd", "bwd_workspace_bytes", "varlen_fwd", "varlen_bwd",

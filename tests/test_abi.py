@@ -1,0 +1,123 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load and export every symbol include/ffpa.h declares, and
+every invalid call must be rejected with the documented status before any
+device work (so these calls are safe without a GPU). The product path must
+fail loudly when the library is missing.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from head_dim_flash_gb300 import _ffi, build
+
+    build.build()
+    return _ffi.load()
+
+
+def header_symbols():
+    txt = open(os.path.join(ROOT, "include", "ffpa.h")).read()
+    return sorted(set(re.findall(r"FFPA_API\s+[\w\s\*]+?\b(ffpa_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_documented_entry_points():
+    syms = header_symbols()
+    for name in ("ffpa_fwd", "ffpa_bwd", "ffpa_varlen_fwd", "ffpa_varlen_bwd", "ffpa_bwd_workspace_bytes",
+                 "ffpa_varlen_bwd_workspace_bytes", "ffpa_get_status", "ffpa_last_error"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from head_dim_flash_gb300 import _ffi
+
+    syms = header_symbols()
+    assert set(syms) == set(_ffi.EXPORTS)
+    for name in syms:
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    from head_dim_flash_gb300 import _ffi
+
+    with pytest.raises(RuntimeError, match="missing"):
+        _ffi.load(str(tmp_path / "nope.so"))
+
+
+FAKE = 0x10000  # 16-byte aligned fake device address; never dereferenced by rejected calls
+
+
+def fwd(lib, dt=0, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Hq=2, Hkv=1, Nq=8, Nkv=8, D=512, causal=0,
+        scale=0.05):
+    return lib.ffpa_fwd(dt, q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dt=5), 2),                 # dtype outside bf16/fp16
+    (dict(D=100), 2),                # D not a multiple of 64
+    (dict(D=1088), 2),               # D above 1024
+    (dict(D=32), 2),                 # D below 64
+    (dict(Hq=3, Hkv=2), 1),          # Hq not a multiple of Hkv
+    (dict(Hkv=0), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(Nq=-1), 1),
+    (dict(q=0), 1),                  # NULL with a non-empty problem
+    (dict(lse=0), 1),
+    (dict(k=FAKE + 2), 1),           # misaligned
+    (dict(B=70000, Hq=1, Hkv=1), 2),  # grid limit
+])
+def test_invalid_forward_calls_are_rejected(lib, kw, status):
+    assert fwd(lib, **kw) == status
+    assert lib.ffpa_last_error()  # a message explains the rejection
+
+
+def test_empty_problem_is_ok_without_launch(lib):
+    assert fwd(lib, B=0, q=0, k=0, v=0, o=0, lse=0) == 0
+    assert fwd(lib, Nq=0, q=0, o=0, lse=0, k=0, v=0) == 0
+
+
+def test_workspace_size_and_checks(lib):
+    n = lib.ffpa_bwd_workspace_bytes(0, 1, 32, 32, 8192, 8192, 512)
+    assert n >= 2 * 32 * 8192 * 4 and n % 256 == 0
+    args = [0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE]
+    # workspace too small
+    assert lib.ffpa_bwd(*args, FAKE, 16, 1, 32, 32, 8192, 8192, 512, 0, 0.05, None) == 1
+    # workspace misaligned
+    assert lib.ffpa_bwd(*args, FAKE + 16, n, 1, 32, 32, 8192, 8192, 512, 0, 0.05, None) == 1
+    assert lib.ffpa_varlen_bwd_workspace_bytes(0, 2, 100, 100, 60, 60, 4, 2, 512) >= 2 * 4 * 100 * 4
+
+
+def test_varlen_requires_both_cu_seqlens(lib):
+    st = lib.ffpa_varlen_fwd(0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 10, 10, 5, 5, 4, 2, 512, 0, 0.05, None)
+    assert st == 1
+    assert "one-sided" in lib.ffpa_last_error().decode()
+
+
+def test_python_api_maps_status_to_exceptions():
+    from head_dim_flash_gb300 import _ffi
+
+    with pytest.raises(NotImplementedError):
+        _ffi.raise_for(_ffi.ERR_NOT_SUPPORTED, "x")
+    with pytest.raises(ValueError):
+        _ffi.raise_for(_ffi.ERR_INVALID_VALUE, "x")
+    with pytest.raises(TimeoutError):
+        _ffi.raise_for(_ffi.ERR_TIMEOUT, "x")
+    with pytest.raises(RuntimeError):
+        _ffi.raise_for(_ffi.ERR_CUDA, "x")
+
+
+def test_python_api_rejects_unsupported_dtype_before_the_library():
+    import torch
+
+    from head_dim_flash_gb300 import api
+
+    with pytest.raises(NotImplementedError):
+        api._dt(torch.zeros(1, dtype=torch.float32))

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from head_dim_flash_gb300 import attention as api
+from head_dim_flash_gb300 import api
 from head_dim_flash_gb300 import workloads
 from tests.gpu_utils import Guarded, check_grad, check_lse, check_o
 
@@ -124,7 +124,7 @@ def test_varlen_matches_oracle(causal):
 def test_autograd_entry_points():
     inp = workloads.random_dense(1, 2, 2, 64, 64, 512, torch.bfloat16, seed=31)
     q, k, v = (inp[n].cuda().requires_grad_(True) for n in ("q", "k", "v"))
-    from head_dim_flash_gb300 import attention as attn_mod
+    from head_dim_flash_gb300 import api as attn_mod
 
     o = attn_mod.attention(q, k, v, causal=True)
     o.backward(inp["dO"].cuda())

@@ -1,0 +1,369 @@
+"""Benchmark: fwd and fwd+bwd TFLOPS of exact attention at D=512, N=8192, bf16.
+
+One step = the whole hot path on one batch of synthetic input already
+resident in HBM: forward (O, LSE) then backward (preprocess, dK/dV, dQ), all
+through the C ABI. FLOPs follow the usual convention: forward
+4*B*Hq*Nq*Nkv*D, backward 2.5x that, both halved when causal.
+
+Prints ONE JSON line (rank 0). Multi-GPU runs (torchrun) give every rank the
+same per-GPU workload (weak scaling; no data-path collective) and report the
+slowest rank's time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config headline|tiny|gqa|sweep320|sweep640|sweep1024]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd & fwd+bwd TFLOPS, D=512 N=8192 bf16 (1×GB300), % of BF16 tensor peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="headline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload(name):
+    from head_dim_flash_gb300 import workloads as W
+
+    table = {"headline": W.HEADLINE, "tiny": W.TINY, "gqa": W.GQA_CAUSAL,
+             "sweep320": W.SWEEP[0], "sweep640": W.SWEEP[1], "sweep1024": W.SWEEP[2]}
+    if name not in table:
+        raise SystemExit(f"unknown config {name}; choose from {sorted(table)}")
+    return table[name]
+
+
+def flops(w):
+    f = 4.0 * w.B * w.Hq * w.Nq * w.Nkv * w.D
+    if w.causal:
+        f *= 0.5
+    return f, 2.5 * f
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_baseline(w, n_rows=512, seed_rows=0):
+    """Times the fp64 oracle on a bounded sample of the workload: forward and
+    backward of `n_rows` query rows of head 0 of batch 0 against all its keys.
+    Returns (tflops, seconds, cores, description)."""
+    import numpy as np
+
+    import oracle
+    from head_dim_flash_gb300 import workloads as W
+
+    inp = W.make_inputs(w)
+    g = w.Hq // w.Hkv
+    rows = min(n_rows, w.Nq)
+    q = inp["q"][0:1, 0:1, :rows]
+    k = inp["k"][0:1, 0:1]
+    v = inp["v"][0:1, 0:1]
+    do = inp["dO"][0:1, 0:1, :rows]
+    del g
+    oracle.build()
+    cores = oracle.num_threads()
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, False, w.scale)
+    oracle.attention_bwd(q, k, v, do, False, w.scale)
+    dt = time.perf_counter() - t0
+    f = 3.5 * 4.0 * rows * w.Nkv * w.D  # fwd + bwd counted flops of the sample
+    desc = (f"fwd+bwd of {rows} query rows x {w.Nkv} keys of head 0 (D={w.D}, non-causal sample), "
+            f"fp64 C oracle, OpenMP")
+    return f / dt / 1e12, dt, cores, desc
+
+
+def run_reference(args):
+    """The oracle timed as the reference arm (bounded sample per step)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workload(args.config)
+    import oracle
+
+    oracle.build()
+    rows = 128
+    times = []
+    for i in range(args.warmup + args.steps):
+        tf, dt, cores, desc = cpu_baseline(w, n_rows=rows)
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    f = 3.5 * 4.0 * rows * w.Nkv * w.D
+    value = f / (ms / 1e3) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": f"{rows} query rows of head 0"},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+
+    from head_dim_flash_gb300 import _ffi, api
+    from head_dim_flash_gb300 import workloads as W
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workload(args.config)
+    f_fwd, f_bwd = flops(w)
+    inp = W.make_inputs(w)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "dO"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(api.bwd_workspace_bytes(q, k), 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # per-kernel events: fwd | preprocess | dK/dV | dQ
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        api.fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
+        if ev is not None:
+            ev[1].record(stream)
+        api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=1)
+        if ev is not None:
+            ev[2].record(stream)
+        api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=2)
+        if ev is not None:
+            ev[3].record(stream)
+        api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=4)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    api.get_status()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            step(events[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    api.get_status()
+    total_ms = start.elapsed_time(end)
+    per = {"fwd": [], "preprocess": [], "dkdv": [], "dq": []}
+    for ev in events:
+        for name, a, b in (("fwd", 0, 1), ("preprocess", 1, 2), ("dkdv", 2, 3), ("dq", 3, 4)):
+            per[name].append(ev[a].elapsed_time(ev[b]))
+    per_ms = {n: statistics.mean(x) for n, x in per.items()}
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    fwd_ms = per_ms["fwd"]
+    bwd_ms = per_ms["preprocess"] + per_ms["dkdv"] + per_ms["dq"]
+    value = world * (f_fwd + f_bwd) / (ms_step / 1e3) / 1e12
+    pk = peaks()
+    clocks = clk.summary()
+
+    # roofline of the dominant kernel (largest time share); algorithmic flops
+    # per launch = the GEMMs its outputs require: fwd 2 (S, PV), dK/dV 4
+    # (S, dP, dV, dK), dQ 3 (S, dP, dQ), each 2*B*Hq*Nq*Nkv*D (halved causal)
+    gemm = f_fwd / 2.0
+    algo = {"fwd": 2 * gemm, "dkdv": 4 * gemm, "dq": 3 * gemm}
+    dom = max(algo, key=lambda n: per_ms[n])
+    achieved = algo[dom] / (per_ms[dom] / 1e3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None,
+            "peak_source": f"{pk['source']} sustained bf16 (timed inside a step)"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(w, args, dev, stream, inp, f_fwd + f_bwd, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, dt, cores, desc = cpu_baseline(w)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": desc, "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype.__repr__().endswith("bfloat16") else "fp16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nkv": w.Nkv, "D": w.D,
+                       "causal": w.causal, "l2": "inputs larger than L2 (each of q/k/v/dO > 129 MB)"
+                       if w.B * w.Hq * w.Nq * w.D * 2 > 129e6 else "inputs smaller than L2 (parity-size case)"},
+            "fwd": {"tflops": world * f_fwd / (fwd_ms / 1e3) / 1e12, "ms": fwd_ms,
+                    "pct_peak_burst": 100 * f_fwd / (fwd_ms / 1e3) / 1e12 / pk["bf16_tflops"]},
+            "bwd": {"tflops": world * f_bwd / (bwd_ms / 1e3) / 1e12, "ms": bwd_ms,
+                    "pct_peak_burst": 100 * f_bwd / (bwd_ms / 1e3) / 1e12 / pk["bf16_tflops"]},
+            "kernel_ms": per_ms,
+            "pct_peak_burst": 100 * value / world / pk["bf16_tflops"],
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": 4 * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_e2e(w, args, dev, stream, inp, step_flops, world):
+    """Same metric through the public API with pinned host buffers: every step
+    copies q, k, v, dO host->device and reads dq, dk, dv back."""
+    import torch
+
+    from head_dim_flash_gb300 import api
+
+    host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "dO")}
+    dev_t = {n: torch.empty_like(host[n], device=dev) for n in host}
+    out_h = {n: torch.empty(inp[src].shape, dtype=inp[src].dtype).pin_memory()
+             for n, src in (("dq", "q"), ("dk", "k"), ("dv", "v"))}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+
+    def step():
+        for n in host:
+            dev_t[n].copy_(host[n], non_blocking=True)
+        o, lse = api.fwd(dev_t["q"], dev_t["k"], dev_t["v"], w.causal, w.scale)
+        dq, dk, dv = api.bwd(dev_t["q"], dev_t["k"], dev_t["v"], o, lse, dev_t["dO"], w.causal, w.scale)
+        out_h["dq"].copy_(dq, non_blocking=True)
+        out_h["dk"].copy_(dk, non_blocking=True)
+        out_h["dv"].copy_(dv, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 5))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"value": world * step_flops / (ms / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    from head_dim_flash_gb300 import build
+
+    build.build()
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

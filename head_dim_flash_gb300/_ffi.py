@@ -21,6 +21,7 @@ EXPORTS = (
     "ffpa_fwd",
     "ffpa_bwd_workspace_bytes",
     "ffpa_bwd",
+    "ffpa_bwd_stages",
     "ffpa_varlen_fwd",
     "ffpa_varlen_bwd_workspace_bytes",
     "ffpa_varlen_bwd",
@@ -48,6 +49,9 @@ def _declare(lib):
     lib.ffpa_bwd_workspace_bytes.restype = _sz
     lib.ffpa_bwd.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _p]
     lib.ffpa_bwd.restype = _i
+    lib.ffpa_bwd_stages.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f,
+                                    ctypes.c_uint, _p]
+    lib.ffpa_bwd_stages.restype = _i
     lib.ffpa_varlen_fwd.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p]
     lib.ffpa_varlen_fwd.restype = _i
     lib.ffpa_varlen_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i]
@@ -114,6 +118,10 @@ def ffpa_bwd_workspace_bytes(*args):
 
 def ffpa_bwd(*args):
     return load().ffpa_bwd(*args)
+
+
+def ffpa_bwd_stages(*args):
+    return load().ffpa_bwd_stages(*args)
 
 
 def ffpa_varlen_fwd(*args):

@@ -75,8 +75,9 @@ def bwd_workspace_bytes(q, k) -> int:
 
 
 def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None,
-        dq=None, dk=None, dv=None):
-    """Dense backward through ffpa_bwd. Returns (dq, dk, dv)."""
+        dq=None, dk=None, dv=None, stages: int = 7):
+    """Dense backward through ffpa_bwd (or ffpa_bwd_stages for a subset of its
+    launches: bit 0 preprocess, bit 1 dK/dV, bit 2 dQ). Returns (dq, dk, dv)."""
     q, k, v, o, dout = _prep(q, k, v, o, dout)
     lse = lse.contiguous()
     B, Hq, Nq, D = q.shape
@@ -87,11 +88,16 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    st = _ffi.ffpa_bwd(_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                       dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                       B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D), _stream())
-    _ffi.raise_for(st, "ffpa_bwd")
+    args = (_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D))
+    if stages == 7:
+        st = _ffi.ffpa_bwd(*args, _stream())
+        _ffi.raise_for(st, "ffpa_bwd")
+    else:
+        st = _ffi.ffpa_bwd_stages(*args, int(stages), _stream())
+        _ffi.raise_for(st, "ffpa_bwd_stages")
     return dq, dk, dv
 
 

@@ -743,7 +743,7 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
     const long rows = pb.varlen ? static_cast<long>(pb.Hq) * pb.total_q : static_cast<long>(pb.B) * pb.Hq * pb.Nq;
     const bool q_empty = q_side_empty(pb), kv_empty = kv_side_empty(pb);
     cudaError_t e;
-    if (!q_empty) {
+    if (!q_empty && (a.stages & 1u)) {
         const int sms = num_sms() > 0 ? num_sms() : 148;
         long blocks = (rows + 7) / 8;
         const long cap = static_cast<long>(sms) * 8;
@@ -765,7 +765,7 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
         return cudaErrorInvalidValue;
     const int nd = pb.D / kChunk;
     // dK/dV: 128-column slabs
-    if (!kv_empty) {
+    if (!kv_empty && (a.stages & 2u)) {
         const int fixed = 1024 + 1024 + 131072;
         int stages = (kMaxSmem - fixed) / 16384;
         if (stages > kMaxStages) stages = kMaxStages;
@@ -779,7 +779,7 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // dQ: <= 256-column slabs
-    if (!q_empty) {
+    if (!q_empty && (a.stages & 4u)) {
         const int n_slabs = (nd + 3) / 4;
         const int slab_chunks = (nd + n_slabs - 1) / n_slabs;
         const int fixed = 1024 + 1024 + 65536;

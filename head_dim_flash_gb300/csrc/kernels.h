@@ -50,6 +50,7 @@ struct BwdArgs {
     void *dq, *dk, *dv;
     float* delta;      // workspace [rows] fp32: rowsum(dO * O)
     float* lse_log2;   // workspace [rows] fp32: LSE * log2(e), +inf for empty rows
+    unsigned stages;   // bit 0 preprocess, bit 1 dK/dV, bit 2 dQ
     DeviceCtl ctl;
 };
 

@@ -103,6 +103,21 @@ FFPA_API ffpa_status ffpa_bwd(ffpa_dtype dt, const void* q, const void* k, const
                      ffpa_stream_t stream);
 
 /*
+ * The three launches of ffpa_bwd, selectable: bit 0 = preprocess (delta and
+ * scaled LSE into the workspace), bit 1 = dK/dV, bit 2 = dQ. Stages run in
+ * that order on `stream`; the gradient stages read the workspace the
+ * preprocess stage wrote, so a caller that splits them issues bit 0 first
+ * (the FFPA docs' Triton page, "Configuration", describes the same split as
+ * separate dKdV and dQ launches). ffpa_bwd(...) == ffpa_bwd_stages(..., 7).
+ * Arguments otherwise as ffpa_bwd.
+ */
+FFPA_API ffpa_status ffpa_bwd_stages(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                     void* workspace, size_t workspace_bytes,
+                                     int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale,
+                                     unsigned stages, ffpa_stream_t stream);
+
+/*
  * Packed varlen forward (FFPA docs, CuTe-DSL Backend page, "Varlen (packed
  * THD) API"): sequences are packed along T; sequence b owns query rows
  * [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key rows

@@ -13,7 +13,7 @@ import torch
 import oracle
 from head_dim_flash_gb300 import api
 from head_dim_flash_gb300 import workloads
-from tests.gpu_utils import Guarded, check_grad, check_lse, check_o
+from tests.gpu_utils import Guarded, check_empty_rows_exact, check_grad, check_lse, check_o
 
 pytestmark = pytest.mark.gpu
 
@@ -28,8 +28,11 @@ def _lib():
     oracle.build()
 
 
-def run_dense(B, Hq, Hkv, Nq, Nkv, D, causal, dtype=torch.bfloat16, seed=0, amp=1.0, scale=None, backward=True):
+def run_dense(B, Hq, Hkv, Nq, Nkv, D, causal, dtype=torch.bfloat16, seed=0, amp=1.0, scale=None, backward=True,
+              v_amp=None):
     inp = workloads.random_dense(B, Hq, Hkv, Nq, Nkv, D, dtype, seed=seed, amplitude=amp)
+    if v_amp is not None:
+        inp["v"] = (inp["v"].float() * (v_amp / amp)).to(dtype)
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dO"))
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     og = Guarded(q.shape, dtype)
@@ -52,6 +55,9 @@ def run_dense(B, Hq, Hkv, Nq, Nkv, D, causal, dtype=torch.bfloat16, seed=0, amp=
     check_grad(dqg.t, dq_ref, "dQ")
     check_grad(dkg.t, dk_ref, "dK")
     check_grad(dvg.t, dv_ref, "dV")
+    empty = np.isneginf(lse_ref)
+    if empty.any():
+        check_empty_rows_exact(og.t, lg.t, dqg.t, empty)
 
 
 def test_tiny_config_full_parity():
@@ -95,9 +101,12 @@ def test_fp16_causal_gqa():
     run_dense(1, 4, 1, 257, 257, 320, True, dtype=torch.float16, seed=13, amp=0.5)
 
 
-def test_large_scores_trigger_rescaling():
-    # amplitude 3 and scale 1: scores of magnitude ~100 exercise the lazy O rescale
-    run_dense(1, 1, 1, 256, 1024, 128, False, seed=14, amp=3.0, scale=1.0)
+@pytest.mark.parametrize("causal", [False, True])
+def test_large_scores_trigger_rescaling(causal):
+    # q, k amplitude 3 and scale 1: scores of magnitude ~100 make the running
+    # row max jump by far more than 2^8 between key tiles, exercising the lazy
+    # O rescale; v keeps amplitude 1 so |O| stays where bf16 resolves 2e-2
+    run_dense(1, 2, 1, 256, 1024, 128, causal, seed=14, amp=3.0, scale=1.0, v_amp=1.0)
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -34,7 +34,7 @@ METRIC = "fwd & fwd+bwd TFLOPS, D=512 N=8192 bf16 (1×GB300), % of BF16 tensor p
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="headline")

@@ -22,6 +22,7 @@ EXPORTS = (
     "ffpa_bwd_workspace_bytes",
     "ffpa_bwd",
     "ffpa_bwd_stages",
+    "ffpa_bwd_noalloc",
     "ffpa_varlen_fwd",
     "ffpa_varlen_bwd_workspace_bytes",
     "ffpa_varlen_bwd",
@@ -52,6 +53,8 @@ def _declare(lib):
     lib.ffpa_bwd_stages.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f,
                                     ctypes.c_uint, _p]
     lib.ffpa_bwd_stages.restype = _i
+    lib.ffpa_bwd_noalloc.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p]
+    lib.ffpa_bwd_noalloc.restype = _i
     lib.ffpa_varlen_fwd.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p]
     lib.ffpa_varlen_fwd.restype = _i
     lib.ffpa_varlen_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i]
@@ -122,6 +125,10 @@ def ffpa_bwd(*args):
 
 def ffpa_bwd_stages(*args):
     return load().ffpa_bwd_stages(*args)
+
+
+def ffpa_bwd_noalloc(*args):
+    return load().ffpa_bwd_noalloc(*args)
 
 
 def ffpa_varlen_fwd(*args):

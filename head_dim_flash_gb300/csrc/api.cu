@@ -240,6 +240,17 @@ __global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns)
 
 }  // namespace
 
+int ffpa::set_error(int status, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return status;
+}
+
 extern "C" {
 
 ffpa_status ffpa_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

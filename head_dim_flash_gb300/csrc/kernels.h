@@ -72,6 +72,10 @@ inline bool kv_side_empty(const Problem& pb) { return pb.varlen ? pb.total_k == 
 
 int num_sms();
 
+// Records `fmt` as the thread's last-error message (ffpa_last_error) and
+// returns `status` (an ffpa_status value).
+int set_error(int status, const char* fmt, ...);
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
 

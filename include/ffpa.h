@@ -118,6 +118,28 @@ FFPA_API ffpa_status ffpa_bwd_stages(ffpa_dtype dt, const void* q, const void* k
                                      unsigned stages, ffpa_stream_t stream);
 
 /*
+ * Dense backward that allocates nothing and takes no workspace. The FFPA
+ * pages have no counterpart of this call; it exists for callers that cannot
+ * allocate device memory at all (a fixed, pre-planned memory pool with no
+ * spare buffer, a plugin host that owns every allocation, or a latency path
+ * where cudaMalloc would synchronise the device).
+ *   Arguments, layouts and results are those of ffpa_bwd without the
+ *   workspace pair. The scratch comes from a 4 MiB array inside the library's
+ *   device image, which holds B*Hq*Nq <= 524288 query rows; larger problems
+ *   return FFPA_ERR_INVALID_VALUE (use ffpa_bwd). Every GPU that loads the
+ *   library keeps that array until the process exits.
+ *   The first call on a device looks up the array's device address (once per
+ *   device); make that first call before any stream capture.
+ *   All calls on a device share the array: calls whose kernels overlap on the
+ *   GPU (unordered streams) race on it. Calls ordered on one stream do not;
+ *   nothing in the array needs to start at zero.
+ */
+FFPA_API ffpa_status ffpa_bwd_noalloc(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                      int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale,
+                                      ffpa_stream_t stream);
+
+/*
  * Packed varlen forward (FFPA docs, CuTe-DSL Backend page, "Varlen (packed
  * THD) API"): sequences are packed along T; sequence b owns query rows
  * [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key rows

@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--config", default="headline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override Hq=Hkv (profiling a smaller case of the same kernels)")
     return ap.parse_args()
 
 
@@ -209,6 +211,12 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workload(args.config)
+    if args.heads:
+        import dataclasses
+
+        g = w.Hq // w.Hkv
+        w = dataclasses.replace(w, name=w.name.replace(f"H{w.Hq}", f"H{args.heads}") + f" (heads={args.heads})",
+                                Hq=args.heads, Hkv=max(1, args.heads // g))
     f_fwd, f_bwd = flops(w)
     inp = W.make_inputs(w)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "dO"))

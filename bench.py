@@ -226,29 +226,26 @@ def run_ours(args):
     ws = torch.empty(max(api.bwd_workspace_bytes(q, k), 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    # per-kernel events: fwd | preprocess | dK/dV | dQ
+    # per-kernel events: fwd | preprocess | dV | dK | dQ (ffpa_bwd_stages bits 0, 1, 3, 2)
+    names = ("fwd", "preprocess", "dv", "dk", "dq")
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         api.fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
+        for i, bit in enumerate((1, 2, 8, 4)):
+            if ev is not None:
+                ev[i + 1].record(stream)
+            api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=bit)
         if ev is not None:
-            ev[1].record(stream)
-        api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=1)
-        if ev is not None:
-            ev[2].record(stream)
-        api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=2)
-        if ev is not None:
-            ev[3].record(stream)
-        api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=4)
-        if ev is not None:
-            ev[4].record(stream)
+            ev[5].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
     api.get_status()
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -264,10 +261,10 @@ def run_ours(args):
         torch.distributed.barrier()
     api.get_status()
     total_ms = start.elapsed_time(end)
-    per = {"fwd": [], "preprocess": [], "dkdv": [], "dq": []}
+    per = {n: [] for n in names}
     for ev in events:
-        for name, a, b in (("fwd", 0, 1), ("preprocess", 1, 2), ("dkdv", 2, 3), ("dq", 3, 4)):
-            per[name].append(ev[a].elapsed_time(ev[b]))
+        for i, n in enumerate(names):
+            per[n].append(ev[i].elapsed_time(ev[i + 1]))
     per_ms = {n: statistics.mean(x) for n, x in per.items()}
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -275,16 +272,16 @@ def run_ours(args):
         total_ms = float(t.item())
     ms_step = total_ms / args.steps
     fwd_ms = per_ms["fwd"]
-    bwd_ms = per_ms["preprocess"] + per_ms["dkdv"] + per_ms["dq"]
+    bwd_ms = per_ms["preprocess"] + per_ms["dv"] + per_ms["dk"] + per_ms["dq"]
     value = world * (f_fwd + f_bwd) / (ms_step / 1e3) / 1e12
     pk = peaks()
     clocks = clk.summary()
 
     # roofline of the dominant kernel (largest time share); algorithmic flops
-    # per launch = the GEMMs its outputs require: fwd 2 (S, PV), dK/dV 4
-    # (S, dP, dV, dK), dQ 3 (S, dP, dQ), each 2*B*Hq*Nq*Nkv*D (halved causal)
+    # per launch = the GEMMs its outputs require: fwd 2 (S, PV), dV 2 (S, dV),
+    # dK 3 (S, dP, dK), dQ 3 (S, dP, dQ), each 2*B*Hq*Nq*Nkv*D (halved causal)
     gemm = f_fwd / 2.0
-    algo = {"fwd": 2 * gemm, "dkdv": 4 * gemm, "dq": 3 * gemm}
+    algo = {"fwd": 2 * gemm, "dv": 2 * gemm, "dk": 3 * gemm, "dq": 3 * gemm}
     dom = max(algo, key=lambda n: per_ms[n])
     achieved = algo[dom] / (per_ms[dom] / 1e3) / 1e12
     peak = pk["bf16_tflops_sustained"]
@@ -317,7 +314,7 @@ def run_ours(args):
             "kernel_ms": per_ms,
             "pct_peak_burst": 100 * value / world / pk["bf16_tflops"],
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 5 * args.steps,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -75,9 +75,9 @@ def bwd_workspace_bytes(q, k) -> int:
 
 
 def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None,
-        dq=None, dk=None, dv=None, stages: int = 7):
+        dq=None, dk=None, dv=None, stages: int = 15):
     """Dense backward through ffpa_bwd (or ffpa_bwd_stages for a subset of its
-    launches: bit 0 preprocess, bit 1 dK/dV, bit 2 dQ). Returns (dq, dk, dv)."""
+    launches: bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK). Returns (dq, dk, dv)."""
     q, k, v, o, dout = _prep(q, k, v, o, dout)
     lse = lse.contiguous()
     B, Hq, Nq, D = q.shape
@@ -92,7 +92,7 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
             dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
             B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D))
-    if stages == 7:
+    if stages == 15:
         st = _ffi.ffpa_bwd(*args, _stream())
         _ffi.raise_for(st, "ffpa_bwd")
     else:

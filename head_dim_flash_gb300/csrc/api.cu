@@ -209,7 +209,7 @@ ffpa_status run_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, 
     a.dv = dv;
     a.delta = static_cast<float*>(workspace);
     a.lse_log2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + need / 2);
-    a.stages = stages & 7u;
+    a.stages = stages & 15u;
     return launch_result(ffpa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)), "backward launch");
 }
 
@@ -278,7 +278,7 @@ ffpa_status ffpa_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v,
     const long q_rows = static_cast<long>(B) * Hq * Nq;
     const long k_rows = static_cast<long>(B) * Hkv * Nkv;
     return run_bwd(dt, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes,
-                   dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, scale), q_rows, k_rows, q_rows, 7u, stream);
+                   dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, scale), q_rows, k_rows, q_rows, 15u, stream);
 }
 
 ffpa_status ffpa_bwd_stages(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
@@ -288,7 +288,7 @@ ffpa_status ffpa_bwd_stages(ffpa_dtype dt, const void* q, const void* k, const v
 {
     FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
     FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
-    if (stages > 7u) return fail(FFPA_ERR_INVALID_VALUE, "stages mask %u: only bits 0..2", stages);
+    if (stages > 15u) return fail(FFPA_ERR_INVALID_VALUE, "stages mask %u: only bits 0..3", stages);
     const long q_rows = static_cast<long>(B) * Hq * Nq;
     const long k_rows = static_cast<long>(B) * Hkv * Nkv;
     return run_bwd(dt, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes,
@@ -329,7 +329,7 @@ ffpa_status ffpa_varlen_bwd(ffpa_dtype dt, const void* q, const void* k, const v
     return run_bwd(dt, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes,
                    varlen_problem(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, causal, scale,
                                   cu_seqlens_q, cu_seqlens_k),
-                   q_rows, k_rows, q_rows, 7u, stream);
+                   q_rows, k_rows, q_rows, 15u, stream);
 }
 
 ffpa_status ffpa_get_status(ffpa_stream_t stream)

@@ -50,9 +50,26 @@ struct BwdArgs {
     void *dq, *dk, *dv;
     float* delta;      // workspace [rows] fp32: rowsum(dO * O)
     float* lse_log2;   // workspace [rows] fp32: LSE * log2(e), +inf for empty rows
-    unsigned stages;   // bit 0 preprocess, bit 1 dK/dV, bit 2 dQ
+    unsigned stages;   // bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK
     DeviceCtl ctl;
 };
+
+// The four GEMM kernels of the cluster-exchange design.
+enum XOp { XOP_FWD = 0, XOP_DQ = 1, XOP_DV = 2, XOP_DK = 3 };
+
+struct XArgs {
+    Problem pb;
+    int bf16;
+    const void *q, *k, *v, *dO;
+    void* o;
+    float* lse;                        // forward output
+    const float* delta;                // backward: rowsum(dO * O)
+    const float* lse_log2;             // backward: LSE * log2(e), +inf for empty rows
+    void *dq, *dk, *dv;
+    DeviceCtl ctl;
+};
+
+cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s);
 
 // Function pointer to the driver's cuTensorMapEncodeTiled (resolved once).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

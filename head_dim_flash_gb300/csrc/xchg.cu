@@ -1,0 +1,782 @@
+// Cluster-exchange kernels: the forward and the three backward GEMM kernels
+// (dV, dK, dQ) of exact attention at large head dim on sm_103a.
+//
+// Every kernel here has the same shape. A cluster of C CTAs owns one 128-row
+// tile of "rows" (queries for the forward and dQ, keys for dV and dK) and
+// walks over 128-wide tiles of "columns" (keys, resp. queries) in
+// super-steps of C tiles. In super-step s, CTA c
+//   1. computes the score tile(s) of column tile C*s + c with tcgen05 MMAs
+//      over the full head dim: X = S (and Y = dP for dQ / dK),
+//   2. turns them into one bf16/fp16 operand tile Z (P, P^T, dS or dS^T;
+//      the forward first exchanges row maxima with its peers so every CTA
+//      uses the same softmax reference),
+//   3. keeps Z in TMEM for itself and writes it into every peer's shared
+//      memory (DSMEM), and
+//   4. accumulates its own D-slab of the output over all C tiles of the
+//      super-step: acc += Z_{c'} W_{tile C*s+c'}[:, slab] for c' = 0..C-1
+//      (W = V, K, dO or Q), own Z read from TMEM, peers' Z from shared memory.
+// So each score product is computed once, while the fp32 accumulator of a
+// 128-row tile is split over C CTAs by head-dim slabs of <= 256 columns (a
+// 128 x 512 fp32 tile would fill all 512 TMEM columns of one SM).
+//
+// The pages this implements: FFPA docs, "CuTe-DSL Backend" page, "Hard
+// constraints" (bottom-right causal, GQA/MQA broadcast, empty rows give
+// O = 0, LSE = -inf and zero gradients), "Varlen (packed THD) API" (packed
+// layout, LSE [H, T]), "Blackwell status" (preprocess plus separate
+// gradient launches, split because one SM cannot hold a whole dK/dV tile).
+//
+// Warp roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
+// warps 2..5 elementwise (one tile row per thread) and epilogue.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_common.cuh"
+
+namespace ffpa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kStages = 16;      // upper bound of the TMA ring depth
+constexpr int kMaxC = 4;         // cluster size bound (D <= 1024 in 256-column slabs)
+constexpr float kTau = 8.0f;     // forward: rescale O only when the row max grows by more than 2^8
+constexpr float kLn2 = 0.693147180559945309f;
+
+enum Site : uint32_t {
+    XS_PROD = 32, XS_A1, XS_XFREE, XS_RING, XS_ZFULL, XS_ZPEER, XS_XFULL, XS_RMAX, XS_ACC, XS_SLOT, XS_STAT,
+    XS_LSUM, XS_EPI, XS_DRAIN
+};
+
+struct Geo {
+    int C;            // CTAs per cluster (= D-slabs)
+    int slab_chunks;  // 64-wide head-dim chunks per slab (the last slab may be smaller)
+    int stages;       // TMA ring depth
+    int res;          // first row operand resident in shared memory (D <= 512)
+};
+
+template <int OP>
+struct Traits {
+    static constexpr bool kTwo = (OP == XOP_DQ || OP == XOP_DK);      // X and Y score tiles
+    static constexpr bool kRowsQ = (OP == XOP_FWD || OP == XOP_DQ);   // rows are queries
+    static constexpr bool kXdb = !kTwo;                               // X double-buffered
+};
+
+// Barriers and flags live in one static block of exactly 1 KiB, so that the
+// dynamic shared memory right after it starts 1024-byte aligned (the 128-byte
+// swizzle of TMA tiles and MMA descriptors needs that); the kernel checks the
+// alignment at run time and reports an error instead of running misaligned.
+struct __align__(1024) StaticSmem {
+    uint64_t full[kStages], empty[kStages];
+    uint64_t a1, x_full[2], x_free[2], z_full, acc;
+    uint64_t zpeer[kMaxC], slot_free[kMaxC], stat[2], rmax[2], lsum, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(StaticSmem) == 1024, "static shared block must be exactly 1 KiB");
+
+// Bytes of the per-kernel statistics area (rounded to 1 KiB):
+//   forward: rmax[2][C-1][128] and lsum[C-1][128] (peer values, by slot)
+//   dV / dK: lse2[2][128] and delta[2][128] (column statistics, double-buffered)
+__host__ __device__ inline int stats_bytes(int op, int C)
+{
+    int b = 0;
+    if (op == XOP_FWD) b = 3 * (C > 1 ? C - 1 : 0) * 128 * 4;
+    else if (op == XOP_DV || op == XOP_DK) b = 4 * 128 * 4;
+    return (b + 1023) & ~1023;
+}
+
+template <int OP, bool BF16, bool VARLEN>
+__global__ void __launch_bounds__(kThreads, 1)
+    xchg_kernel(const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tA2,
+                const __grid_constant__ CUtensorMap tB1, const __grid_constant__ CUtensorMap tB2,
+                const __grid_constant__ CUtensorMap tW, const XArgs a, const Geo gm)
+{
+    using T = Traits<OP>;
+    const Problem& pb = a.pb;
+    const int C = gm.C;
+    const int c = static_cast<int>(cluster_ctarank());
+    const int G = pb.Hq / pb.Hkv;
+
+    // ------------------------------------------------------------ work unit
+    // All CTAs of a cluster share blockIdx.y / blockIdx.z, hence the same unit.
+    const int n_rt = gridDim.y;
+    const int bz = blockIdx.z;
+    int b, h = 0, hk;
+    if (T::kRowsQ) {
+        b = bz / pb.Hq;
+        h = bz % pb.Hq;
+        hk = h / G;
+    } else {
+        b = bz / pb.Hkv;
+        hk = bz % pb.Hkv;
+    }
+    int lq, lk, tq0 = 0, tk0 = 0;
+    if constexpr (VARLEN) {
+        tq0 = pb.cu_q[b];
+        lq = pb.cu_q[b + 1] - tq0;
+        tk0 = pb.cu_k[b];
+        lk = pb.cu_k[b + 1] - tk0;
+    } else {
+        lq = pb.Nq;
+        lk = pb.Nkv;
+    }
+    const int off = lk - lq;  // causal: key j legal for query i iff j <= i + off
+    const int rt = (T::kRowsQ && pb.causal) ? (n_rt - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
+    const int r0 = rt * 128;
+    const int row_len = T::kRowsQ ? lq : lk;
+    if (r0 >= row_len) return;  // uniform over the cluster, before any cluster barrier
+
+    int n_ct;            // column tiles of the unit
+    int m_start = 0, n_mt = 0;
+    if (T::kRowsQ) {
+        n_ct = (lk + 127) / 128;
+        if (pb.causal) {
+            const int kmax = min(r0 + 127, lq - 1) + off;
+            n_ct = kmax < 0 ? 0 : min(n_ct, kmax / 128 + 1);
+        }
+    } else {
+        if (pb.causal) m_start = max(0, r0 - off) / 128;
+        n_mt = max(0, (lq + 127) / 128 - m_start);
+        n_ct = G * n_mt;
+    }
+    const int n_steps = (n_ct + C - 1) / C;
+
+    const int nd = pb.D / 64;
+    const int c_begin = c * gm.slab_chunks;
+    const int nb = min(gm.slab_chunks, nd - c_begin);  // 64-wide blocks in my slab
+    const int sw = nb * 64;
+    const int d0 = c_begin * 64;
+
+    // ------------------------------------------------------------ shared memory
+    __shared__ StaticSmem sh;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t* sA1 = smem;                                    // resident row operand: nd x 16 KiB
+    uint8_t* sZ = sA1 + (gm.res ? nd * 16384 : 0);          // C-1 peer slots x 32 KiB
+    float* stats = reinterpret_cast<float*>(sZ + (C - 1) * 32768);
+    uint8_t* sRing = reinterpret_cast<uint8_t*>(stats) + stats_bytes(OP, C);
+    uint64_t* const bar_full = sh.full;
+    uint64_t* const bar_empty = sh.empty;
+    uint64_t& bar_a1 = sh.a1;
+    uint64_t* const bar_x_full = sh.x_full;
+    uint64_t* const bar_x_free = sh.x_free;
+    uint64_t& bar_z_full = sh.z_full;
+    uint64_t& bar_acc = sh.acc;
+    uint64_t* const bar_zpeer = sh.zpeer;
+    uint64_t* const bar_slot_free = sh.slot_free;
+    uint64_t* const bar_stat = sh.stat;
+    uint64_t* const bar_rmax = sh.rmax;
+    uint64_t& bar_lsum = sh.lsum;
+    uint64_t& bar_drain = sh.drain;
+    if (smem_u32(smem) & 1023u) {  // uniform over the block: report, do not run misaligned
+        if (threadIdx.x == 0) atomicCAS(a.ctl.status, 0u, 5u | (0xffu << 8));
+        return;
+    }
+
+    const int warp = threadIdx.x / 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < gm.stages; ++i) {
+            mbar_init(&bar_full[i], 1);
+            mbar_init(&bar_empty[i], 1);
+        }
+        mbar_init(&bar_a1, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_x_full[i], 1);
+            mbar_init(&bar_x_free[i], 1);
+            mbar_init(&bar_stat[i], 128);
+            mbar_init(&bar_rmax[i], 128 * (C > 1 ? C - 1 : 1));
+        }
+        mbar_init(&bar_z_full, 128);
+        mbar_init(&bar_acc, 1);
+        for (int i = 0; i < kMaxC; ++i) {
+            mbar_init(&bar_zpeer[i], 128);
+            mbar_init(&bar_slot_free[i], 1);
+        }
+        mbar_init(&bar_lsum, 128 * (C > 1 ? C - 1 : 1));
+        mbar_init(&bar_drain, 1);
+        sh.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    cluster_sync_all();  // every CTA's barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    const uint32_t t_acc = tmem;        // [0, 256): accumulator slab
+    const uint32_t t_x0 = tmem + 256;   // X buffers (and Y for the two-product kernels)
+    volatile int* abort_flag = &sh.abort_flag;
+    uint32_t* status = a.ctl.status;
+    const uint64_t lim = a.ctl.limit_ns;
+
+    // Peer bookkeeping: slot index of writer w inside consumer p's slot array.
+    auto slot_of = [&](int writer, int consumer) { return writer < consumer ? writer : writer - 1; };
+    uint16_t peer_mask = 0;
+    for (int p = 0; p < C; ++p)
+        if (p != c) peer_mask |= static_cast<uint16_t>(1u << p);
+
+    // Column tile t -> (head, first row) on the column side; t past the end is
+    // clamped for loading (its results are masked to zero).
+    auto col_head = [&](int t) { return T::kRowsQ ? hk : hk * G + min(t, n_ct - 1) / max(n_mt, 1); };
+    auto col_row0 = [&](int t) {
+        const int tc = min(t, n_ct - 1);
+        return T::kRowsQ ? tc * 128 : (m_start + tc % max(n_mt, 1)) * 128;
+    };
+    // TMA coordinates. Dense maps: (d, row, b*H + head); packed maps: (d, head, token).
+    auto q_c1 = [&](int head, int row) { return VARLEN ? head : row; };
+    auto q_c2 = [&](int head, int row) { return VARLEN ? tq0 + row : b * pb.Hq + head; };
+    auto k_c1 = [&](int head, int row) { return VARLEN ? head : row; };
+    auto k_c2 = [&](int head, int row) { return VARLEN ? tk0 + row : b * pb.Hkv + head; };
+    auto row_c1 = [&](int row) { return T::kRowsQ ? q_c1(h, row) : k_c1(hk, row); };
+    auto row_c2 = [&](int row) { return T::kRowsQ ? q_c2(h, row) : k_c2(hk, row); };
+    auto col_c1 = [&](int head, int row) { return T::kRowsQ ? k_c1(head, row) : q_c1(head, row); };
+    auto col_c2 = [&](int head, int row) { return T::kRowsQ ? k_c2(head, row) : q_c2(head, row); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (elect_one()) {
+            prefetch_tmap(&tA1);
+            prefetch_tmap(&tB1);
+            prefetch_tmap(&tW);
+            RingPos rp;
+            int issued = 0;
+            bool ok = true;
+            auto put = [&](const CUtensorMap* m, int boxes, int box_bytes, int x0, int y, int z) -> bool {
+                if (!mbar_wait(&bar_empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, XS_PROD)) return false;
+                uint8_t* dst = sRing + rp.slot * 16384;
+                mbar_arrive_expect_tx(&bar_full[rp.slot], boxes * box_bytes);
+                for (int i = 0; i < boxes; ++i) tma_load_3d(dst + i * box_bytes, m, &bar_full[rp.slot], x0 + i * 64, y, z);
+                rp.advance(gm.stages);
+                ++issued;
+                return true;
+            };
+            if (gm.res && n_steps > 0) {
+                mbar_arrive_expect_tx(&bar_a1, nd * 16384);
+                for (int d = 0; d < nd; ++d) tma_load_3d(sA1 + d * 16384, &tA1, &bar_a1, d * 64, row_c1(r0), row_c2(r0));
+            }
+            auto load_score = [&](int s) -> bool {
+                const int t = s * C + c;
+                const int hh = col_head(t), cr = col_row0(t);
+                for (int d = 0; d < nd; ++d) {
+                    if (!gm.res && !put(&tA1, 1, 16384, d * 64, row_c1(r0), row_c2(r0))) return false;
+                    if (!put(&tB1, 1, 16384, d * 64, col_c1(hh, cr), col_c2(hh, cr))) return false;
+                }
+                if (T::kTwo)
+                    for (int d = 0; d < nd; ++d) {
+                        if (!put(&tA2, 1, 16384, d * 64, row_c1(r0), row_c2(r0))) return false;
+                        if (!put(&tB2, 1, 16384, d * 64, col_c1(hh, cr), col_c2(hh, cr))) return false;
+                    }
+                return true;
+            };
+            auto load_value = [&](int s) -> bool {
+                for (int cc = 0; cc < C; ++cc) {
+                    const int t = s * C + cc;
+                    const int hh = col_head(t), cr = col_row0(t);
+                    for (int vc = 0; vc < 4; ++vc)
+                        if (!put(&tW, nb, 32 * 128, d0, col_c1(hh, cr + vc * 32), col_c2(hh, cr + vc * 32))) return false;
+                }
+                return true;
+            };
+            if (T::kXdb) {
+                if (n_steps > 0) ok = load_score(0);
+                for (int s = 0; ok && s < n_steps; ++s) {
+                    if (s + 1 < n_steps) ok = load_score(s + 1);
+                    if (ok) ok = load_value(s);
+                }
+            } else {
+                for (int s = 0; ok && s < n_steps; ++s) {
+                    ok = load_score(s);
+                    if (ok) ok = load_value(s);
+                }
+            }
+            const int last = min(issued, gm.stages);
+            RingPos dp = rp;
+            for (int i = 0; i < last; ++i) {
+                dp.retreat(gm.stages);
+                int dummy = 0;
+                mbar_wait(&bar_full[dp.slot], dp.phase, &dummy, status, lim, XS_DRAIN, false);
+            }
+            if (gm.res && n_steps > 0) {
+                int dummy = 0;
+                mbar_wait(&bar_a1, 0, &dummy, status, lim, XS_DRAIN, false);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (elect_one()) {
+            const uint32_t idesc_s = idesc_f16(128, 128, BF16, false, false);
+            const uint32_t idesc_v = idesc_f16(128, sw, BF16, false, true);
+            RingPos rp;
+            bool ok = true;
+            if (gm.res && n_steps > 0) {
+                ok = mbar_wait(&bar_a1, 0, abort_flag, status, lim, XS_A1);
+                tc_fence_after();
+            }
+            auto take = [&]() -> const uint8_t* {
+                if (!mbar_wait(&bar_full[rp.slot], rp.phase, abort_flag, status, lim, XS_RING)) return nullptr;
+                tc_fence_after();
+                return sRing + rp.slot * 16384;
+            };
+            auto give = [&](int slot) { umma_commit(&bar_empty[slot]); };
+            auto issue_score = [&](int s) -> bool {
+                const int sb = T::kXdb ? (s & 1) : 0;
+                if (T::kXdb ? s >= 2 : s >= 1) {
+                    const uint32_t par = T::kXdb ? (((s - 2) >> 1) & 1) : ((s - 1) & 1);
+                    if (!mbar_wait(&bar_x_free[sb], par, abort_flag, status, lim, XS_XFREE)) return false;
+                    tc_fence_after();
+                }
+                for (int prod = 0; prod < (T::kTwo ? 2 : 1); ++prod) {
+                    const uint32_t dst = t_x0 + (T::kXdb ? sb * 128 : prod * 128);
+                    for (int d = 0; d < nd; ++d) {
+                        const uint8_t* A;
+                        int a_slot = -1;
+                        if (prod == 0 && gm.res) {
+                            A = sA1 + d * 16384;
+                        } else {
+                            A = take();
+                            if (!A) return false;
+                            a_slot = rp.slot;
+                            rp.advance(gm.stages);
+                        }
+                        const uint8_t* B = take();
+                        if (!B) return false;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_f16(dst, sdesc_sw128(smem_u32(A + kk * 32), 16, 1024),
+                                     sdesc_sw128(smem_u32(B + kk * 32), 16, 1024), idesc_s, (d | kk) != 0);
+                        if (a_slot >= 0) give(a_slot);
+                        give(rp.slot);
+                        rp.advance(gm.stages);
+                    }
+                }
+                umma_commit(&bar_x_full[sb]);
+                return true;
+            };
+            auto issue_value = [&](int s) -> bool {
+                const int sb = T::kXdb ? (s & 1) : 0;
+                const uint32_t z_own = t_x0 + sb * 128;  // own Z: 64 packed columns at the start of X
+                if (!mbar_wait(&bar_z_full, s & 1, abort_flag, status, lim, XS_ZFULL)) return false;
+                for (int p = 0; p < C; ++p)
+                    if (p != c && !mbar_wait_cluster(&bar_zpeer[slot_of(p, c)], s & 1, abort_flag, status, lim, XS_ZPEER))
+                        return false;
+                tc_fence_after();
+                for (int cc = 0; cc < C; ++cc) {
+                    const uint8_t* zs = sZ + (cc == c ? 0 : slot_of(cc, c) * 32768);
+                    for (int vc = 0; vc < 4; ++vc) {
+                        const uint8_t* W = take();
+                        if (!W) return false;
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const int kt = vc * 32 + t * 16;
+                            const uint64_t bd = sdesc_sw128(smem_u32(W + t * 2048), 32 * 128, 1024);
+                            const uint32_t acc = (s | cc | vc | t) != 0;
+                            if (cc == c)
+                                umma_f16_tmem_a(t_acc, z_own + kt / 2, bd, idesc_v, acc);
+                            else
+                                umma_f16(t_acc, sdesc_sw128(smem_u32(zs + (kt / 64) * 16384 + (kt % 64) * 2), 16, 1024),
+                                         bd, idesc_v, acc);
+                        }
+                        give(rp.slot);
+                        rp.advance(gm.stages);
+                    }
+                }
+                umma_commit(&bar_acc);
+                umma_commit(&bar_x_free[sb]);
+                if (C > 1) umma_commit_multicast(&bar_slot_free[c], peer_mask);
+                return true;
+            };
+            if (T::kXdb) {
+                if (ok && n_steps > 0) ok = issue_score(0);
+                for (int s = 0; ok && s < n_steps; ++s) {
+                    if (s + 1 < n_steps) ok = issue_score(s + 1);
+                    if (ok) ok = issue_value(s);
+                }
+            } else {
+                for (int s = 0; ok && s < n_steps; ++s) {
+                    ok = issue_score(s);
+                    if (ok) ok = issue_value(s);
+                }
+            }
+            umma_commit(&bar_drain);
+            int dummy = 0;
+            mbar_wait(&bar_drain, 0, &dummy, status, lim, XS_DRAIN, false);
+        }
+    } else {
+        // ------------------------------------------------------ elementwise
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + static_cast<int>(lane_id());  // tile row = TMEM lane
+        const int tid = threadIdx.x - 64;                             // 0..127
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const float c2 = pb.scale_log2;
+        const int row = r0 + r;  // query (rows = queries) or key (rows = keys)
+        // rows = queries: legal keys [0, key_end); rows = keys: legal queries [i_min, lq)
+        const int key_end = pb.causal ? min(lk, row + off + 1) : lk;
+        const int i_min = pb.causal ? max(0, row - off) : 0;
+        const bool row_ok = row < row_len;
+        float l2_row = INFINITY, dl_row = 0.f;  // dQ: own row statistics
+        if (OP == XOP_DQ && row_ok) {
+            const size_t si = VARLEN ? static_cast<size_t>(h) * pb.total_q + tq0 + row
+                                     : (static_cast<size_t>(b) * pb.Hq + h) * pb.Nq + row;
+            l2_row = a.lse_log2[si];
+            dl_row = a.delta[si];
+        }
+        float m_ref = -INFINITY, l_part = 0.f;  // forward softmax state (l over own tiles)
+        bool ok = true;
+        auto warp_ok = [&](bool v) { return __all_sync(0xffffffffu, v); };
+        for (int s = 0; s < n_steps; ++s) {
+            const int t = s * C + c;
+            const int sb = T::kXdb ? (s & 1) : 0;
+            const uint32_t tx = t_x0 + sb * 128 + lane_off;
+            const uint32_t ty = t_x0 + 128 + lane_off;  // Y (two-product kernels)
+            const int sbuf = s & 1;
+            if (!T::kRowsQ) {
+                // stage the column statistics of tile t: +inf lse2 masks queries
+                // past the sequence and tiles past the end
+                const int qi = col_row0(t) + tid;
+                const int hh = col_head(t);
+                float l2 = INFINITY, dl = 0.f;
+                if (t < n_ct && qi < lq) {
+                    const size_t si = VARLEN ? static_cast<size_t>(hh) * pb.total_q + tq0 + qi
+                                             : (static_cast<size_t>(b) * pb.Hq + hh) * pb.Nq + qi;
+                    l2 = a.lse_log2[si];
+                    dl = a.delta[si];
+                }
+                stats[sbuf * 128 + tid] = l2;          // lse2[sbuf][tid]
+                stats[256 + sbuf * 128 + tid] = dl;    // delta[sbuf][tid]
+                mbar_arrive(&bar_stat[sbuf]);
+            }
+            const uint32_t xpar = T::kXdb ? ((s >> 1) & 1) : (s & 1);
+            if (!warp_ok(mbar_wait(&bar_x_full[sb], xpar, abort_flag, status, lim, XS_XFULL))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (!T::kRowsQ && !warp_ok(mbar_wait(&bar_stat[sbuf], (s >> 1) & 1, abort_flag, status, lim, XS_STAT))) {
+                ok = false;
+                break;
+            }
+            // Writes packed Z units [u0, u0+n) of this row: own copy to TMEM by the
+            // caller, peer copies into every peer's slot (K-major, 128-byte swizzle).
+            auto wait_slots = [&]() -> bool {
+                if (C == 1 || s == 0) return true;
+                bool got = true;
+                for (int p = 0; p < C && got; ++p)
+                    if (p != c) got = mbar_wait_cluster(&bar_slot_free[p], (s - 1) & 1, abort_flag, status, lim, XS_SLOT);
+                return warp_ok(got);
+            };
+            auto to_peers = [&](const uint32_t* zz, int u0, int n) {
+                for (int p = 0; p < C; ++p) {
+                    if (p == c) continue;
+                    const uint32_t base = mapa_shared(smem_u32(sZ + slot_of(c, p) * 32768), p);
+                    for (int k = 0; k < n; ++k) {
+                        const int u = u0 + k;
+                        st_cluster_u4(base + (u >> 3) * 16384 + sw128_offset(r, u & 7),
+                                      make_uint4(zz[4 * k], zz[4 * k + 1], zz[4 * k + 2], zz[4 * k + 3]));
+                    }
+                }
+            };
+            if constexpr (OP == XOP_FWD) {
+                uint32_t z[64];  // the row of P as packed pairs
+                uint32_t x[128];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tx + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[q4 * 32]));
+                tmem_ld_wait(x);
+                const int limit = key_end - t * 128;  // legal columns [0, limit)
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 128; ++j)
+                    if (j < limit) mx = fmaxf(mx, __uint_as_float(x[j]));
+                float m_tile = mx * c2;
+                if (C > 1) {
+                    // exchange row maxima so every CTA of the cluster uses one reference:
+                    // rmax[sbuf][slot][r] at stats + (sbuf*(C-1) + slot)*128 + r
+                    for (int p = 0; p < C; ++p) {
+                        if (p == c) continue;
+                        float* dst = stats + (sbuf * (C - 1) + slot_of(c, p)) * 128 + r;
+                        st_cluster_f32(mapa_shared(smem_u32(dst), p), m_tile);
+                    }
+                    for (int p = 0; p < C; ++p)
+                        if (p != c) mbar_arrive_remote(mapa_shared(smem_u32(&bar_rmax[sbuf]), p));
+                    if (!warp_ok(mbar_wait_cluster(&bar_rmax[sbuf], (s >> 1) & 1, abort_flag, status, lim, XS_RMAX))) {
+                        ok = false;
+                        break;
+                    }
+                    for (int q = 0; q < C - 1; ++q) m_tile = fmaxf(m_tile, stats[(sbuf * (C - 1) + q) * 128 + r]);
+                }
+                float new_ref = m_ref;
+                bool need = false;
+                if (m_tile > -INFINITY) {
+                    if (m_ref == -INFINITY) {
+                        new_ref = m_tile;
+                    } else if (m_tile > m_ref + kTau) {
+                        new_ref = m_tile;
+                        need = true;
+                    }
+                }
+                const float alpha = need ? ex2_approx(m_ref - new_ref) : 1.f;
+                if (__any_sync(0xffffffffu, need)) {
+                    // O must be stable: wait for the previous super-step's value MMAs
+                    if (s > 0 && !warp_ok(mbar_wait(&bar_acc, (s - 1) & 1, abort_flag, status, lim, XS_ACC))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int cc = 0; cc < sw; cc += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(t_acc + lane_off + cc, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(t_acc + lane_off + cc, o);
+                    }
+                    tmem_st_wait();
+                }
+                l_part *= alpha;
+                m_ref = new_ref;
+                const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+                float sum = 0.f;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    const int j = 2 * e;
+                    const float p0 = (j < limit) ? ex2_approx(__uint_as_float(x[j]) * c2 - mu) : 0.f;
+                    const float p1 = (j + 1 < limit) ? ex2_approx(__uint_as_float(x[j + 1]) * c2 - mu) : 0.f;
+                    sum += p0 + p1;
+                    z[e] = pack2<BF16>(p0, p1);
+                }
+                l_part += sum;
+                // own P -> TMEM (start of the X buffer; every X column it overwrites is read)
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    tmem_st16(tx + q4 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&z[q4 * 16]));
+                if (!wait_slots()) {
+                    ok = false;
+                    break;
+                }
+                if (C > 1) to_peers(z, 0, 16);
+            } else {
+                // one 32-column chunk at a time: Z of chunk q4 goes to TMEM columns
+                // [16*q4, 16*q4+16), all of which were read before
+                if (!wait_slots()) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll 1
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t x[32], y[32], z[16];
+                    tmem_ld32(tx + q4 * 32, x);
+                    if (T::kTwo) tmem_ld32(ty + q4 * 32, y);
+                    tmem_ld_wait(x);
+                    if (T::kTwo) tmem_ld_wait(y);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float zz[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int j = q4 * 32 + 2 * e + u;
+                            const float sv = __uint_as_float(x[2 * e + u]);
+                            float p, v;
+                            if (T::kRowsQ) {  // dQ: row = query, column = key
+                                const bool legal = (t * 128 + j) < key_end;
+                                p = legal ? ex2_approx(sv * c2 - l2_row) : 0.f;
+                                v = p * (__uint_as_float(y[2 * e + u]) - dl_row);
+                            } else {  // dV / dK: row = key, column = query
+                                const int qi = col_row0(t) + j;
+                                const bool legal = row_ok && qi >= i_min;
+                                p = legal ? ex2_approx(sv * c2 - stats[sbuf * 128 + j]) : 0.f;
+                                v = (OP == XOP_DK) ? p * (__uint_as_float(y[2 * e + u]) - stats[256 + sbuf * 128 + j])
+                                                   : p;
+                            }
+                            zz[u] = v;
+                        }
+                        z[e] = pack2<BF16>(zz[0], zz[1]);
+                    }
+                    tmem_st16(tx + q4 * 16, z);
+                    if (C > 1) to_peers(z, q4 * 4, 4);
+                }
+            }
+            if (C > 1) fence_proxy_async_cluster();
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar_z_full);
+            for (int p = 0; p < C; ++p)
+                if (p != c) mbar_arrive_remote(mapa_shared(smem_u32(&bar_zpeer[slot_of(c, p)]), p));
+        }
+        // ------------------------------------------------------ epilogue
+        if (ok && n_steps > 0) {
+            ok = warp_ok(mbar_wait(&bar_acc, (n_steps - 1) & 1, abort_flag, status, lim, XS_EPI));
+            tc_fence_after();
+        }
+        float l_tot = l_part;
+        if (OP == XOP_FWD && ok && n_steps > 0 && C > 1) {
+            // lsum[slot][r] at stats + (2*(C-1) + slot)*128 + r
+            for (int p = 0; p < C; ++p)
+                if (p != c) {
+                    float* dst = stats + (2 * (C - 1) + slot_of(c, p)) * 128 + r;
+                    st_cluster_f32(mapa_shared(smem_u32(dst), p), l_part);
+                }
+            for (int p = 0; p < C; ++p)
+                if (p != c) mbar_arrive_remote(mapa_shared(smem_u32(&bar_lsum), p));
+            ok = warp_ok(mbar_wait_cluster(&bar_lsum, 0, abort_flag, status, lim, XS_LSUM));
+            for (int q = 0; q < C - 1; ++q) l_tot += stats[(2 * (C - 1) + q) * 128 + r];
+        }
+        if (ok) {
+            float mul;
+            void* out;
+            int out_heads, out_n, t0, head;
+            if (OP == XOP_FWD) {
+                mul = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                out = a.o;
+            } else if (OP == XOP_DQ) {
+                mul = pb.scale;
+                out = a.dq;
+            } else if (OP == XOP_DV) {
+                mul = 1.f;
+                out = a.dv;
+            } else {
+                mul = pb.scale;
+                out = a.dk;
+            }
+            if (T::kRowsQ) {
+                out_heads = pb.Hq;
+                out_n = pb.Nq;
+                t0 = tq0;
+                head = h;
+            } else {
+                out_heads = pb.Hkv;
+                out_n = pb.Nkv;
+                t0 = tk0;
+                head = hk;
+            }
+            const size_t orow = VARLEN ? (static_cast<size_t>(t0 + row) * out_heads + head) * pb.D
+                                       : ((static_cast<size_t>(b) * out_heads + head) * out_n + row) * pb.D;
+            uint16_t* dst = reinterpret_cast<uint16_t*>(out) + orow + d0;
+            for (int cc = 0; cc < sw; cc += 32) {
+                uint32_t v[32];
+                if (n_steps > 0) {
+                    tmem_ld32(t_acc + lane_off + cc, v);
+                    tmem_ld_wait(v);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                if (row_ok) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                }
+            }
+            if (OP == XOP_FWD && c == 0 && row_ok) {
+                const float lse = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
+                const size_t li = VARLEN ? static_cast<size_t>(h) * pb.total_q + tq0 + row
+                                         : (static_cast<size_t>(b) * pb.Hq + h) * pb.Nq + row;
+                a.lse[li] = lse;
+            }
+        }
+    }
+
+    // -------------------------------------------------------------- teardown
+    // No CTA leaves while a peer may still write into its shared memory.
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int OP, bool BF16, bool VARLEN>
+cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const Geo& gm, int n_rt, int bz, int smem,
+                      cudaStream_t s)
+{
+    auto kern = xchg_kernel<OP, BF16, VARLEN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gm.C, n_rt, bz);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = gm.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], a, gm);
+}
+
+template <int OP>
+cudaError_t dispatch(const XArgs& a, const CUtensorMap* maps, const Geo& gm, int n_rt, int bz, int smem,
+                     cudaStream_t s)
+{
+    if (a.bf16) return a.pb.varlen ? launch_op<OP, true, true>(a, maps, gm, n_rt, bz, smem, s)
+                                   : launch_op<OP, true, false>(a, maps, gm, n_rt, bz, smem, s);
+    return a.pb.varlen ? launch_op<OP, false, true>(a, maps, gm, n_rt, bz, smem, s)
+                       : launch_op<OP, false, false>(a, maps, gm, n_rt, bz, smem, s);
+}
+
+}  // namespace
+
+cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
+{
+    const Problem& pb = a.pb;
+    const bool q_empty = q_side_empty(pb), kv_empty = kv_side_empty(pb);
+    const bool rows_q = (op == XOP_FWD || op == XOP_DQ);
+    if (rows_q ? q_empty : kv_empty) return cudaSuccess;  // no output rows
+    const int nd = pb.D / 64;
+    Geo gm;
+    gm.C = (nd + 3) / 4;
+    gm.slab_chunks = (nd + gm.C - 1) / gm.C;
+    gm.res = pb.D <= 512 ? 1 : 0;
+    const int fixed = (gm.res ? nd * 16384 : 0) + (gm.C - 1) * 32768 + stats_bytes(op, gm.C);
+    gm.stages = (kMaxSmem - static_cast<int>(sizeof(StaticSmem)) - fixed) / 16384;
+    if (gm.stages > kStages) gm.stages = kStages;
+    if (gm.stages < 2) return cudaErrorInvalidConfiguration;
+    const int smem = fixed + gm.stages * 16384;
+
+    // maps: A1, A2 (row side, 128-row boxes), B1, B2 (column side, 128-row boxes), W (32-row boxes)
+    const void* qp = q_empty ? a.k : a.q;
+    const void* dop = q_empty ? a.k : (a.dO ? a.dO : a.q);
+    const void* kp = kv_empty ? a.q : a.k;
+    const void* vp = kv_empty ? a.q : a.v;
+    const bool qs = !q_empty ? false : true;  // side flag of the q-side maps (kv side when q is empty)
+    const bool ks = !kv_empty;                // side flag of the kv-side maps
+    CUtensorMap m[5];
+    bool okm = true;
+    auto mk = [&](int i, const void* p, bool kv_side, int rows) { okm = okm && make_row_map(&m[i], p, pb, kv_side, a.bf16, rows); };
+    int n_rt, bz;
+    switch (op) {
+    case XOP_FWD:
+        mk(0, qp, qs, 128); mk(1, qp, qs, 128); mk(2, kp, ks, 128); mk(3, kp, ks, 128); mk(4, vp, ks, 32);
+        n_rt = (pb.Nq + 127) / 128; bz = pb.B * pb.Hq;
+        break;
+    case XOP_DQ:
+        mk(0, qp, qs, 128); mk(1, dop, qs, 128); mk(2, kp, ks, 128); mk(3, vp, ks, 128); mk(4, kp, ks, 32);
+        n_rt = (pb.Nq + 127) / 128; bz = pb.B * pb.Hq;
+        break;
+    case XOP_DV:
+        mk(0, kp, ks, 128); mk(1, kp, ks, 128); mk(2, qp, qs, 128); mk(3, qp, qs, 128); mk(4, dop, qs, 32);
+        n_rt = (pb.Nkv + 127) / 128; bz = pb.B * pb.Hkv;
+        break;
+    default:  // XOP_DK
+        mk(0, kp, ks, 128); mk(1, vp, ks, 128); mk(2, qp, qs, 128); mk(3, dop, qs, 128); mk(4, qp, qs, 32);
+        n_rt = (pb.Nkv + 127) / 128; bz = pb.B * pb.Hkv;
+        break;
+    }
+    if (!okm) return cudaErrorInvalidValue;
+    if (n_rt == 0 || bz == 0) return cudaSuccess;
+    switch (op) {
+    case XOP_FWD: return dispatch<XOP_FWD>(a, m, gm, n_rt, bz, smem, s);
+    case XOP_DQ: return dispatch<XOP_DQ>(a, m, gm, n_rt, bz, smem, s);
+    case XOP_DV: return dispatch<XOP_DV>(a, m, gm, n_rt, bz, smem, s);
+    default: return dispatch<XOP_DK>(a, m, gm, n_rt, bz, smem, s);
+    }
+}
+
+}  // namespace ffpa

@@ -89,8 +89,8 @@ FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, 
 /*
  * Dense backward (FFPA docs, CuTe-DSL Backend page, "Blackwell status": a
  * preprocess launch followed by gradient launches; gradients are returned in
- * the input dtype, "Configuration"). Runs three kernels in stream order:
- * delta = rowsum(dO * O), then dK/dV, then dQ.
+ * the input dtype, "Configuration"). Runs four kernels in stream order:
+ * delta = rowsum(dO * O), then dV, dK and dQ.
  *   q, o, dO, dq : [B, Hq, Nq, D];  k, v, dk, dv : [B, Hkv, Nkv, D]
  *   lse : [B, Hq, Nq] fp32 as written by ffpa_fwd for the same inputs.
  *   workspace : device scratch of >= ffpa_bwd_workspace_bytes() bytes,
@@ -103,12 +103,12 @@ FFPA_API ffpa_status ffpa_bwd(ffpa_dtype dt, const void* q, const void* k, const
                      ffpa_stream_t stream);
 
 /*
- * The three launches of ffpa_bwd, selectable: bit 0 = preprocess (delta and
- * scaled LSE into the workspace), bit 1 = dK/dV, bit 2 = dQ. Stages run in
- * that order on `stream`; the gradient stages read the workspace the
- * preprocess stage wrote, so a caller that splits them issues bit 0 first
- * (the FFPA docs' Triton page, "Configuration", describes the same split as
- * separate dKdV and dQ launches). ffpa_bwd(...) == ffpa_bwd_stages(..., 7).
+ * The launches of ffpa_bwd, selectable: bit 0 = preprocess (delta and scaled
+ * LSE into the workspace), bit 1 = dV, bit 2 = dQ, bit 3 = dK. Stages run in
+ * the order preprocess, dV, dK, dQ on `stream`; the gradient stages read the
+ * workspace the preprocess stage wrote, so a caller that splits them issues
+ * bit 0 first (the FFPA docs' CuTe-DSL page, "Blackwell status", describes the
+ * same four launches). ffpa_bwd(...) == ffpa_bwd_stages(..., 15).
  * Arguments otherwise as ffpa_bwd.
  */
 FFPA_API ffpa_status ffpa_bwd_stages(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,

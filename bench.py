@@ -87,6 +87,23 @@ def dist_setup(n_gpus):
     return rank, world, local
 
 
+def slowest_rank_ms(ms: float, world: int, device="cpu") -> float:
+    """Max over ranks of a timed region (ms): the whole job is as fast as its slowest rank."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(per_rank_flops: float, world: int, ms: float) -> float:
+    """Weak scaling: every rank runs the same per-GPU work; value = all ranks' FLOPs / slowest time."""
+    return world * per_rank_flops / (ms / 1e3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -266,14 +283,11 @@ def run_ours(args):
         for i, n in enumerate(names):
             per[n].append(ev[i].elapsed_time(ev[i + 1]))
     per_ms = {n: statistics.mean(x) for n, x in per.items()}
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(total_ms, world, dev)
     ms_step = total_ms / args.steps
     fwd_ms = per_ms["fwd"]
     bwd_ms = per_ms["preprocess"] + per_ms["dv"] + per_ms["dk"] + per_ms["dq"]
-    value = world * (f_fwd + f_bwd) / (ms_step / 1e3) / 1e12
+    value = job_throughput(f_fwd + f_bwd, world, ms_step)
     pk = peaks()
     clocks = clk.summary()
 

@@ -179,6 +179,22 @@ __device__ __forceinline__ void st_cluster_u4(uint32_t addr, uint4 v)
                  : "memory");
 }
 
+// Asynchronous stores into another CTA's shared memory that complete their
+// byte count on an mbarrier of that CTA (which must be armed with expect_tx).
+__device__ __forceinline__ void st_async_u4(uint32_t addr, uint4 v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");

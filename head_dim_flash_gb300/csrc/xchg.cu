@@ -181,17 +181,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_x_full[i], 1);
             mbar_init(&bar_x_free[i], 1);
             mbar_init(&bar_stat[i], 128);
-            mbar_init(&bar_rmax[i], 128 * (C > 1 ? C - 1 : 1));
+            mbar_init(&bar_rmax[i], 1);
         }
         mbar_init(&bar_z_full, 128);
         mbar_init(&bar_acc, 1);
         for (int i = 0; i < kMaxC; ++i) {
-            mbar_init(&bar_zpeer[i], 128);
+            mbar_init(&bar_zpeer[i], 1);
             mbar_init(&bar_slot_free[i], 1);
         }
-        mbar_init(&bar_lsum, 128 * (C > 1 ? C - 1 : 1));
+        mbar_init(&bar_lsum, 1);
         mbar_init(&bar_drain, 1);
         sh.abort_flag = 0;
+        // Peers deliver with st.async, completing bytes on these barriers; each is
+        // armed (one arrival + expected bytes) by its receiver before any peer can
+        // write the phase it guards: here for the first phase (the first two for
+        // the double-buffered row maxima), later right after each completed wait.
+        if (C > 1) {
+            for (int i = 0; i < C - 1; ++i) mbar_arrive_expect_tx(&bar_zpeer[i], 32768);
+            if (OP == XOP_FWD) {
+                mbar_arrive_expect_tx(&bar_rmax[0], 512 * (C - 1));
+                mbar_arrive_expect_tx(&bar_rmax[1], 512 * (C - 1));
+                mbar_arrive_expect_tx(&bar_lsum, 512 * (C - 1));
+            }
+        }
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -356,8 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t z_own = t_x0 + sb * 128;  // own Z: 64 packed columns at the start of X
                 if (!mbar_wait(&bar_z_full, s & 1, abort_flag, status, lim, XS_ZFULL)) return false;
                 for (int p = 0; p < C; ++p)
-                    if (p != c && !mbar_wait_cluster(&bar_zpeer[slot_of(p, c)], s & 1, abort_flag, status, lim, XS_ZPEER))
-                        return false;
+                    if (p != c) {
+                        if (!mbar_wait_cluster(&bar_zpeer[slot_of(p, c)], s & 1, abort_flag, status, lim, XS_ZPEER))
+                            return false;
+                        // arm the next phase before this step's slot_free lets the peer write it
+                        mbar_arrive_expect_tx(&bar_zpeer[slot_of(p, c)], 32768);
+                    }
+                fence_proxy_async_smem();
                 tc_fence_after();
                 for (int cc = 0; cc < C; ++cc) {
                     const uint8_t* zs = sZ + (cc == c ? 0 : slot_of(cc, c) * 32768);
@@ -467,10 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int p = 0; p < C; ++p) {
                     if (p == c) continue;
                     const uint32_t base = mapa_shared(smem_u32(sZ + slot_of(c, p) * 32768), p);
+                    const uint32_t rbar = mapa_shared(smem_u32(&bar_zpeer[slot_of(c, p)]), p);
                     for (int k = 0; k < n; ++k) {
                         const int u = u0 + k;
-                        st_cluster_u4(base + (u >> 3) * 16384 + sw128_offset(r, u & 7),
-                                      make_uint4(zz[4 * k], zz[4 * k + 1], zz[4 * k + 2], zz[4 * k + 3]));
+                        st_async_u4(base + (u >> 3) * 16384 + sw128_offset(r, u & 7),
+                                    make_uint4(zz[4 * k], zz[4 * k + 1], zz[4 * k + 2], zz[4 * k + 3]), rbar);
                     }
                 }
             };
@@ -492,14 +510,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int p = 0; p < C; ++p) {
                         if (p == c) continue;
                         float* dst = stats + (sbuf * (C - 1) + slot_of(c, p)) * 128 + r;
-                        st_cluster_f32(mapa_shared(smem_u32(dst), p), m_tile);
+                        st_async_f32(mapa_shared(smem_u32(dst), p), m_tile, mapa_shared(smem_u32(&bar_rmax[sbuf]), p));
                     }
-                    for (int p = 0; p < C; ++p)
-                        if (p != c) mbar_arrive_remote(mapa_shared(smem_u32(&bar_rmax[sbuf]), p));
                     if (!warp_ok(mbar_wait_cluster(&bar_rmax[sbuf], (s >> 1) & 1, abort_flag, status, lim, XS_RMAX))) {
                         ok = false;
                         break;
                     }
+                    // re-arm this buffer for step s+2: no peer writes it before every
+                    // thread here has sent its step s+1 maximum
+                    if (tid == 0) mbar_arrive_expect_tx(&bar_rmax[sbuf], 512 * (C - 1));
                     for (int q = 0; q < C - 1; ++q) m_tile = fmaxf(m_tile, stats[(sbuf * (C - 1) + q) * 128 + r]);
                 }
                 float new_ref = m_ref;
@@ -593,12 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (C > 1) to_peers(z, q4 * 4, 4);
                 }
             }
-            if (C > 1) fence_proxy_async_cluster();
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar_z_full);
-            for (int p = 0; p < C; ++p)
-                if (p != c) mbar_arrive_remote(mapa_shared(smem_u32(&bar_zpeer[slot_of(c, p)]), p));
         }
         // ------------------------------------------------------ epilogue
         if (ok && n_steps > 0) {
@@ -611,10 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int p = 0; p < C; ++p)
                 if (p != c) {
                     float* dst = stats + (2 * (C - 1) + slot_of(c, p)) * 128 + r;
-                    st_cluster_f32(mapa_shared(smem_u32(dst), p), l_part);
+                    st_async_f32(mapa_shared(smem_u32(dst), p), l_part, mapa_shared(smem_u32(&bar_lsum), p));
                 }
-            for (int p = 0; p < C; ++p)
-                if (p != c) mbar_arrive_remote(mapa_shared(smem_u32(&bar_lsum), p));
             ok = warp_ok(mbar_wait_cluster(&bar_lsum, 0, abort_flag, status, lim, XS_LSUM));
             for (int q = 0; q < C - 1; ++q) l_tot += stats[(2 * (C - 1) + q) * 128 + r];
         }

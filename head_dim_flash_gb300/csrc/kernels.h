@@ -81,6 +81,10 @@ EncodeTiledFn encode_fn();
 // Box = 64 head-dim elements x `box_rows` rows, 128-byte swizzle.
 bool make_row_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int box_rows);
 
+// Tensor map reading `rows` rows x `chunks` 64-wide head-dim chunks in one box
+// (shared-memory layout [chunk][row][64], 128-byte swizzle).
+bool make_slab_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int rows, int chunks);
+
 // True when the query side / key side of a problem has no rows at all. Such a
 // side has no storage; tensor maps for it are built over the other side's
 // tensor (never loaded from, because every tile loop is empty).

@@ -57,6 +57,10 @@ struct Traits {
     static constexpr bool kTwo = (OP == XOP_DQ || OP == XOP_DK);      // X and Y score tiles
     static constexpr bool kRowsQ = (OP == XOP_FWD || OP == XOP_DQ);   // rows are queries
     static constexpr bool kXdb = !kTwo;                               // X double-buffered
+    // Two-product kernels keep their own Z in a shared-memory slot, so X and Y
+    // are free as soon as the elementwise warps have read them and the next
+    // score products overlap this step's elementwise and value work.
+    static constexpr bool kOwnSlot = kTwo;
 };
 
 // Barriers and flags live in one static block of exactly 1 KiB, so that the
@@ -149,8 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ StaticSmem sh;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* sA1 = smem;                                    // resident row operand: nd x 16 KiB
-    uint8_t* sZ = sA1 + (gm.res ? nd * 16384 : 0);          // C-1 peer slots x 32 KiB
-    float* stats = reinterpret_cast<float*>(sZ + (C - 1) * 32768);
+    uint8_t* sZ = sA1 + (gm.res ? nd * 16384 : 0);          // C-1 peer slots (+ own slot) x 32 KiB
+    const int n_slots = T::kOwnSlot ? C : C - 1;
+    uint8_t* sZown = sZ + (C - 1) * 32768;                  // own slot (two-product kernels)
+    float* stats = reinterpret_cast<float*>(sZ + n_slots * 32768);
     uint8_t* sRing = reinterpret_cast<uint8_t*>(stats) + stats_bytes(OP, C);
     uint64_t* const bar_full = sh.full;
     uint64_t* const bar_empty = sh.empty;
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_a1, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_x_full[i], 1);
-            mbar_init(&bar_x_free[i], 1);
+            mbar_init(&bar_x_free[i], T::kOwnSlot ? 128 : 1);
             mbar_init(&bar_stat[i], 128);
             mbar_init(&bar_rmax[i], 1);
         }
@@ -279,26 +285,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 return true;
             };
+            // value operand: one 4-D box = 32 rows x my slab's 64-wide chunks (chunks past
+            // the head dim of a narrower last slab read as zero and are not used)
+            const int wbytes = 32 * 128 * gm.slab_chunks;
             auto load_value = [&](int s) -> bool {
                 for (int cc = 0; cc < C; ++cc) {
                     const int t = s * C + cc;
                     const int hh = col_head(t), cr = col_row0(t);
-                    for (int vc = 0; vc < 4; ++vc)
-                        if (!put(&tW, nb, 32 * 128, d0, col_c1(hh, cr + vc * 32), col_c2(hh, cr + vc * 32))) return false;
+                    for (int vc = 0; vc < 4; ++vc) {
+                        if (!mbar_wait(&bar_empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, XS_PROD)) return false;
+                        uint8_t* dst = sRing + rp.slot * 16384;
+                        mbar_arrive_expect_tx(&bar_full[rp.slot], wbytes);
+                        const int row = cr + vc * 32;
+                        if (VARLEN) {
+                            const int tok = T::kRowsQ ? tk0 + row : tq0 + row;
+                            tma_load_4d(dst, &tW, &bar_full[rp.slot], 0, tok, c_begin, hh);
+                        } else {
+                            const int bhh = T::kRowsQ ? b * pb.Hkv + hh : b * pb.Hq + hh;
+                            tma_load_4d(dst, &tW, &bar_full[rp.slot], 0, row, c_begin, bhh);
+                        }
+                        rp.advance(gm.stages);
+                        ++issued;
+                    }
                 }
                 return true;
             };
-            if (T::kXdb) {
-                if (n_steps > 0) ok = load_score(0);
-                for (int s = 0; ok && s < n_steps; ++s) {
-                    if (s + 1 < n_steps) ok = load_score(s + 1);
-                    if (ok) ok = load_value(s);
-                }
-            } else {
-                for (int s = 0; ok && s < n_steps; ++s) {
-                    ok = load_score(s);
-                    if (ok) ok = load_value(s);
-                }
+            if (n_steps > 0) ok = load_score(0);
+            for (int s = 0; ok && s < n_steps; ++s) {
+                if (s + 1 < n_steps) ok = load_score(s + 1);
+                if (ok) ok = load_value(s);
             }
             const int last = min(issued, gm.stages);
             RingPos dp = rp;
@@ -331,6 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto give = [&](int slot) { umma_commit(&bar_empty[slot]); };
             auto issue_score = [&](int s) -> bool {
                 const int sb = T::kXdb ? (s & 1) : 0;
+                // XDB: buffer sb last held Z of step s-2 (freed by value(s-2));
+                // own-slot kernels: X/Y of step s-1 released by the elementwise warps
                 if (T::kXdb ? s >= 2 : s >= 1) {
                     const uint32_t par = T::kXdb ? (((s - 2) >> 1) & 1) : ((s - 1) & 1);
                     if (!mbar_wait(&bar_x_free[sb], par, abort_flag, status, lim, XS_XFREE)) return false;
@@ -377,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_after();
                 for (int cc = 0; cc < C; ++cc) {
-                    const uint8_t* zs = sZ + (cc == c ? 0 : slot_of(cc, c) * 32768);
+                    const uint8_t* zs = (cc == c) ? sZown : sZ + slot_of(cc, c) * 32768;
                     for (int vc = 0; vc < 4; ++vc) {
                         const uint8_t* W = take();
                         if (!W) return false;
@@ -386,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int kt = vc * 32 + t * 16;
                             const uint64_t bd = sdesc_sw128(smem_u32(W + t * 2048), 32 * 128, 1024);
                             const uint32_t acc = (s | cc | vc | t) != 0;
-                            if (cc == c)
+                            if (cc == c && !T::kOwnSlot)
                                 umma_f16_tmem_a(t_acc, z_own + kt / 2, bd, idesc_v, acc);
                             else
                                 umma_f16(t_acc, sdesc_sw128(smem_u32(zs + (kt / 64) * 16384 + (kt % 64) * 2), 16, 1024),
@@ -397,21 +414,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 umma_commit(&bar_acc);
-                umma_commit(&bar_x_free[sb]);
+                if (!T::kOwnSlot) umma_commit(&bar_x_free[sb]);
                 if (C > 1) umma_commit_multicast(&bar_slot_free[c], peer_mask);
                 return true;
             };
-            if (T::kXdb) {
-                if (ok && n_steps > 0) ok = issue_score(0);
-                for (int s = 0; ok && s < n_steps; ++s) {
-                    if (s + 1 < n_steps) ok = issue_score(s + 1);
-                    if (ok) ok = issue_value(s);
-                }
-            } else {
-                for (int s = 0; ok && s < n_steps; ++s) {
-                    ok = issue_score(s);
-                    if (ok) ok = issue_value(s);
-                }
+            if (ok && n_steps > 0) ok = issue_score(0);
+            for (int s = 0; ok && s < n_steps; ++s) {
+                if (s + 1 < n_steps) ok = issue_score(s + 1);
+                if (ok) ok = issue_value(s);
             }
             umma_commit(&bar_drain);
             int dummy = 0;
@@ -572,15 +582,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (C > 1) to_peers(z, 0, 16);
             } else {
-                // one 32-column chunk at a time: Z of chunk q4 goes to TMEM columns
-                // [16*q4, 16*q4+16), all of which were read before
-                if (!wait_slots()) {
-                    ok = false;
-                    break;
+                uint32_t z[64];
+                // legal columns of this tile: [j_lo, j_hi)
+                int j_lo, j_hi;
+                if (T::kRowsQ) {  // dQ: keys below key_end
+                    j_lo = 0;
+                    j_hi = key_end - t * 128;
+                } else {          // dV / dK: queries at or after i_min (sequence end folded into lse2 = +inf)
+                    j_lo = row_ok ? i_min - col_row0(t) : 128;
+                    j_hi = 128;
                 }
-#pragma unroll 1
+                const float* s_l2 = stats + sbuf * 128;
+                const float* s_dl = stats + 256 + sbuf * 128;
+                // one 32-column chunk at a time (X, and Y for the two-product kernels)
+#pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t x[32], y[32], z[16];
+                    uint32_t x[32], y[32];
                     tmem_ld32(tx + q4 * 32, x);
                     if (T::kTwo) tmem_ld32(ty + q4 * 32, y);
                     tmem_ld_wait(x);
@@ -591,26 +608,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             const int j = q4 * 32 + 2 * e + u;
+                            const bool legal = j >= j_lo && j < j_hi;
                             const float sv = __uint_as_float(x[2 * e + u]);
-                            float p, v;
-                            if (T::kRowsQ) {  // dQ: row = query, column = key
-                                const bool legal = (t * 128 + j) < key_end;
-                                p = legal ? ex2_approx(sv * c2 - l2_row) : 0.f;
+                            float v;
+                            if (T::kRowsQ) {  // dQ: dS = P (dP - delta) with the row's statistics
+                                const float p = legal ? ex2_approx(sv * c2 - l2_row) : 0.f;
                                 v = p * (__uint_as_float(y[2 * e + u]) - dl_row);
-                            } else {  // dV / dK: row = key, column = query
-                                const int qi = col_row0(t) + j;
-                                const bool legal = row_ok && qi >= i_min;
-                                p = legal ? ex2_approx(sv * c2 - stats[sbuf * 128 + j]) : 0.f;
-                                v = (OP == XOP_DK) ? p * (__uint_as_float(y[2 * e + u]) - stats[256 + sbuf * 128 + j])
-                                                   : p;
+                            } else {          // dV: P^T; dK: dS^T = P^T (dP^T - delta)
+                                const float p = legal ? ex2_approx(sv * c2 - s_l2[j]) : 0.f;
+                                v = (OP == XOP_DK) ? p * (__uint_as_float(y[2 * e + u]) - s_dl[j]) : p;
                             }
                             zz[u] = v;
                         }
-                        z[e] = pack2<BF16>(zz[0], zz[1]);
+                        z[q4 * 16 + e] = pack2<BF16>(zz[0], zz[1]);
                     }
-                    tmem_st16(tx + q4 * 16, z);
-                    if (C > 1) to_peers(z, q4 * 4, 4);
                 }
+                if (T::kOwnSlot) {
+                    // X and Y are read: the next score products may overwrite them
+                    tc_fence_before();
+                    mbar_arrive(&bar_x_free[0]);
+                    // own slot: the previous step's value MMAs must have read it
+                    if (s > 0 && !warp_ok(mbar_wait(&bar_acc, (s - 1) & 1, abort_flag, status, lim, XS_ACC))) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        *reinterpret_cast<uint4*>(sZown + (u >> 3) * 16384 + sw128_offset(r, u & 7)) =
+                            make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
+                    fence_proxy_async_smem();
+                } else {
+                    // own Z -> TMEM (start of the X buffer; every column it overwrites was read)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        tmem_st16(tx + q4 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&z[q4 * 16]));
+                }
+                if (!wait_slots()) {
+                    ok = false;
+                    break;
+                }
+                if (C > 1) to_peers(z, 0, 16);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -747,8 +784,9 @@ cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
     Geo gm;
     gm.C = (nd + 3) / 4;
     gm.slab_chunks = (nd + gm.C - 1) / gm.C;
-    gm.res = pb.D <= 512 ? 1 : 0;
-    const int fixed = (gm.res ? nd * 16384 : 0) + (gm.C - 1) * 32768 + stats_bytes(op, gm.C);
+    const bool own_slot = (op == XOP_DQ || op == XOP_DK);
+    gm.res = (pb.D <= 512 && !own_slot) ? 1 : 0;
+    const int fixed = (gm.res ? nd * 16384 : 0) + (gm.C - 1 + (own_slot ? 1 : 0)) * 32768 + stats_bytes(op, gm.C);
     gm.stages = (kMaxSmem - static_cast<int>(sizeof(StaticSmem)) - fixed) / 16384;
     if (gm.stages > kStages) gm.stages = kStages;
     if (gm.stages < 2) return cudaErrorInvalidConfiguration;
@@ -763,7 +801,10 @@ cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
     const bool ks = !kv_empty;                // side flag of the kv-side maps
     CUtensorMap m[5];
     bool okm = true;
-    auto mk = [&](int i, const void* p, bool kv_side, int rows) { okm = okm && make_row_map(&m[i], p, pb, kv_side, a.bf16, rows); };
+    auto mk = [&](int i, const void* p, bool kv_side, int rows) {
+        okm = okm && (rows == 32 ? make_slab_map(&m[i], p, pb, kv_side, a.bf16, 32, gm.slab_chunks)
+                                 : make_row_map(&m[i], p, pb, kv_side, a.bf16, rows));
+    };
     int n_rt, bz;
     switch (op) {
     case XOP_FWD:

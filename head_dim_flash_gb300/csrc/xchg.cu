@@ -34,7 +34,7 @@
 namespace ffpa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 elementwise (two per TMEM row)
 constexpr int kStages = 16;      // upper bound of the TMA ring depth
 constexpr int kMaxC = 4;         // cluster size bound (D <= 1024 in 256-column slabs)
 constexpr float kTau = 8.0f;     // forward: rescale O only when the row max grows by more than 2^8
@@ -70,7 +70,7 @@ struct Traits {
 struct __align__(1024) StaticSmem {
     uint64_t full[kStages], empty[kStages];
     uint64_t a1, x_full[2], x_free[2], z_full, acc;
-    uint64_t zpeer[kMaxC], slot_free[kMaxC], stat[2], rmax[2], lsum, drain;
+    uint64_t zpeer[kMaxC], slot_free[kMaxC], stat[2], rmax[2], lsum, drain, x_read, half;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -171,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* const bar_rmax = sh.rmax;
     uint64_t& bar_lsum = sh.lsum;
     uint64_t& bar_drain = sh.drain;
+    uint64_t& bar_x_read = sh.x_read;  // forward: both threads of each row finished reading X
+    uint64_t& bar_half = sh.half;      // forward epilogue: both halves' row sums written
     if (smem_u32(smem) & 1023u) {  // uniform over the block: report, do not run misaligned
         if (threadIdx.x == 0) atomicCAS(a.ctl.status, 0u, 5u | (0xffu << 8));
         return;
@@ -185,11 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_a1, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_x_full[i], 1);
-            mbar_init(&bar_x_free[i], T::kOwnSlot ? 128 : 1);
-            mbar_init(&bar_stat[i], 128);
+            mbar_init(&bar_x_free[i], T::kOwnSlot ? 256 : 1);
+            mbar_init(&bar_stat[i], 256);
             mbar_init(&bar_rmax[i], 1);
         }
-        mbar_init(&bar_z_full, 128);
+        mbar_init(&bar_z_full, 256);
+        mbar_init(&bar_x_read, 256);
+        mbar_init(&bar_half, 256);
         mbar_init(&bar_acc, 1);
         for (int i = 0; i < kMaxC; ++i) {
             mbar_init(&bar_zpeer[i], 1);
@@ -403,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int kt = vc * 32 + t * 16;
                             const uint64_t bd = sdesc_sw128(smem_u32(W + t * 2048), 32 * 128, 1024);
                             const uint32_t acc = (s | cc | vc | t) != 0;
-                            if (cc == c && !T::kOwnSlot)
-                                umma_f16_tmem_a(t_acc, z_own + kt / 2, bd, idesc_v, acc);
+                            if (cc == c && !T::kOwnSlot)  // own Z: packed K-columns of half h at X column 96*h
+                                umma_f16_tmem_a(t_acc, z_own + kt / 2 + (kt >= 64 ? 64 : 0), bd, idesc_v, acc);
                             else
                                 umma_f16(t_acc, sdesc_sw128(smem_u32(zs + (kt / 64) * 16384 + (kt % 64) * 2), 16, 1024),
                                          bd, idesc_v, acc);
@@ -429,9 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------ elementwise
+        // Two threads per tile row: warps 2..5 take columns [0, 64), warps 6..9
+        // columns [64, 128) of the same TMEM lanes.
         const int quarter = warp & 3;
         const int r = quarter * 32 + static_cast<int>(lane_id());  // tile row = TMEM lane
-        const int tid = threadIdx.x - 64;                             // 0..127
+        const int ew = threadIdx.x - 64;                              // 0..255
+        const int half = ew >> 7;
+        const int col0 = half * 64;                                   // my columns [col0, col0 + 64)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const float c2 = pb.scale_log2;
         const int row = r0 + r;  // query (rows = queries) or key (rows = keys)
@@ -446,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             l2_row = a.lse_log2[si];
             dl_row = a.delta[si];
         }
-        float m_ref = -INFINITY, l_part = 0.f;  // forward softmax state (l over own tiles)
+        float m_ref = -INFINITY, l_part = 0.f;  // forward softmax state (l over my columns of own tiles)
         bool ok = true;
         auto warp_ok = [&](bool v) { return __all_sync(0xffffffffu, v); };
         for (int s = 0; s < n_steps; ++s) {
@@ -456,19 +464,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ty = t_x0 + 128 + lane_off;  // Y (two-product kernels)
             const int sbuf = s & 1;
             if (!T::kRowsQ) {
-                // stage the column statistics of tile t: +inf lse2 masks queries
-                // past the sequence and tiles past the end
-                const int qi = col_row0(t) + tid;
-                const int hh = col_head(t);
-                float l2 = INFINITY, dl = 0.f;
-                if (t < n_ct && qi < lq) {
-                    const size_t si = VARLEN ? static_cast<size_t>(hh) * pb.total_q + tq0 + qi
-                                             : (static_cast<size_t>(b) * pb.Hq + hh) * pb.Nq + qi;
-                    l2 = a.lse_log2[si];
-                    dl = a.delta[si];
+                // stage the column statistics of tile t (threads of half 0): +inf
+                // lse2 masks queries past the sequence and tiles past the end
+                if (half == 0) {
+                    const int qi = col_row0(t) + r;
+                    const int hh = col_head(t);
+                    float l2 = INFINITY, dl = 0.f;
+                    if (t < n_ct && qi < lq) {
+                        const size_t si = VARLEN ? static_cast<size_t>(hh) * pb.total_q + tq0 + qi
+                                                 : (static_cast<size_t>(b) * pb.Hq + hh) * pb.Nq + qi;
+                        l2 = a.lse_log2[si];
+                        dl = a.delta[si];
+                    }
+                    stats[sbuf * 128 + r] = l2;          // lse2[sbuf][column]
+                    stats[256 + sbuf * 128 + r] = dl;    // delta[sbuf][column]
                 }
-                stats[sbuf * 128 + tid] = l2;          // lse2[sbuf][tid]
-                stats[256 + sbuf * 128 + tid] = dl;    // delta[sbuf][tid]
                 mbar_arrive(&bar_stat[sbuf]);
             }
             const uint32_t xpar = T::kXdb ? ((s >> 1) & 1) : (s & 1);
@@ -481,8 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            // Writes packed Z units [u0, u0+n) of this row: own copy to TMEM by the
-            // caller, peer copies into every peer's slot (K-major, 128-byte swizzle).
+            // Peers' slots for this step are free once their previous value MMAs ran.
             auto wait_slots = [&]() -> bool {
                 if (C == 1 || s == 0) return true;
                 bool got = true;
@@ -490,46 +499,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p != c) got = mbar_wait_cluster(&bar_slot_free[p], (s - 1) & 1, abort_flag, status, lim, XS_SLOT);
                 return warp_ok(got);
             };
-            auto to_peers = [&](const uint32_t* zz, int u0, int n) {
+            // My 8 packed 16-byte units of the row (columns col0..col0+63) into
+            // every peer's slot (K-major, 128-byte swizzle), by st.async.
+            auto to_peers = [&](const uint32_t* zz) {
                 for (int p = 0; p < C; ++p) {
                     if (p == c) continue;
-                    const uint32_t base = mapa_shared(smem_u32(sZ + slot_of(c, p) * 32768), p);
+                    const uint32_t base = mapa_shared(smem_u32(sZ + slot_of(c, p) * 32768 + half * 16384), p);
                     const uint32_t rbar = mapa_shared(smem_u32(&bar_zpeer[slot_of(c, p)]), p);
-                    for (int k = 0; k < n; ++k) {
-                        const int u = u0 + k;
-                        st_async_u4(base + (u >> 3) * 16384 + sw128_offset(r, u & 7),
-                                    make_uint4(zz[4 * k], zz[4 * k + 1], zz[4 * k + 2], zz[4 * k + 3]), rbar);
-                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_async_u4(base + sw128_offset(r, k), make_uint4(zz[4 * k], zz[4 * k + 1], zz[4 * k + 2], zz[4 * k + 3]),
+                                    rbar);
                 }
             };
+            uint32_t z[32];  // my 64 columns of Z as packed pairs
             if constexpr (OP == XOP_FWD) {
-                uint32_t z[64];  // the row of P as packed pairs
-                uint32_t x[128];
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tx + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[q4 * 32]));
-                tmem_ld_wait(x);
                 const int limit = key_end - t * 128;  // legal columns [0, limit)
+                // row maximum over all 128 columns (both threads of a row compute it)
                 float mx = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 128; ++j)
-                    if (j < limit) mx = fmaxf(mx, __uint_as_float(x[j]));
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t x[32];
+                    tmem_ld32(tx + q4 * 32, x);
+                    tmem_ld_wait(x);
+                    if (limit >= 128) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(x[j]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (q4 * 32 + j < limit) mx = fmaxf(mx, __uint_as_float(x[j]));
+                    }
+                }
                 float m_tile = mx * c2;
                 if (C > 1) {
                     // exchange row maxima so every CTA of the cluster uses one reference:
                     // rmax[sbuf][slot][r] at stats + (sbuf*(C-1) + slot)*128 + r
-                    for (int p = 0; p < C; ++p) {
-                        if (p == c) continue;
-                        float* dst = stats + (sbuf * (C - 1) + slot_of(c, p)) * 128 + r;
-                        st_async_f32(mapa_shared(smem_u32(dst), p), m_tile, mapa_shared(smem_u32(&bar_rmax[sbuf]), p));
-                    }
+                    if (half == 0)
+                        for (int p = 0; p < C; ++p) {
+                            if (p == c) continue;
+                            float* dst = stats + (sbuf * (C - 1) + slot_of(c, p)) * 128 + r;
+                            st_async_f32(mapa_shared(smem_u32(dst), p), m_tile, mapa_shared(smem_u32(&bar_rmax[sbuf]), p));
+                        }
                     if (!warp_ok(mbar_wait_cluster(&bar_rmax[sbuf], (s >> 1) & 1, abort_flag, status, lim, XS_RMAX))) {
                         ok = false;
                         break;
                     }
-                    // re-arm this buffer for step s+2: no peer writes it before every
-                    // thread here has sent its step s+1 maximum
-                    if (tid == 0) mbar_arrive_expect_tx(&bar_rmax[sbuf], 512 * (C - 1));
                     for (int q = 0; q < C - 1; ++q) m_tile = fmaxf(m_tile, stats[(sbuf * (C - 1) + q) * 128 + r]);
+                    // re-arm this buffer for step s+2: no peer writes it before every
+                    // thread here has passed this wait and sent its step s+1 maximum
+                    if (ew == 0) mbar_arrive_expect_tx(&bar_rmax[sbuf], 512 * (C - 1));
                 }
                 float new_ref = m_ref;
                 bool need = false;
@@ -543,13 +562,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float alpha = need ? ex2_approx(m_ref - new_ref) : 1.f;
                 if (__any_sync(0xffffffffu, need)) {
-                    // O must be stable: wait for the previous super-step's value MMAs
+                    // O must be stable: wait for the previous super-step's value MMAs;
+                    // each half rescales half of the row's accumulator columns
                     if (s > 0 && !warp_ok(mbar_wait(&bar_acc, (s - 1) & 1, abort_flag, status, lim, XS_ACC))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    for (int cc = 0; cc < sw; cc += 32) {
+                    const int half_w = sw / 2;
+                    for (int cc = half * half_w; cc < (half + 1) * half_w; cc += 32) {
                         uint32_t o[32];
                         tmem_ld32(t_acc + lane_off + cc, o);
                         tmem_ld_wait(o);
@@ -564,25 +585,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
                 float sum = 0.f;
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const int j = 2 * e;
-                    const float p0 = (j < limit) ? ex2_approx(__uint_as_float(x[j]) * c2 - mu) : 0.f;
-                    const float p1 = (j + 1 < limit) ? ex2_approx(__uint_as_float(x[j + 1]) * c2 - mu) : 0.f;
-                    sum += p0 + p1;
-                    z[e] = pack2<BF16>(p0, p1);
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    uint32_t x[32];
+                    tmem_ld32(tx + col0 + q2 * 32, x);
+                    tmem_ld_wait(x);
+                    const int lim2 = limit - col0 - q2 * 32;
+                    if (lim2 >= 32) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float p0 = ex2_approx(fmaf(__uint_as_float(x[2 * e]), c2, -mu));
+                            const float p1 = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), c2, -mu));
+                            sum += p0 + p1;
+                            z[q2 * 16 + e] = pack2<BF16>(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float p0 = (2 * e < lim2) ? ex2_approx(fmaf(__uint_as_float(x[2 * e]), c2, -mu)) : 0.f;
+                            const float p1 = (2 * e + 1 < lim2) ? ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), c2, -mu)) : 0.f;
+                            sum += p0 + p1;
+                            z[q2 * 16 + e] = pack2<BF16>(p0, p1);
+                        }
+                    }
                 }
                 l_part += sum;
-                // own P -> TMEM (start of the X buffer; every X column it overwrites is read)
+                // own P -> TMEM, packed into X columns [96*half, 96*half + 32): wait until
+                // both threads of the row have finished reading X (the max pass reads all)
+                tc_fence_before();
+                mbar_arrive(&bar_x_read);
+                if (!warp_ok(mbar_wait(&bar_x_read, s & 1, abort_flag, status, lim, XS_XFULL))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    tmem_st16(tx + q4 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&z[q4 * 16]));
+                for (int q2 = 0; q2 < 2; ++q2)
+                    tmem_st16(tx + 96 * half + q2 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&z[q2 * 16]));
                 if (!wait_slots()) {
                     ok = false;
                     break;
                 }
-                if (C > 1) to_peers(z, 0, 16);
+                if (C > 1) to_peers(z);
             } else {
-                uint32_t z[64];
                 // legal columns of this tile: [j_lo, j_hi)
                 int j_lo, j_hi;
                 if (T::kRowsQ) {  // dQ: keys below key_end
@@ -592,14 +636,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     j_lo = row_ok ? i_min - col_row0(t) : 128;
                     j_hi = 128;
                 }
+                const bool full = j_lo <= col0 && j_hi >= col0 + 64;
                 const float* s_l2 = stats + sbuf * 128;
                 const float* s_dl = stats + 256 + sbuf * 128;
-                // one 32-column chunk at a time (X, and Y for the two-product kernels)
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int q2 = 0; q2 < 2; ++q2) {
                     uint32_t x[32], y[32];
-                    tmem_ld32(tx + q4 * 32, x);
-                    if (T::kTwo) tmem_ld32(ty + q4 * 32, y);
+                    tmem_ld32(tx + col0 + q2 * 32, x);
+                    if (T::kTwo) tmem_ld32(ty + col0 + q2 * 32, y);
                     tmem_ld_wait(x);
                     if (T::kTwo) tmem_ld_wait(y);
 #pragma unroll
@@ -607,20 +651,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float zz[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int j = q4 * 32 + 2 * e + u;
-                            const bool legal = j >= j_lo && j < j_hi;
+                            const int j = col0 + q2 * 32 + 2 * e + u;
+                            const bool legal = full || (j >= j_lo && j < j_hi);
                             const float sv = __uint_as_float(x[2 * e + u]);
                             float v;
                             if (T::kRowsQ) {  // dQ: dS = P (dP - delta) with the row's statistics
-                                const float p = legal ? ex2_approx(sv * c2 - l2_row) : 0.f;
+                                const float p = legal ? ex2_approx(fmaf(sv, c2, -l2_row)) : 0.f;
                                 v = p * (__uint_as_float(y[2 * e + u]) - dl_row);
                             } else {          // dV: P^T; dK: dS^T = P^T (dP^T - delta)
-                                const float p = legal ? ex2_approx(sv * c2 - s_l2[j]) : 0.f;
+                                const float p = legal ? ex2_approx(fmaf(sv, c2, -s_l2[j])) : 0.f;
                                 v = (OP == XOP_DK) ? p * (__uint_as_float(y[2 * e + u]) - s_dl[j]) : p;
                             }
                             zz[u] = v;
                         }
-                        z[q4 * 16 + e] = pack2<BF16>(zz[0], zz[1]);
+                        z[q2 * 16 + e] = pack2<BF16>(zz[0], zz[1]);
                     }
                 }
                 if (T::kOwnSlot) {
@@ -633,21 +677,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
 #pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        *reinterpret_cast<uint4*>(sZown + (u >> 3) * 16384 + sw128_offset(r, u & 7)) =
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<uint4*>(sZown + half * 16384 + sw128_offset(r, u)) =
                             make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
                     fence_proxy_async_smem();
                 } else {
-                    // own Z -> TMEM (start of the X buffer; every column it overwrites was read)
+                    // own Z -> TMEM, packed into X columns [96*half, 96*half + 32): inside
+                    // the columns this thread itself has read (the other half never reads them)
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        tmem_st16(tx + q4 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&z[q4 * 16]));
+                    for (int q2 = 0; q2 < 2; ++q2)
+                        tmem_st16(tx + 96 * half + q2 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&z[q2 * 16]));
                 }
                 if (!wait_slots()) {
                     ok = false;
                     break;
                 }
-                if (C > 1) to_peers(z, 0, 16);
+                if (C > 1) to_peers(z);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -658,16 +703,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = warp_ok(mbar_wait(&bar_acc, (n_steps - 1) & 1, abort_flag, status, lim, XS_EPI));
             tc_fence_after();
         }
-        float l_tot = l_part;
-        if (OP == XOP_FWD && ok && n_steps > 0 && C > 1) {
-            // lsum[slot][r] at stats + (2*(C-1) + slot)*128 + r
-            for (int p = 0; p < C; ++p)
-                if (p != c) {
-                    float* dst = stats + (2 * (C - 1) + slot_of(c, p)) * 128 + r;
-                    st_async_f32(mapa_shared(smem_u32(dst), p), l_part, mapa_shared(smem_u32(&bar_lsum), p));
-                }
-            ok = warp_ok(mbar_wait_cluster(&bar_lsum, 0, abort_flag, status, lim, XS_LSUM));
-            for (int q = 0; q < C - 1; ++q) l_tot += stats[(2 * (C - 1) + q) * 128 + r];
+        float l_tot = 0.f;
+        if (OP == XOP_FWD && ok && n_steps > 0) {
+            // Row sum: both halves' parts (the TMA ring is idle now and serves as
+            // scratch), then the CTA sums of the peers.
+            float* lsum_local = reinterpret_cast<float*>(sRing);
+            lsum_local[half * 128 + r] = l_part;
+            mbar_arrive(&bar_half);
+            ok = warp_ok(mbar_wait(&bar_half, 0, abort_flag, status, lim, XS_LSUM));
+            const float l_cta = lsum_local[r] + lsum_local[128 + r];
+            l_tot = l_cta;
+            if (ok && C > 1) {
+                if (half == 0)
+                    for (int p = 0; p < C; ++p)
+                        if (p != c) {
+                            float* dst = stats + (2 * (C - 1) + slot_of(c, p)) * 128 + r;
+                            st_async_f32(mapa_shared(smem_u32(dst), p), l_cta, mapa_shared(smem_u32(&bar_lsum), p));
+                        }
+                ok = warp_ok(mbar_wait_cluster(&bar_lsum, 0, abort_flag, status, lim, XS_LSUM));
+                for (int q = 0; q < C - 1; ++q) l_tot += stats[(2 * (C - 1) + q) * 128 + r];
+            }
         }
         if (ok) {
             float mul;
@@ -700,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t orow = VARLEN ? (static_cast<size_t>(t0 + row) * out_heads + head) * pb.D
                                        : ((static_cast<size_t>(b) * out_heads + head) * out_n + row) * pb.D;
             uint16_t* dst = reinterpret_cast<uint16_t*>(out) + orow + d0;
-            for (int cc = 0; cc < sw; cc += 32) {
+            for (int cc = half * (sw / 2); cc < (half + 1) * (sw / 2); cc += 32) {
                 uint32_t v[32];
                 if (n_steps > 0) {
                     tmem_ld32(t_acc + lane_off + cc, v);
@@ -719,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
                 }
             }
-            if (OP == XOP_FWD && c == 0 && row_ok) {
+            if (OP == XOP_FWD && c == 0 && half == 0 && row_ok) {
                 const float lse = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
                 const size_t li = VARLEN ? static_cast<size_t>(h) * pb.total_q + tq0 + row
                                          : (static_cast<size_t>(b) * pb.Hq + h) * pb.Nq + row;

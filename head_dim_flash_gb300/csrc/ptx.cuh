@@ -195,6 +195,18 @@ __device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t re
                  : "memory");
 }
 
+// Bulk copy from this CTA's shared memory into another CTA's shared memory of
+// the cluster; completes `bytes` on the destination CTA's mbarrier. Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster_addr, const void* src, uint32_t bytes,
+                                                    uint32_t remote_bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster_addr),
+                 "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");

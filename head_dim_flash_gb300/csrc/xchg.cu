@@ -57,10 +57,6 @@ struct Traits {
     static constexpr bool kTwo = (OP == XOP_DQ || OP == XOP_DK);      // X and Y score tiles
     static constexpr bool kRowsQ = (OP == XOP_FWD || OP == XOP_DQ);   // rows are queries
     static constexpr bool kXdb = !kTwo;                               // X double-buffered
-    // Two-product kernels keep their own Z in a shared-memory slot, so X and Y
-    // are free as soon as the elementwise warps have read them and the next
-    // score products overlap this step's elementwise and value work.
-    static constexpr bool kOwnSlot = kTwo;
 };
 
 // Barriers and flags live in one static block of exactly 1 KiB, so that the
@@ -70,7 +66,7 @@ struct Traits {
 struct __align__(1024) StaticSmem {
     uint64_t full[kStages], empty[kStages];
     uint64_t a1, x_full[2], x_free[2], z_full, acc;
-    uint64_t zpeer[kMaxC], slot_free[kMaxC], stat[2], rmax[2], lsum, drain, x_read, half;
+    uint64_t zpeer[kMaxC], slot_free[kMaxC], stat[2], rmax[2], lsum, drain, half;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -153,10 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ StaticSmem sh;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* sA1 = smem;                                    // resident row operand: nd x 16 KiB
-    uint8_t* sZ = sA1 + (gm.res ? nd * 16384 : 0);          // C-1 peer slots (+ own slot) x 32 KiB
-    const int n_slots = T::kOwnSlot ? C : C - 1;
-    uint8_t* sZown = sZ + (C - 1) * 32768;                  // own slot (two-product kernels)
-    float* stats = reinterpret_cast<float*>(sZ + n_slots * 32768);
+    uint8_t* sZ = sA1 + (gm.res ? nd * 16384 : 0);          // C-1 peer slots + own slot, 32 KiB each
+    uint8_t* sZown = sZ + (C - 1) * 32768;                  // own slot
+    float* stats = reinterpret_cast<float*>(sZ + C * 32768);
     uint8_t* sRing = reinterpret_cast<uint8_t*>(stats) + stats_bytes(OP, C);
     uint64_t* const bar_full = sh.full;
     uint64_t* const bar_empty = sh.empty;
@@ -171,7 +166,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* const bar_rmax = sh.rmax;
     uint64_t& bar_lsum = sh.lsum;
     uint64_t& bar_drain = sh.drain;
-    uint64_t& bar_x_read = sh.x_read;  // forward: both threads of each row finished reading X
     uint64_t& bar_half = sh.half;      // forward epilogue: both halves' row sums written
     if (smem_u32(smem) & 1023u) {  // uniform over the block: report, do not run misaligned
         if (threadIdx.x == 0) atomicCAS(a.ctl.status, 0u, 5u | (0xffu << 8));
@@ -187,12 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_a1, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_x_full[i], 1);
-            mbar_init(&bar_x_free[i], T::kOwnSlot ? 256 : 1);
+            mbar_init(&bar_x_free[i], 256);
             mbar_init(&bar_stat[i], 256);
             mbar_init(&bar_rmax[i], 1);
         }
         mbar_init(&bar_z_full, 256);
-        mbar_init(&bar_x_read, 256);
         mbar_init(&bar_half, 256);
         mbar_init(&bar_acc, 1);
         for (int i = 0; i < kMaxC; ++i) {
@@ -385,8 +378,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto issue_value = [&](int s) -> bool {
-                const int sb = T::kXdb ? (s & 1) : 0;
-                const uint32_t z_own = t_x0 + sb * 128;  // own Z: 64 packed columns at the start of X
                 if (!mbar_wait(&bar_z_full, s & 1, abort_flag, status, lim, XS_ZFULL)) return false;
                 for (int p = 0; p < C; ++p)
                     if (p != c) {
@@ -407,18 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int kt = vc * 32 + t * 16;
                             const uint64_t bd = sdesc_sw128(smem_u32(W + t * 2048), 32 * 128, 1024);
                             const uint32_t acc = (s | cc | vc | t) != 0;
-                            if (cc == c && !T::kOwnSlot)  // own Z: packed K-columns of half h at X column 96*h
-                                umma_f16_tmem_a(t_acc, z_own + kt / 2 + (kt >= 64 ? 64 : 0), bd, idesc_v, acc);
-                            else
-                                umma_f16(t_acc, sdesc_sw128(smem_u32(zs + (kt / 64) * 16384 + (kt % 64) * 2), 16, 1024),
-                                         bd, idesc_v, acc);
+                            umma_f16(t_acc, sdesc_sw128(smem_u32(zs + (kt / 64) * 16384 + (kt % 64) * 2), 16, 1024),
+                                     bd, idesc_v, acc);
                         }
                         give(rp.slot);
                         rp.advance(gm.stages);
                     }
                 }
                 umma_commit(&bar_acc);
-                if (!T::kOwnSlot) umma_commit(&bar_x_free[sb]);
                 if (C > 1) umma_commit_multicast(&bar_slot_free[c], peer_mask);
                 return true;
             };
@@ -498,19 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int p = 0; p < C && got; ++p)
                     if (p != c) got = mbar_wait_cluster(&bar_slot_free[p], (s - 1) & 1, abort_flag, status, lim, XS_SLOT);
                 return warp_ok(got);
-            };
-            // My 8 packed 16-byte units of the row (columns col0..col0+63) into
-            // every peer's slot (K-major, 128-byte swizzle), by st.async.
-            auto to_peers = [&](const uint32_t* zz) {
-                for (int p = 0; p < C; ++p) {
-                    if (p == c) continue;
-                    const uint32_t base = mapa_shared(smem_u32(sZ + slot_of(c, p) * 32768 + half * 16384), p);
-                    const uint32_t rbar = mapa_shared(smem_u32(&bar_zpeer[slot_of(c, p)]), p);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_async_u4(base + sw128_offset(r, k), make_uint4(zz[4 * k], zz[4 * k + 1], zz[4 * k + 2], zz[4 * k + 3]),
-                                    rbar);
-                }
             };
             uint32_t z[32];  // my 64 columns of Z as packed pairs
             if constexpr (OP == XOP_FWD) {
@@ -609,23 +583,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 l_part += sum;
-                // own P -> TMEM, packed into X columns [96*half, 96*half + 32): wait until
-                // both threads of the row have finished reading X (the max pass reads all)
-                tc_fence_before();
-                mbar_arrive(&bar_x_read);
-                if (!warp_ok(mbar_wait(&bar_x_read, s & 1, abort_flag, status, lim, XS_XFULL))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2)
-                    tmem_st16(tx + 96 * half + q2 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&z[q2 * 16]));
-                if (!wait_slots()) {
-                    ok = false;
-                    break;
-                }
-                if (C > 1) to_peers(z);
             } else {
                 // legal columns of this tile: [j_lo, j_hi)
                 int j_lo, j_hi;
@@ -667,36 +624,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                         z[q2 * 16 + e] = pack2<BF16>(zz[0], zz[1]);
                     }
                 }
-                if (T::kOwnSlot) {
-                    // X and Y are read: the next score products may overwrite them
-                    tc_fence_before();
-                    mbar_arrive(&bar_x_free[0]);
-                    // own slot: the previous step's value MMAs must have read it
-                    if (s > 0 && !warp_ok(mbar_wait(&bar_acc, (s - 1) & 1, abort_flag, status, lim, XS_ACC))) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        *reinterpret_cast<uint4*>(sZown + half * 16384 + sw128_offset(r, u)) =
-                            make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
-                    fence_proxy_async_smem();
-                } else {
-                    // own Z -> TMEM, packed into X columns [96*half, 96*half + 32): inside
-                    // the columns this thread itself has read (the other half never reads them)
-#pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2)
-                        tmem_st16(tx + 96 * half + q2 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&z[q2 * 16]));
-                }
-                if (!wait_slots()) {
-                    ok = false;
-                    break;
-                }
-                if (C > 1) to_peers(z);
             }
-            tmem_st_wait();
+            // X (and Y) are read: the next score products into this buffer may start
             tc_fence_before();
+            mbar_arrive(&bar_x_free[sb]);
+            // The own slot may be rewritten once the previous step's value MMAs here
+            // (acc) and every peer (slot_free: it consumed our copy, so the copy has
+            // read the slot) are done with it.
+            if (s > 0 && !warp_ok(mbar_wait(&bar_acc, (s - 1) & 1, abort_flag, status, lim, XS_ACC))) {
+                ok = false;
+                break;
+            }
+            if (!wait_slots()) {
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<uint4*>(sZown + half * 16384 + sw128_offset(r, u)) =
+                    make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
+            fence_proxy_async_smem();
             mbar_arrive(&bar_z_full);
+            if (C > 1 && ew == 0) {
+                // one bulk copy of the whole slot into every peer, once all 256 threads
+                // have written it (on a time-out the copies are skipped; the abort flag
+                // then ends every wait of this CTA and of its peers)
+                if (mbar_wait(&bar_z_full, s & 1, abort_flag, status, lim, XS_ZFULL)) {
+                    for (int p = 0; p < C; ++p) {
+                        if (p == c) continue;
+                        bulk_copy_s2cluster(mapa_shared(smem_u32(sZ + slot_of(c, p) * 32768), p), sZown, 32768,
+                                            mapa_shared(smem_u32(&bar_zpeer[slot_of(c, p)]), p));
+                    }
+                }
+            }
         }
         // ------------------------------------------------------ epilogue
         if (ok && n_steps > 0) {
@@ -839,9 +799,11 @@ cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
     Geo gm;
     gm.C = (nd + 3) / 4;
     gm.slab_chunks = (nd + gm.C - 1) / gm.C;
-    const bool own_slot = (op == XOP_DQ || op == XOP_DK);
-    gm.res = (pb.D <= 512 && !own_slot) ? 1 : 0;
-    const int fixed = (gm.res ? nd * 16384 : 0) + (gm.C - 1 + (own_slot ? 1 : 0)) * 32768 + stats_bytes(op, gm.C);
+    const int slots_bytes = gm.C * 32768;  // own slot + C-1 peer slots
+    const int budget = kMaxSmem - static_cast<int>(sizeof(StaticSmem));
+    // keep the first row operand resident only if a ring of >= 6 stages still fits
+    gm.res = (nd * 16384 + slots_bytes + stats_bytes(op, gm.C) + 6 * 16384 <= budget) ? 1 : 0;
+    const int fixed = (gm.res ? nd * 16384 : 0) + slots_bytes + stats_bytes(op, gm.C);
     gm.stages = (kMaxSmem - static_cast<int>(sizeof(StaticSmem)) - fixed) / 16384;
     if (gm.stages > kStages) gm.stages = kStages;
     if (gm.stages < 2) return cudaErrorInvalidConfiguration;

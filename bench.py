@@ -40,6 +40,7 @@ def parse():
     ap.add_argument("--config", default="headline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all", action="store_true", help="one line per workload (parity-size cases excluded)")
     ap.add_argument("--heads", type=int, default=0,
                     help="override Hq=Hkv (profiling a smaller case of the same kernels)")
     return ap.parse_args()
@@ -49,14 +50,17 @@ def workload(name):
     from head_dim_flash_gb300 import workloads as W
 
     table = {"headline": W.HEADLINE, "tiny": W.TINY, "gqa": W.GQA_CAUSAL,
-             "sweep320": W.SWEEP[0], "sweep640": W.SWEEP[1], "sweep1024": W.SWEEP[2]}
+             "sweep320": W.SWEEP[0], "sweep640": W.SWEEP[1], "sweep1024": W.SWEEP[2], "varlen": W.VARLEN}
     if name not in table:
         raise SystemExit(f"unknown config {name}; choose from {sorted(table)}")
     return table[name]
 
 
 def flops(w):
-    f = 4.0 * w.B * w.Hq * w.Nq * w.Nkv * w.D
+    if w.varlen:
+        f = sum(4.0 * w.Hq * n * n * w.D for n in w.seqlens)
+    else:
+        f = 4.0 * w.B * w.Hq * w.Nq * w.Nkv * w.D
     if w.causal:
         f *= 0.5
     return f, 2.5 * f
@@ -238,31 +242,47 @@ def run_ours(args):
     inp = W.make_inputs(w)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "dO"))
     o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(max(api.bwd_workspace_bytes(q, k), 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if w.varlen:
+        # packed batch: forward and the whole backward through the varlen entry points
+        cu = inp["cu_seqlens"].to(dev)
+        mx = max(w.seqlens)
+        names = ("fwd", "bwd")
+        state = {}
 
-    # per-kernel events: fwd | preprocess | dV | dK | dQ (ffpa_bwd_stages bits 0, 1, 3, 2)
-    names = ("fwd", "preprocess", "dv", "dk", "dq")
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        api.fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
-        for i, bit in enumerate((1, 2, 8, 4)):
+        def step(ev=None):
             if ev is not None:
-                ev[i + 1].record(stream)
-            api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=bit)
-        if ev is not None:
-            ev[5].record(stream)
+                ev[0].record(stream)
+            state["o"], state["lse"] = api.varlen_fwd(q, k, v, cu, cu, mx, mx, w.causal, w.scale)
+            if ev is not None:
+                ev[1].record(stream)
+            api.varlen_bwd(q, k, v, state["o"], state["lse"], do, cu, cu, mx, mx, w.causal, w.scale)
+            if ev is not None:
+                ev[2].record(stream)
+    else:
+        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(api.bwd_workspace_bytes(q, k), 1), dtype=torch.uint8, device=dev)
+        # per-kernel events: fwd | preprocess | dV | dK | dQ (ffpa_bwd_stages bits 0, 1, 3, 2)
+        names = ("fwd", "preprocess", "dv", "dk", "dq")
+
+        def step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            api.fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
+            for i, bit in enumerate((1, 2, 8, 4)):
+                if ev is not None:
+                    ev[i + 1].record(stream)
+                api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=bit)
+            if ev is not None:
+                ev[5].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
     api.get_status()
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -286,7 +306,7 @@ def run_ours(args):
     total_ms = slowest_rank_ms(total_ms, world, dev)
     ms_step = total_ms / args.steps
     fwd_ms = per_ms["fwd"]
-    bwd_ms = per_ms["preprocess"] + per_ms["dv"] + per_ms["dk"] + per_ms["dq"]
+    bwd_ms = sum(v for n, v in per_ms.items() if n != "fwd")
     value = job_throughput(f_fwd + f_bwd, world, ms_step)
     pk = peaks()
     clocks = clk.summary()
@@ -295,7 +315,10 @@ def run_ours(args):
     # per launch = the GEMMs its outputs require: fwd 2 (S, PV), dV 2 (S, dV),
     # dK 3 (S, dP, dK), dQ 3 (S, dP, dQ), each 2*B*Hq*Nq*Nkv*D (halved causal)
     gemm = f_fwd / 2.0
-    algo = {"fwd": 2 * gemm, "dv": 2 * gemm, "dk": 3 * gemm, "dq": 3 * gemm}
+    if w.varlen:
+        algo = {"fwd": 2 * gemm, "bwd": 8 * gemm}  # bwd: preprocess + dV (2) + dK (3) + dQ (3) units
+    else:
+        algo = {"fwd": 2 * gemm, "dv": 2 * gemm, "dk": 3 * gemm, "dq": 3 * gemm}
     dom = max(algo, key=lambda n: per_ms[n])
     achieved = algo[dom] / (per_ms[dom] / 1e3) / 1e12
     peak = pk["bf16_tflops_sustained"]
@@ -328,7 +351,7 @@ def run_ours(args):
             "kernel_ms": per_ms,
             "pct_peak_burst": 100 * value / world / pk["bf16_tflops"],
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": 5 * args.steps,  # fwd, preprocess, dV, dK, dQ per step
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -381,6 +404,11 @@ def main():
     from head_dim_flash_gb300 import build
 
     build.build()
+    if args.all:
+        for name in ("headline", "gqa", "sweep320", "sweep640", "sweep1024", "varlen"):
+            args.config = name
+            run_ours(args)
+        return
     run_ours(args)
 
 

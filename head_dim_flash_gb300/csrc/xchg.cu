@@ -49,7 +49,7 @@ struct Geo {
     int C;            // CTAs per cluster (= D-slabs)
     int slab_chunks;  // 64-wide head-dim chunks per slab (the last slab may be smaller)
     int stages;       // TMA ring depth
-    int res;          // first row operand resident in shared memory (D <= 512)
+    int res;          // leading 64-wide chunks of the first row operand kept resident in shared memory
 };
 
 template <int OP>
@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ shared memory
     __shared__ StaticSmem sh;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* sA1 = smem;                                    // resident row operand: nd x 16 KiB
-    uint8_t* sZ = sA1 + (gm.res ? nd * 16384 : 0);          // C-1 peer slots + own slot, 32 KiB each
+    uint8_t* sA1 = smem;                                    // resident row-operand chunks: res x 16 KiB
+    uint8_t* sZ = sA1 + gm.res * 16384;                     // C-1 peer slots + own slot, 32 KiB each
     uint8_t* sZown = sZ + (C - 1) * 32768;                  // own slot
     float* stats = reinterpret_cast<float*>(sZ + C * 32768);
     uint8_t* sRing = reinterpret_cast<uint8_t*>(stats) + stats_bytes(OP, C);
@@ -264,15 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++issued;
                 return true;
             };
-            if (gm.res && n_steps > 0) {
-                mbar_arrive_expect_tx(&bar_a1, nd * 16384);
-                for (int d = 0; d < nd; ++d) tma_load_3d(sA1 + d * 16384, &tA1, &bar_a1, d * 64, row_c1(r0), row_c2(r0));
+            if (gm.res > 0 && n_steps > 0) {
+                mbar_arrive_expect_tx(&bar_a1, gm.res * 16384);
+                for (int d = 0; d < gm.res; ++d) tma_load_3d(sA1 + d * 16384, &tA1, &bar_a1, d * 64, row_c1(r0), row_c2(r0));
             }
             auto load_score = [&](int s) -> bool {
                 const int t = s * C + c;
                 const int hh = col_head(t), cr = col_row0(t);
                 for (int d = 0; d < nd; ++d) {
-                    if (!gm.res && !put(&tA1, 1, 16384, d * 64, row_c1(r0), row_c2(r0))) return false;
+                    if (d >= gm.res && !put(&tA1, 1, 16384, d * 64, row_c1(r0), row_c2(r0))) return false;
                     if (!put(&tB1, 1, 16384, d * 64, col_c1(hh, cr), col_c2(hh, cr))) return false;
                 }
                 if (T::kTwo)
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int dummy = 0;
                 mbar_wait(&bar_full[dp.slot], dp.phase, &dummy, status, lim, XS_DRAIN, false);
             }
-            if (gm.res && n_steps > 0) {
+            if (gm.res > 0 && n_steps > 0) {
                 int dummy = 0;
                 mbar_wait(&bar_a1, 0, &dummy, status, lim, XS_DRAIN, false);
             }
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_v = idesc_f16(128, sw, BF16, false, true);
             RingPos rp;
             bool ok = true;
-            if (gm.res && n_steps > 0) {
+            if (gm.res > 0 && n_steps > 0) {
                 ok = mbar_wait(&bar_a1, 0, abort_flag, status, lim, XS_A1);
                 tc_fence_after();
             }
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int d = 0; d < nd; ++d) {
                         const uint8_t* A;
                         int a_slot = -1;
-                        if (prod == 0 && gm.res) {
+                        if (prod == 0 && d < gm.res) {
                             A = sA1 + d * 16384;
                         } else {
                             A = take();
@@ -801,9 +801,15 @@ cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
     gm.slab_chunks = (nd + gm.C - 1) / gm.C;
     const int slots_bytes = gm.C * 32768;  // own slot + C-1 peer slots
     const int budget = kMaxSmem - static_cast<int>(sizeof(StaticSmem));
-    // keep the first row operand resident only if a ring of >= 6 stages still fits
-    gm.res = (nd * 16384 + slots_bytes + stats_bytes(op, gm.C) + 6 * 16384 <= budget) ? 1 : 0;
-    const int fixed = (gm.res ? nd * 16384 : 0) + slots_bytes + stats_bytes(op, gm.C);
+    // keep as many leading chunks of the first row operand resident as leave a
+    // ring of >= 10 stages (they are reused by every step of the work unit; the
+    // ring depth matters more than the bytes they save)
+    {
+        const int spare = budget - slots_bytes - stats_bytes(op, gm.C) - 10 * 16384;
+        gm.res = spare > 0 ? spare / 16384 : 0;
+        if (gm.res > nd) gm.res = nd;
+    }
+    const int fixed = gm.res * 16384 + slots_bytes + stats_bytes(op, gm.C);
     gm.stages = (kMaxSmem - static_cast<int>(sizeof(StaticSmem)) - fixed) / 16384;
     if (gm.stages > kStages) gm.stages = kStages;
     if (gm.stages < 2) return cudaErrorInvalidConfiguration;

@@ -69,7 +69,12 @@ struct XArgs {
     DeviceCtl ctl;
 };
 
+// Runs one of the four GEMM kernels. The CTA-pair form (2-SM MMAs, clusters
+// of 2C CTAs) is the default; FFPA_KERNEL=single in the environment selects
+// the one-CTA-per-slab form (clusters of C CTAs) instead.
 cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s);
+cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s);
+cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s);
 
 // Function pointer to the driver's cuTensorMapEncodeTiled (resolved once).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

@@ -27,6 +27,9 @@
 //
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
 // warps 2..5 elementwise (one tile row per thread) and epilogue.
+#include <cstdlib>
+#include <cstring>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tile_common.cuh"
@@ -789,7 +792,7 @@ cudaError_t dispatch(const XArgs& a, const CUtensorMap* maps, const Geo& gm, int
 
 }  // namespace
 
-cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
+cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
 {
     const Problem& pb = a.pb;
     const bool q_empty = q_side_empty(pb), kv_empty = kv_side_empty(pb);
@@ -855,6 +858,15 @@ cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
     case XOP_DV: return dispatch<XOP_DV>(a, m, gm, n_rt, bz, smem, s);
     default: return dispatch<XOP_DK>(a, m, gm, n_rt, bz, smem, s);
     }
+}
+
+cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
+{
+    static const bool single = [] {
+        const char* e = std::getenv("FFPA_KERNEL");
+        return e != nullptr && std::strcmp(e, "single") == 0;
+    }();
+    return single ? launch_single(op, a, s) : launch_pair(op, a, s);
 }
 
 }  // namespace ffpa

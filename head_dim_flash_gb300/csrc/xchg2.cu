@@ -31,9 +31,20 @@
 // layout, LSE [H, T]), "Blackwell status" (preprocess plus separate
 // gradient launches, split because one SM cannot hold a whole dK/dV tile).
 //
+// When shared memory allows, the Z tiles are double-buffered (own tile and
+// the copies received from the other pairs), so that producing and shipping
+// Z of step s overlaps the value products of step s-1; the value products
+// take the pair's own tile first, which needs no copy.
+//
 // Warp roles in every CTA: warp 0 TMA producer, warp 1 MMA issuer (even rank)
 // or barrier forwarder (odd rank), warps 2..9 elementwise (two threads per
-// TMEM row) and epilogue.
+// TMEM row) and epilogue, warp 10 ships the own Z tile to the other pairs.
+//
+// Every per-step barrier is indexed by buffer and every waiter observes each
+// of its phases in order, at most one phase away from the barrier's state,
+// so that the parity waits are exact.
+#include <cstdlib>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tile_common.cuh"
@@ -41,22 +52,24 @@
 namespace ffpa {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kStages = 16;      // upper bound of the TMA ring depth
+constexpr int kThreads = 352;
+constexpr int kStages = 8;       // upper bound of the TMA ring depth
 constexpr int kMaxC = 4;         // pairs per cluster (D <= 1024 in 256-column slabs; <= 8 CTAs)
-constexpr int kSlot = 16384;     // bytes of one ring slot in each CTA
+constexpr int kSlot = 32768;     // bytes of one ring slot (one TMA box) in each CTA
 constexpr float kTau = 8.0f;     // forward: rescale O only when the row max grows by more than 2^8
 constexpr float kLn2 = 0.693147180559945309f;
 
 enum Site : uint32_t {
     PS_PROD = 64, PS_A1, PS_XFREE, PS_RING, PS_ZFULL, PS_ZPEER, PS_ZPAIR, PS_XFULL, PS_RMAX, PS_ACC, PS_SLOT,
-    PS_STAT, PS_LSUM, PS_EPI, PS_DRAIN, PS_FWDR
+    PS_STAT, PS_LSUM, PS_EPI, PS_DRAIN, PS_FWDR, PS_COPY
 };
 
 struct PGeo {
     int C;       // pairs per cluster (= head-dim slabs of <= 256 columns)
     int stages;  // TMA ring depth
     int res;     // leading 64-wide chunks of the first row operand kept resident in shared memory
+    int nbuf;    // Z buffers per slot (1 or 2)
+    int nprod;   // producer lanes (ring positions are dealt round-robin)
 };
 
 template <int OP>
@@ -70,8 +83,8 @@ struct Traits {
 // shared memory after it starts 1024-byte aligned (checked at run time).
 struct __align__(1024) StaticSmem {
     uint64_t full[kStages], empty[kStages];
-    uint64_t a1, x_full[2], x_free[2], z_full, zpair, acc;
-    uint64_t zpeer[kMaxC], slot_free[kMaxC], stat[2], rmax[2], lsum, drain, half;
+    uint64_t a1, x_full[2], x_free[2], z_full[2], zpair_own[2], zpair_peer[2], acc[2];
+    uint64_t zpeer[kMaxC][2], slot_free[kMaxC][2], stat[2], rmax[2], lsum, drain, half;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -150,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_steps = (n_ct + C - 1) / C;
 
     const int nd = pb.D / 64;          // 64-wide head-dim chunks
-    const int nb2 = (nd + 1) / 2;      // chunk pairs (one column-operand box each)
+    const int nb4 = (nd + 3) / 4;      // groups of four chunks (one column-operand box each)
     const int d0 = c * 256;            // first column of my pair's slab
     const int d_pad = (pb.D + 127) & ~127;
     const int sw = min(256, d_pad - d0);  // slab width: 256 or 128 (N of the value MMA)
@@ -161,10 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ shared memory
     __shared__ StaticSmem sh;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* sA1 = smem;                     // resident row-operand chunks: res x 16 KiB
-    uint8_t* sZ = sA1 + gm.res * kSlot;      // C-1 slots of the other pairs + own slot, 32 KiB each
-    uint8_t* sZown = sZ + (C - 1) * 32768;
-    float* stats = reinterpret_cast<float*>(sZ + C * 32768);
+    const int nbuf = gm.nbuf;
+    uint8_t* sA1 = smem;                          // resident row-operand chunks, two per 32 KiB
+    uint8_t* sZ = sA1 + (gm.res / 2) * kSlot;     // Z slots, 32 KiB each: [C-1 other pairs + own][nbuf]
+    float* stats = reinterpret_cast<float*>(sZ + C * nbuf * 32768);
     uint8_t* sRing = reinterpret_cast<uint8_t*>(stats) + pair_stats_bytes(OP, C);
     if (smem_u32(smem) & 1023u) {  // uniform over the cluster: report, do not run misaligned
         if (threadIdx.x == 0) atomicCAS(a.ctl.status, 0u, 5u | (0xffu << 8));
@@ -172,7 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     const int warp = threadIdx.x / 32;
-    const int zpair_count = 8 + (C > 1 ? 1 : 0);  // follower: 8 elementwise warps + forwarder
     if (threadIdx.x == 0) {
         for (int i = 0; i < gm.stages; ++i) {
             mbar_init(&sh.full[i], 1);
@@ -181,18 +193,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sh.a1, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.x_full[i], 1);
-            mbar_init(&sh.x_free[i], 16);  // 8 elementwise warps of each CTA of the pair
+            mbar_init(&sh.x_free[i], 16);     // 8 elementwise warps of each CTA of the pair
             mbar_init(&sh.stat[i], 256);
             mbar_init(&sh.rmax[i], 1);
+            mbar_init(&sh.z_full[i], 256);    // own elementwise threads wrote the own Z buffer
+            mbar_init(&sh.zpair_own[i], 8);   // (even rank) the odd rank's 8 elementwise warps did
+            mbar_init(&sh.zpair_peer[i], 1);  // (even rank) the odd rank received the other pairs' Z
+            mbar_init(&sh.acc[i], 1);
+            for (int j = 0; j < kMaxC; ++j) {
+                mbar_init(&sh.zpeer[j][i], 1);
+                mbar_init(&sh.slot_free[j][i], 1);
+            }
         }
-        mbar_init(&sh.z_full, 256);
-        mbar_init(&sh.zpair, zpair_count);
         mbar_init(&sh.half, 256);
-        mbar_init(&sh.acc, 1);
-        for (int i = 0; i < kMaxC; ++i) {
-            mbar_init(&sh.zpeer[i], 1);
-            mbar_init(&sh.slot_free[i], 1);
-        }
         mbar_init(&sh.lsum, 1);
         mbar_init(&sh.drain, 1);
         sh.abort_flag = 0;
@@ -203,10 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // and live in the even rank.
         if (leader) {
             for (int i = 0; i < gm.stages; ++i) mbar_arrive_expect_tx(&sh.full[i], 2 * kSlot);
-            if (gm.res > 0 && n_steps > 0) mbar_arrive_expect_tx(&sh.a1, 2 * gm.res * kSlot);
+            if (gm.res > 0 && n_steps > 0) mbar_arrive_expect_tx(&sh.a1, 2 * (gm.res / 2) * kSlot);
         }
         if (C > 1) {
-            for (int i = 0; i < C - 1; ++i) mbar_arrive_expect_tx(&sh.zpeer[i], 32768);
+            for (int i = 0; i < C - 1; ++i)
+                for (int bb = 0; bb < nbuf; ++bb) mbar_arrive_expect_tx(&sh.zpeer[i][bb], 32768);
             if (OP == XOP_FWD) {
                 mbar_arrive_expect_tx(&sh.rmax[0], 512 * (C - 1));
                 mbar_arrive_expect_tx(&sh.rmax[1], 512 * (C - 1));
@@ -235,6 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the CTA of pair p that holds my rows has rank 2p + rh.
     auto slot_of = [&](int writer, int consumer) { return writer < consumer ? writer : writer - 1; };
     auto xrank = [&](int p) { return 2 * p + rh; };
+    auto zslot = [&](int slot, int bb) { return sZ + (slot * nbuf + bb) * 32768; };  // slot C-1 = own
+    // Step s uses Z buffer s % nbuf for the (s / nbuf)-th time.
+    auto zbuf = [&](int s) { return s % nbuf; };
+    auto zpar = [&](int s) { return static_cast<uint32_t>((s / nbuf) & 1); };
+    auto accpar = [&](int s) { return static_cast<uint32_t>((s >> 1) & 1); };  // acc[s & 1]
 
     // Column tile t -> (head, first row) on the column side; t past the end is
     // clamped for loading (its results are masked to zero).
@@ -243,86 +262,85 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tc = min(t, n_ct - 1);
         return T::kRowsQ ? tc * 128 : (m_start + tc % max(n_mt, 1)) * 128;
     };
-    // TMA coordinates. Dense maps: (d, row, b*H + head) / (64, row, chunk, b*H + head);
-    // packed maps: (d, head, token) / (64, token, chunk, head).
-    auto q_c1 = [&](int head, int row) { return VARLEN ? head : row; };
-    auto q_c2 = [&](int head, int row) { return VARLEN ? tq0 + row : b * pb.Hq + head; };
-    auto k_c1 = [&](int head, int row) { return VARLEN ? head : row; };
-    auto k_c2 = [&](int head, int row) { return VARLEN ? tk0 + row : b * pb.Hkv + head; };
-    auto row_c1 = [&](int row) { return T::kRowsQ ? q_c1(h, row) : k_c1(hk, row); };
-    auto row_c2 = [&](int row) { return T::kRowsQ ? q_c2(h, row) : k_c2(hk, row); };
-    // 4-D slab boxes on the column side: (row coordinate, head coordinate)
+    // TMA coordinates of the 4-D maps: dense (64, row, chunk, b*H + head), packed
+    // (64, token, chunk, head). On the column side:
     auto col_slab_row = [&](int head, int row) {
         return VARLEN ? (T::kRowsQ ? tk0 + row : tq0 + row) : row;
     };
     auto col_slab_head = [&](int head) {
         return VARLEN ? head : (T::kRowsQ ? b * pb.Hkv + head : b * pb.Hq + head);
     };
+    // ... and on the row side (the unit's own head)
+    auto row_slab_row = [&](int row) { return VARLEN ? (T::kRowsQ ? tq0 + row : tk0 + row) : row; };
+    auto row_slab_head = [&]() { return VARLEN ? (T::kRowsQ ? h : hk) : (T::kRowsQ ? b * pb.Hq + h : b * pb.Hkv + hk); };
 
     if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+        // ------------------------------------------------------ TMA producers
         // Both CTAs of the pair load the same sequence of slots (each its own
-        // part of every operand); every load completes on the even rank's
-        // full barrier, which its MMA thread arms with both CTAs' bytes.
-        if (elect_one()) {
-            prefetch_tmap(&tA1);
-            prefetch_tmap(&tB1);
-            prefetch_tmap(&tW);
-            if (T::kTwo) {
-                prefetch_tmap(&tA2);
-                prefetch_tmap(&tB2);
+        // part of every operand); every load completes on the even rank's full
+        // barrier, which its MMA thread arms with both CTAs' bytes. Lanes
+        // 0 .. nprod-1 issue the ring positions round-robin: the loads one thread
+        // issues are served one after another, several threads keep several
+        // boxes in flight at a time.
+        const int me = static_cast<int>(lane_id());
+        const int nprod = gm.nprod;
+        if (me < nprod) {
+            if (me == 0) {
+                prefetch_tmap(&tA1);
+                prefetch_tmap(&tB1);
+                prefetch_tmap(&tW);
+                if (T::kTwo) {
+                    prefetch_tmap(&tA2);
+                    prefetch_tmap(&tB2);
+                }
             }
             RingPos rp;
-            int issued = 0;
+            int pos = 0;  // ring positions handed out so far (both lanes)
             bool ok = true;
-            auto slot_wait = [&]() -> bool {
-                return mbar_wait(&sh.empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, PS_PROD);
-            };
             auto lead_full = [&](int slot) { return mapa_shared(smem_u32(&sh.full[slot]), lead_rank); };
-            auto put_row = [&](const CUtensorMap* m, int chunk) -> bool {
-                if (!slot_wait()) return false;
-                tma_load_3d_pair(sRing + rp.slot * kSlot, m, lead_full(rp.slot), chunk * 64, row_c1(r0), row_c2(r0));
+            // one 4-D box into the next ring position, if that position is mine
+            auto put = [&](const CUtensorMap* m, int row_coord, int chunk, int head_coord) -> bool {
+                bool got = true;
+                if (pos % nprod == me) {
+                    got = mbar_wait(&sh.empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, PS_PROD);
+                    if (got)
+                        tma_load_4d_pair(sRing + rp.slot * kSlot, m, lead_full(rp.slot), 0, row_coord, chunk, head_coord);
+                }
                 rp.advance(gm.stages);
-                ++issued;
-                return true;
+                ++pos;
+                return got;
             };
-            auto put_slab = [&](const CUtensorMap* m, int chunk, int head, int row) -> bool {
-                if (!slot_wait()) return false;
-                tma_load_4d_pair(sRing + rp.slot * kSlot, m, lead_full(rp.slot), 0, col_slab_row(head, row), chunk,
-                                 col_slab_head(head));
-                rp.advance(gm.stages);
-                ++issued;
-                return true;
-            };
-            if (gm.res > 0 && n_steps > 0) {
+            if (me == 0 && gm.res > 0 && n_steps > 0) {
                 const uint32_t a1 = mapa_shared(smem_u32(&sh.a1), lead_rank);
-                for (int d = 0; d < gm.res; ++d)
-                    tma_load_3d_pair(sA1 + d * kSlot, &tA1, a1, d * 64, row_c1(r0), row_c2(r0));
+                for (int j = 0; 2 * j < gm.res; ++j)
+                    tma_load_4d_pair(sA1 + j * kSlot, &tA1, a1, 0, row_slab_row(r0), 2 * j, row_slab_head());
             }
-            // score operands of step s: per product, per chunk pair j: A(2j), B(j), A(2j+1)
+            // score operands of step s, per product and per group of four chunks q:
+            // A(4q, 4q+1), B(4q .. 4q+3), A(4q+2, 4q+3)
             auto load_score = [&](int s) -> bool {
                 const int t = s * C + c;
                 const int hh = col_head(t), cr = col_row0(t) + 64 * rh;
                 for (int prod = 0; prod < (T::kTwo ? 2 : 1); ++prod) {
                     const CUtensorMap* mA = prod ? &tA2 : &tA1;
                     const CUtensorMap* mB = prod ? &tB2 : &tB1;
-                    for (int j = 0; j < nb2; ++j) {
-                        if (!(prod == 0 && 2 * j < gm.res) && !put_row(mA, 2 * j)) return false;
-                        if (!put_slab(mB, 2 * j, hh, cr)) return false;
-                        if (2 * j + 1 < nd && !(prod == 0 && 2 * j + 1 < gm.res) && !put_row(mA, 2 * j + 1))
+                    for (int q = 0; q < nb4; ++q) {
+                        if (!(prod == 0 && 4 * q < gm.res) && !put(mA, row_slab_row(r0), 4 * q, row_slab_head()))
+                            return false;
+                        if (!put(mB, col_slab_row(hh, cr), 4 * q, col_slab_head(hh))) return false;
+                        if (4 * q + 2 < nd && !(prod == 0 && 4 * q + 2 < gm.res) &&
+                            !put(mA, row_slab_row(r0), 4 * q + 2, row_slab_head()))
                             return false;
                     }
                 }
                 return true;
             };
-            // value operand of step s: per column tile, two boxes of 64 keys x my
-            // two 64-wide chunks of the slab
+            // value operand of step s: per column tile (own pair's tile first), one
+            // box of the tile's 128 keys x my two 64-wide chunks of the slab
             auto load_value = [&](int s) -> bool {
-                for (int cc = 0; cc < C; ++cc) {
-                    const int t = s * C + cc;
-                    const int hh = col_head(t), cr = col_row0(t);
-                    for (int i = 0; i < 2; ++i)
-                        if (!put_slab(&tW, w_chunk, hh, cr + 64 * i)) return false;
+                for (int k = 0; k < C; ++k) {
+                    const int t = s * C + (c + k) % C;
+                    const int hh = col_head(t);
+                    if (!put(&tW, col_slab_row(hh, col_row0(t)), w_chunk, col_slab_head(hh))) return false;
                 }
                 return true;
             };
@@ -333,10 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // No CTA leaves with loads in flight: the MMA thread releases a slot only
             // after its data landed in both CTAs and was consumed.
-            const int last = min(issued, gm.stages);
+            const int last = min(pos, gm.stages);
             RingPos dp = rp;
             for (int i = 0; i < last; ++i) {
                 dp.retreat(gm.stages);
+                if ((pos - 1 - i) % nprod != me) continue;
                 int dummy = 0;
                 if (!mbar_wait(&sh.empty[dp.slot], dp.phase, &dummy, status, lim, PS_DRAIN, false)) break;
             }
@@ -347,9 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (elect_one()) {
                 const uint32_t idesc_s = idesc_f16(256, 128, BF16, false, false);
                 const uint32_t idesc_v = idesc_f16(256, sw, BF16, false, true);
-                uint16_t others = 0;  // every CTA outside my pair
-                for (int p = 0; p < 2 * C; ++p)
-                    if ((p >> 1) != c) others |= static_cast<uint16_t>(1u << p);
                 RingPos rp;
                 bool ok = true;
                 if (gm.res > 0 && n_steps > 0) {
@@ -375,33 +391,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     for (int prod = 0; prod < (T::kTwo ? 2 : 1); ++prod) {
                         const uint32_t dst = t_x0 + (T::kXdb ? sb * 128 : prod * 128);
-                        for (int j = 0; j < nb2; ++j) {
+                        for (int q = 0; q < nb4; ++q) {
+                            // A slots hold chunks (4q, 4q+1) and (4q+2, 4q+3), 128 rows each;
+                            // the B slot holds chunks 4q .. 4q+3, 64 rows each
                             const uint8_t* B = nullptr;
                             int b_slot = -1;
-                            for (int u = 0; u < 2; ++u) {
-                                const int d = 2 * j + u;
-                                if (d >= nd) break;
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int d_first = 4 * q + 2 * h2;
+                                if (d_first >= nd) break;
                                 const uint8_t* A;
                                 int a_slot = -1;
-                                if (prod == 0 && d < gm.res) {
-                                    A = sA1 + d * kSlot;
+                                if (prod == 0 && d_first < gm.res) {
+                                    A = sA1 + (d_first / 2) * kSlot;
                                 } else {
                                     A = take();
                                     if (!A) return false;
                                     a_slot = rp.slot;
                                     rp.advance(gm.stages);
                                 }
-                                if (u == 0) {
+                                if (h2 == 0) {
                                     B = take();
                                     if (!B) return false;
                                     b_slot = rp.slot;
                                     rp.advance(gm.stages);
                                 }
+                                for (int u2 = 0; u2 < 2; ++u2) {
+                                    const int d = d_first + u2;
+                                    if (d >= nd) break;
 #pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    umma_f16_pair(dst, sdesc_sw128(smem_u32(A + kk * 32), 16, 1024),
-                                                  sdesc_sw128(smem_u32(B + u * 8192 + kk * 32), 16, 1024), idesc_s,
-                                                  (d | kk) != 0);
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        umma_f16_pair(dst, sdesc_sw128(smem_u32(A + u2 * 16384 + kk * 32), 16, 1024),
+                                                      sdesc_sw128(smem_u32(B + (2 * h2 + u2) * 8192 + kk * 32), 16, 1024),
+                                                      idesc_s, (d | kk) != 0);
+                                }
                                 if (a_slot >= 0) give(a_slot);
                             }
                             give(b_slot);
@@ -411,36 +433,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return true;
                 };
                 auto issue_value = [&](int s) -> bool {
-                    if (!mbar_wait(&sh.z_full, s & 1, abort_flag, status, lim, PS_ZFULL)) return false;
-                    for (int p = 0; p < C; ++p)
-                        if (p != c) {
-                            if (!mbar_wait_cluster(&sh.zpeer[slot_of(p, c)], s & 1, abort_flag, status, lim, PS_ZPEER))
-                                return false;
-                            // arm the next phase before this step's slot_free lets the writer in
-                            mbar_arrive_expect_tx(&sh.zpeer[slot_of(p, c)], 32768);
-                        }
-                    if (!mbar_wait_cluster(&sh.zpair, s & 1, abort_flag, status, lim, PS_ZPAIR)) return false;
+                    const int bb = zbuf(s);
+                    const uint32_t par = zpar(s);
+                    // own tile: written by both CTAs' elementwise threads
+                    if (!mbar_wait(&sh.z_full[bb], par, abort_flag, status, lim, PS_ZFULL)) return false;
+                    if (!mbar_wait_cluster(&sh.zpair_own[bb], par, abort_flag, status, lim, PS_ZPAIR)) return false;
                     tc_fence_after();
-                    for (int cc = 0; cc < C; ++cc) {
-                        const uint8_t* zs = (cc == c) ? sZown : sZ + slot_of(cc, c) * 32768;
-                        for (int i = 0; i < 2; ++i) {
+                    for (int k = 0; k < C; ++k) {
+                        const int cc = (c + k) % C;
+                        const uint8_t* zs = zslot(k == 0 ? C - 1 : slot_of(cc, c), bb);
+                        if (k > 0) {
+                            // another pair's tile: landed here and (forwarded) in the odd rank
+                            if (!mbar_wait_cluster(&sh.zpeer[slot_of(cc, c)][bb], par, abort_flag, status, lim, PS_ZPEER))
+                                return false;
+                            // arm the buffer's next use before this step's slot_free lets the writer in
+                            mbar_arrive_expect_tx(&sh.zpeer[slot_of(cc, c)][bb], 32768);
+                            if (k == 1 && !mbar_wait_cluster(&sh.zpair_peer[bb], par, abort_flag, status, lim, PS_ZPAIR))
+                                return false;
+                            tc_fence_after();
+                        }
+                        {
                             const uint8_t* W = take();
                             if (!W) return false;
 #pragma unroll
-                            for (int t = 0; t < 4; ++t) {
-                                // keys 64 i + 16 t of the tile: Z chunk i, W rows 16 t (MN-major,
-                                // 64-column blocks 64 keys x 128 bytes apart)
-                                const uint64_t bd = sdesc_sw128(smem_u32(W + t * 2048), 64 * 128, 1024);
-                                const uint32_t acc = (s | cc | i | t) != 0;
-                                umma_f16_pair(t_acc, sdesc_sw128(smem_u32(zs + i * 16384 + t * 32), 16, 1024), bd,
-                                              idesc_v, acc);
+                            for (int t = 0; t < 8; ++t) {
+                                // keys 16 t of the tile: Z chunk t / 4, W rows 16 t (MN-major,
+                                // 64-column blocks 128 keys x 128 bytes apart)
+                                const uint64_t bd = sdesc_sw128(smem_u32(W + t * 2048), 128 * 128, 1024);
+                                const uint32_t acc = (s | k | t) != 0;
+                                umma_f16_pair(t_acc, sdesc_sw128(smem_u32(zs + (t >> 2) * 16384 + (t & 3) * 32), 16, 1024),
+                                              bd, idesc_v, acc);
                             }
                             give(rp.slot);
                             rp.advance(gm.stages);
                         }
+                        // pair cc may overwrite its copy in this buffer once these MMAs are done
+                        if (k > 0) umma_commit_pair_multicast(&sh.slot_free[c][bb], static_cast<uint16_t>(3u << (2 * cc)));
                     }
-                    umma_commit_pair_multicast(&sh.acc, pair_mask);
-                    if (C > 1) umma_commit_pair_multicast(&sh.slot_free[c], others);
+                    umma_commit_pair_multicast(&sh.acc[s & 1], pair_mask);
                     return true;
                 };
                 if (ok && n_steps > 0) ok = issue_score(0);
@@ -458,17 +488,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             // on this CTA's barriers; the MMA thread of the even rank learns of them
             // through one arrival per step.
             if (elect_one()) {
-                const uint32_t lead_zpair = mapa_shared(smem_u32(&sh.zpair), lead_rank);
                 for (int s = 0; s < n_steps; ++s) {
+                    const int bb = zbuf(s);
                     bool ok = true;
                     for (int p = 0; p < C && ok; ++p)
                         if (p != c) {
-                            ok = mbar_wait_cluster(&sh.zpeer[slot_of(p, c)], s & 1, abort_flag, status, lim, PS_FWDR);
-                            if (ok) mbar_arrive_expect_tx(&sh.zpeer[slot_of(p, c)], 32768);
+                            ok = mbar_wait_cluster(&sh.zpeer[slot_of(p, c)][bb], zpar(s), abort_flag, status, lim, PS_FWDR);
+                            if (ok) mbar_arrive_expect_tx(&sh.zpeer[slot_of(p, c)][bb], 32768);
                         }
                     if (!ok) break;
-                    mbar_arrive_remote(lead_zpair);
+                    mbar_arrive_remote(mapa_shared(smem_u32(&sh.zpair_peer[bb]), lead_rank));
                 }
+            }
+        }
+    } else if (warp == 10) {
+        // ------------------------------------------------------ Z copier
+        // Ships the own Z tile of every step, once all 256 elementwise threads
+        // wrote it, into the CTA of every other pair that holds my rows, as one
+        // bulk copy each, once that pair's value products consumed the previous
+        // copy in the target buffer.
+        if (C > 1 && elect_one()) {
+            for (int s = 0; s < n_steps; ++s) {
+                const int bb = zbuf(s);
+                bool ok = mbar_wait(&sh.z_full[bb], zpar(s), abort_flag, status, lim, PS_COPY);
+                for (int k = 1; k < C && ok; ++k) {
+                    const int p = (c + k) % C;
+                    if (s >= nbuf)
+                        ok = mbar_wait_cluster(&sh.slot_free[p][bb], zpar(s) ^ 1u, abort_flag, status, lim, PS_SLOT);
+                    if (ok)
+                        bulk_copy_s2cluster(mapa_shared(smem_u32(zslot(slot_of(c, p), bb)), xrank(p)), zslot(C - 1, bb),
+                                            32768, mapa_shared(smem_u32(&sh.zpeer[slot_of(c, p)][bb]), xrank(p)));
+                }
+                if (!ok) break;
             }
         }
     } else {
@@ -490,7 +541,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = row < row_len;
         const uint32_t lead_xfree0 = mapa_shared(smem_u32(&sh.x_free[0]), lead_rank);
         const uint32_t lead_xfree1 = mapa_shared(smem_u32(&sh.x_free[1]), lead_rank);
-        const uint32_t lead_zpair = mapa_shared(smem_u32(&sh.zpair), lead_rank);
         float l2_row = INFINITY, dl_row = 0.f;  // dQ: own row statistics
         if (OP == XOP_DQ && row_ok) {
             const size_t si = VARLEN ? static_cast<size_t>(h) * pb.total_q + tq0 + row
@@ -501,6 +551,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l_part = 0.f;  // forward softmax state (l over my columns of own tiles)
         bool ok = true;
         auto warp_ok = [&](bool v) { return __all_sync(0xffffffffu, v); };
+        // dV / dK: column statistic of tile t for column r, fetched one step ahead
+        // (half 0: lse2, +inf past the sequence or the last tile; half 1: delta)
+        auto fetch_stat = [&](int t) -> float {
+            const int qi = col_row0(t) + r;
+            const int hh = col_head(t);
+            if (t < n_ct && qi < lq) {
+                const size_t si = VARLEN ? static_cast<size_t>(hh) * pb.total_q + tq0 + qi
+                                         : (static_cast<size_t>(b) * pb.Hq + hh) * pb.Nq + qi;
+                return half == 0 ? a.lse_log2[si] : a.delta[si];
+            }
+            return half == 0 ? INFINITY : 0.f;
+        };
+        float stat_next = (!T::kRowsQ && n_steps > 0) ? fetch_stat(c) : 0.f;
         for (int s = 0; s < n_steps; ++s) {
             const int t = s * C + c;
             const int sb = T::kXdb ? (s & 1) : 0;
@@ -508,22 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ty = t_x0 + 128 + lane_off;  // Y (two-product kernels)
             const int sbuf = s & 1;
             if (!T::kRowsQ) {
-                // stage the column statistics of tile t (threads of half 0): +inf
-                // lse2 masks queries past the sequence and tiles past the end
-                if (half == 0) {
-                    const int qi = col_row0(t) + r;
-                    const int hh = col_head(t);
-                    float l2 = INFINITY, dl = 0.f;
-                    if (t < n_ct && qi < lq) {
-                        const size_t si = VARLEN ? static_cast<size_t>(hh) * pb.total_q + tq0 + qi
-                                                 : (static_cast<size_t>(b) * pb.Hq + hh) * pb.Nq + qi;
-                        l2 = a.lse_log2[si];
-                        dl = a.delta[si];
-                    }
-                    stats[sbuf * 128 + r] = l2;
-                    stats[256 + sbuf * 128 + r] = dl;
-                }
+                // stage the column statistics of tile t: lse2[sbuf][r] (half 0, +inf
+                // masks queries past the sequence and tiles past the end) and
+                // delta[sbuf][r] (half 1); then fetch those of the next step
+                stats[half * 256 + sbuf * 128 + r] = stat_next;
                 mbar_arrive(&sh.stat[sbuf]);
+                if (s + 1 < n_steps) stat_next = fetch_stat(t + C);
             }
             const uint32_t xpar = T::kXdb ? ((s >> 1) & 1) : (s & 1);
             if (!warp_ok(mbar_wait(&sh.x_full[sb], xpar, abort_flag, status, lim, PS_XFULL))) {
@@ -587,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (__any_sync(0xffffffffu, need)) {
                     // O must be stable: wait for the previous super-step's value MMAs;
                     // each half rescales half of the row's accumulator columns
-                    if (s > 0 && !warp_ok(mbar_wait(&sh.acc, (s - 1) & 1, abort_flag, status, lim, PS_ACC))) {
+                    if (s > 0 && !warp_ok(mbar_wait(&sh.acc[(s - 1) & 1], accpar(s - 1), abort_flag, status, lim, PS_ACC))) {
                         ok = false;
                         break;
                     }
@@ -678,48 +731,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(sb ? lead_xfree1 : lead_xfree0);
-            // The own slot may be rewritten once the previous step's value MMAs of my
-            // pair (acc) and of every other pair (slot_free: it consumed my copy, so
-            // the copy has read the slot) are done with it.
-            if (s > 0 && !warp_ok(mbar_wait(&sh.acc, (s - 1) & 1, abort_flag, status, lim, PS_ACC))) {
-                ok = false;
-                break;
-            }
-            if (C > 1 && s > 0) {
-                bool got = true;
+            // Own buffer bb was last used at step s - nbuf: it may be rewritten once the
+            // value MMAs of that step (acc, observed here at every step, in order)
+            // and the copies of it (slot_free of every other pair: it consumed the
+            // copy, so the copy has read the buffer) are done.
+            const int bb = zbuf(s);
+            if (s >= nbuf) {
+                const int sp = s - nbuf;
+                bool got = mbar_wait(&sh.acc[sp & 1], accpar(sp), abort_flag, status, lim, PS_ACC);
                 for (int p = 0; p < C && got; ++p)
-                    if (p != c) got = mbar_wait_cluster(&sh.slot_free[p], (s - 1) & 1, abort_flag, status, lim, PS_SLOT);
+                    if (p != c) got = mbar_wait_cluster(&sh.slot_free[p][bb], zpar(sp), abort_flag, status, lim, PS_SLOT);
                 if (!warp_ok(got)) {
                     ok = false;
                     break;
                 }
             }
+            uint8_t* zown = zslot(C - 1, bb);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<uint4*>(sZown + half * 16384 + sw128_offset(r, u)) =
+                *reinterpret_cast<uint4*>(zown + half * 16384 + sw128_offset(r, u)) =
                     make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
             fence_proxy_async_smem();
-            mbar_arrive(&sh.z_full);
+            mbar_arrive(&sh.z_full[bb]);
             if (!leader) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(lead_zpair);
-            }
-            if (C > 1 && ew == 0) {
-                // one bulk copy of the whole slot into the CTA of every other pair that
-                // holds my rows, once all 256 threads have written it (on a time-out
-                // the copies are skipped; the abort flag then ends every wait)
-                if (mbar_wait(&sh.z_full, s & 1, abort_flag, status, lim, PS_ZFULL)) {
-                    for (int p = 0; p < C; ++p) {
-                        if (p == c) continue;
-                        bulk_copy_s2cluster(mapa_shared(smem_u32(sZ + slot_of(c, p) * 32768), xrank(p)), sZown, 32768,
-                                            mapa_shared(smem_u32(&sh.zpeer[slot_of(c, p)]), xrank(p)));
-                    }
-                }
+                if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sh.zpair_own[bb]), lead_rank));
             }
         }
         // ------------------------------------------------------ epilogue
         if (ok && n_steps > 0) {
-            ok = warp_ok(mbar_wait(&sh.acc, (n_steps - 1) & 1, abort_flag, status, lim, PS_EPI));
+            // the last two steps' value MMAs, in order (earlier ones were observed above)
+            if (n_steps >= 2) ok = warp_ok(mbar_wait(&sh.acc[n_steps & 1], accpar(n_steps - 2), abort_flag, status, lim, PS_EPI));
+            if (ok) ok = warp_ok(mbar_wait(&sh.acc[(n_steps - 1) & 1], accpar(n_steps - 1), abort_flag, status, lim, PS_EPI));
             tc_fence_after();
         }
         float l_tot = 0.f;
@@ -862,23 +905,28 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     PGeo gm;
     gm.C = (d_pad + 255) / 256;
     if (gm.C > kMaxC) return cudaErrorInvalidConfiguration;
-    const int slots_bytes = gm.C * 32768;  // own slot + C-1 slots of the other pairs
     const int budget = kMaxSmem - static_cast<int>(sizeof(StaticSmem));
-    // keep as many leading chunks of the first row operand resident as leave a
-    // ring of >= 10 stages
+    // double-buffer the Z slots when that leaves a ring of >= 4 stages
+    gm.nbuf = (budget - 2 * gm.C * 32768 - pair_stats_bytes(op, gm.C) >= 4 * kSlot) ? 2 : 1;
+    if (const char* e = std::getenv("FFPA_PAIR_NBUF")) gm.nbuf = (e[0] == '1') ? 1 : 2;
+    const int slots_bytes = gm.nbuf * gm.C * 32768;
+    gm.nprod = 2;
+    if (const char* e = std::getenv("FFPA_PAIR_NPROD")) gm.nprod = (e[0] >= '1' && e[0] <= '4') ? e[0] - '0' : 2;
+    // keep as many leading chunk pairs of the first row operand resident as leave
+    // a ring of >= 5 stages (they are reused by every step of the work unit)
     {
-        const int spare = budget - slots_bytes - pair_stats_bytes(op, gm.C) - 10 * kSlot;
-        gm.res = spare > 0 ? spare / kSlot : 0;
-        if (gm.res > nd) gm.res = nd;
+        const int spare = budget - slots_bytes - pair_stats_bytes(op, gm.C) - 5 * kSlot;
+        gm.res = spare > 0 ? 2 * (spare / kSlot) : 0;
+        if (gm.res > ((nd + 1) & ~1)) gm.res = (nd + 1) & ~1;
     }
-    const int fixed = gm.res * kSlot + slots_bytes + pair_stats_bytes(op, gm.C);
+    const int fixed = (gm.res / 2) * kSlot + slots_bytes + pair_stats_bytes(op, gm.C);
     gm.stages = (budget - fixed) / kSlot;
     if (gm.stages > kStages) gm.stages = kStages;
     if (gm.stages < 2) return cudaErrorInvalidConfiguration;
     const int smem = fixed + gm.stages * kSlot;
 
-    // maps: A1, A2 (row side, 128-row boxes of one chunk), B1, B2 (column side,
-    // 64 rows x 2 chunks), W (column side, 64 rows x 2 chunks)
+    // maps (one 32 KiB box each): A1, A2 (row side, 128 rows x 2 chunks), B1, B2
+    // (column side, 64 rows x 4 chunks), W (column side, 128 rows x 2 chunks)
     const void* qp = q_empty ? a.k : a.q;
     const void* dop = q_empty ? a.k : (a.dO ? a.dO : a.q);
     const void* kp = kv_empty ? a.q : a.k;
@@ -887,25 +935,26 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const bool ks = !kv_empty; // side flag of the kv-side maps
     CUtensorMap m[5];
     bool okm = true;
-    auto row = [&](int i, const void* p, bool kv_side) { okm = okm && make_row_map(&m[i], p, pb, kv_side, a.bf16, 128); };
-    auto slab = [&](int i, const void* p, bool kv_side) { okm = okm && make_slab_map(&m[i], p, pb, kv_side, a.bf16, 64, 2); };
+    auto row = [&](int i, const void* p, bool kv_side) { okm = okm && make_slab_map(&m[i], p, pb, kv_side, a.bf16, 128, 2); };
+    auto col = [&](int i, const void* p, bool kv_side) { okm = okm && make_slab_map(&m[i], p, pb, kv_side, a.bf16, 64, 4); };
+    auto val = [&](int i, const void* p, bool kv_side) { okm = okm && make_slab_map(&m[i], p, pb, kv_side, a.bf16, 128, 2); };
     int n_rows;
     int bz;
     switch (op) {
     case XOP_FWD:
-        row(0, qp, qs); row(1, qp, qs); slab(2, kp, ks); slab(3, kp, ks); slab(4, vp, ks);
+        row(0, qp, qs); row(1, qp, qs); col(2, kp, ks); col(3, kp, ks); val(4, vp, ks);
         n_rows = pb.Nq; bz = pb.B * pb.Hq;
         break;
     case XOP_DQ:
-        row(0, qp, qs); row(1, dop, qs); slab(2, kp, ks); slab(3, vp, ks); slab(4, kp, ks);
+        row(0, qp, qs); row(1, dop, qs); col(2, kp, ks); col(3, vp, ks); val(4, kp, ks);
         n_rows = pb.Nq; bz = pb.B * pb.Hq;
         break;
     case XOP_DV:
-        row(0, kp, ks); row(1, kp, ks); slab(2, qp, qs); slab(3, qp, qs); slab(4, dop, qs);
+        row(0, kp, ks); row(1, kp, ks); col(2, qp, qs); col(3, qp, qs); val(4, dop, qs);
         n_rows = pb.Nkv; bz = pb.B * pb.Hkv;
         break;
     default:  // XOP_DK
-        row(0, kp, ks); row(1, vp, ks); slab(2, qp, qs); slab(3, dop, qs); slab(4, qp, qs);
+        row(0, kp, ks); row(1, vp, ks); col(2, qp, qs); col(3, dop, qs); val(4, qp, qs);
         n_rows = pb.Nkv; bz = pb.B * pb.Hkv;
         break;
     }

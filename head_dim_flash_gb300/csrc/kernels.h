@@ -9,10 +9,7 @@
 
 namespace ffpa {
 
-constexpr int kBlockM = 128;   // query rows per tile (one TMEM lane each)
-constexpr int kBlockN = 128;   // keys per tile
 constexpr int kChunk = 64;     // head-dim elements per 128-byte swizzled row
-constexpr int kVKeys = 32;     // keys per V staging chunk
 constexpr int kMaxSmem = 232448;
 
 // Problem description shared by every kernel. Dense problems use B/Nq/Nkv;
@@ -69,9 +66,10 @@ struct XArgs {
     DeviceCtl ctl;
 };
 
-// Runs one of the four GEMM kernels. The CTA-pair form (2-SM MMAs, clusters
-// of 2C CTAs) is the default; FFPA_KERNEL=single in the environment selects
-// the one-CTA-per-slab form (clusters of C CTAs) instead.
+// Runs one of the four GEMM kernels, in the CTA-pair form (2-SM MMAs,
+// clusters of 2C CTAs, head dims that are multiples of 128 up to 768) or the
+// one-CTA-per-slab form (clusters of C CTAs, every other head dim);
+// FFPA_KERNEL=pair|single in the environment forces one of them.
 cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s);
 cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s);
 cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s);

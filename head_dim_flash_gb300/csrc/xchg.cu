@@ -862,11 +862,13 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
 
 cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
 {
-    static const bool single = [] {
-        const char* e = std::getenv("FFPA_KERNEL");
-        return e != nullptr && std::strcmp(e, "single") == 0;
-    }();
-    return single ? launch_single(op, a, s) : launch_pair(op, a, s);
+    // CTA pairs where the head dim splits into 256-column slabs without padding
+    // waste and the cluster stays within 6 CTAs (measured faster there on
+    // GB300); one CTA per slab otherwise. FFPA_KERNEL=pair|single overrides.
+    const char* e = std::getenv("FFPA_KERNEL");
+    const int forced = e == nullptr ? 0 : std::strcmp(e, "single") == 0 ? 1 : (std::strcmp(e, "pair") == 0 ? 2 : 0);
+    const bool pair = forced ? forced == 2 : (a.pb.D % 128 == 0 && a.pb.D <= 768);
+    return pair ? launch_pair(op, a, s) : launch_single(op, a, s);
 }
 
 }  // namespace ffpa

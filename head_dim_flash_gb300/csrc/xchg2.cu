@@ -43,8 +43,6 @@
 // Every per-step barrier is indexed by buffer and every waiter observes each
 // of its phases in order, at most one phase away from the barrier's state,
 // so that the parity waits are exact.
-#include <cstdlib>
-
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tile_common.cuh"
@@ -908,10 +906,8 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const int budget = kMaxSmem - static_cast<int>(sizeof(StaticSmem));
     // double-buffer the Z slots when that leaves a ring of >= 4 stages
     gm.nbuf = (budget - 2 * gm.C * 32768 - pair_stats_bytes(op, gm.C) >= 4 * kSlot) ? 2 : 1;
-    if (const char* e = std::getenv("FFPA_PAIR_NBUF")) gm.nbuf = (e[0] == '1') ? 1 : 2;
     const int slots_bytes = gm.nbuf * gm.C * 32768;
-    gm.nprod = 2;
-    if (const char* e = std::getenv("FFPA_PAIR_NPROD")) gm.nprod = (e[0] >= '1' && e[0] <= '4') ? e[0] - '0' : 2;
+    gm.nprod = 2;  // measured on GB300: 2 lanes beat 1, 3 and 4 with 32 KiB boxes
     // keep as many leading chunk pairs of the first row operand resident as leave
     // a ring of >= 5 stages (they are reused by every step of the work unit)
     {

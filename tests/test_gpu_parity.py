@@ -130,6 +130,37 @@ def test_varlen_matches_oracle(causal):
         check_grad(got, ref, name)
 
 
+# Both kernel families (one CTA per head-dim slab; CTA pairs with 2-SM MMAs)
+# on shapes the automatic choice by head dim would not give them.
+@pytest.mark.parametrize("family", ["single", "pair"])
+@pytest.mark.parametrize("D,causal", [(512, True), (64, False), (320, True), (1024, False)])
+def test_kernel_families(family, D, causal, monkeypatch):
+    monkeypatch.setenv("FFPA_KERNEL", family)
+    run_dense(1, 4, 2, 150, 333, D, causal, dtype=torch.float16, seed=40 + D, amp=0.5)
+
+
+@pytest.mark.parametrize("family", ["single", "pair"])
+def test_kernel_families_varlen_causal(family, monkeypatch):
+    monkeypatch.setenv("FFPA_KERNEL", family)
+    lq = [130, 1, 300]
+    lk = [200, 5, 260]
+    inp = workloads.random_varlen(lq, lk, 2, 1, 512, seed=45)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dO"))
+    cq, ck = inp["cu_seqlens_q"].cuda(), inp["cu_seqlens_k"].cuda()
+    scale = 1 / math.sqrt(512)
+    o, lse = api.varlen_fwd(q, k, v, cq, ck, max(lq), max(lk), True, scale)
+    dq, dk, dv = api.varlen_bwd(q, k, v, o, lse, do, cq, ck, max(lq), max(lk), True, scale)
+    api.get_status()
+    o_ref, lse_ref = oracle.varlen_fwd(inp["q"], inp["k"], inp["v"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                                       True, scale)
+    g_ref = oracle.varlen_bwd(inp["q"], inp["k"], inp["v"], inp["dO"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                              True, scale)
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+    for name, got, ref in zip(("dQ", "dK", "dV"), (dq, dk, dv), g_ref):
+        check_grad(got, ref, name)
+
+
 def test_autograd_entry_points():
     inp = workloads.random_dense(1, 2, 2, 64, 64, 512, torch.bfloat16, seed=31)
     q, k, v = (inp[n].cuda().requires_grad_(True) for n in ("q", "k", "v"))

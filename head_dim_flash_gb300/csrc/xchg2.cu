@@ -380,14 +380,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 auto give = [&](int slot) { umma_commit_pair_multicast(&sh.empty[slot], pair_mask); };
                 auto issue_score = [&](int s) -> bool {
                     const int sb = T::kXdb ? (s & 1) : 0;
-                    // XDB: buffer sb last held X of step s-2 (read by then);
-                    // two-product kernels: X/Y of step s-1 released by the elementwise warps
-                    if (T::kXdb ? s >= 2 : s >= 1) {
-                        const uint32_t par = T::kXdb ? (((s - 2) >> 1) & 1) : ((s - 1) & 1);
-                        if (!mbar_wait_cluster(&sh.x_free[sb], par, abort_flag, status, lim, PS_XFREE)) return false;
-                        tc_fence_after();
-                    }
                     for (int prod = 0; prod < (T::kTwo ? 2 : 1); ++prod) {
+                        // XDB: buffer sb last held X of step s-2 (read by then); two-product
+                        // kernels: X (prod 0) and Y (prod 1) of step s-1, released separately
+                        const int fb = T::kTwo ? prod : sb;
+                        if (T::kXdb ? s >= 2 : s >= 1) {
+                            const uint32_t par = T::kXdb ? (((s - 2) >> 1) & 1) : ((s - 1) & 1);
+                            if (!mbar_wait_cluster(&sh.x_free[fb], par, abort_flag, status, lim, PS_XFREE)) return false;
+                            tc_fence_after();
+                        }
                         const uint32_t dst = t_x0 + (T::kXdb ? sb * 128 : prod * 128);
                         for (int q = 0; q < nb4; ++q) {
                             // A slots hold chunks (4q, 4q+1) and (4q+2, 4q+3), 128 rows each;
@@ -426,8 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             give(b_slot);
                         }
+                        // two-product kernels: X and Y are announced separately
+                        if (T::kTwo) umma_commit_pair_multicast(&sh.x_full[prod], pair_mask);
                     }
-                    umma_commit_pair_multicast(&sh.x_full[sb], pair_mask);
+                    if (!T::kTwo) umma_commit_pair_multicast(&sh.x_full[sb], pair_mask);
                     return true;
                 };
                 auto issue_value = [&](int s) -> bool {
@@ -696,39 +699,78 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool full = j_lo <= col0 && j_hi >= col0 + 64;
                 const float* s_l2 = stats + sbuf * 128;
                 const float* s_dl = stats + 256 + sbuf * 128;
+                if constexpr (!T::kTwo) {
+                    // dV: Z = P^T of my 64 columns
 #pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    uint32_t x[32], y[32];
-                    tmem_ld32(tx + col0 + q2 * 32, x);
-                    if (T::kTwo) tmem_ld32(ty + col0 + q2 * 32, y);
-                    tmem_ld_wait(x);
-                    if (T::kTwo) tmem_ld_wait(y);
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t x[32];
+                        tmem_ld32(tx + col0 + q2 * 32, x);
+                        tmem_ld_wait(x);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float zz[2];
+                        for (int e = 0; e < 16; ++e) {
+                            float zz[2];
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int j = col0 + q2 * 32 + 2 * e + u;
-                            const bool legal = full || (j >= j_lo && j < j_hi);
-                            const float sv = __uint_as_float(x[2 * e + u]);
-                            float v;
-                            if (T::kRowsQ) {  // dQ: dS = P (dP - delta) with the row's statistics
-                                const float p = legal ? ex2_approx(fmaf(sv, c2, -l2_row)) : 0.f;
-                                v = p * (__uint_as_float(y[2 * e + u]) - dl_row);
-                            } else {          // dV: P^T; dK: dS^T = P^T (dP^T - delta)
-                                const float p = legal ? ex2_approx(fmaf(sv, c2, -s_l2[j])) : 0.f;
-                                v = (OP == XOP_DK) ? p * (__uint_as_float(y[2 * e + u]) - s_dl[j]) : p;
+                            for (int u = 0; u < 2; ++u) {
+                                const int j = col0 + q2 * 32 + 2 * e + u;
+                                const bool legal = full || (j >= j_lo && j < j_hi);
+                                zz[u] = legal ? ex2_approx(fmaf(__uint_as_float(x[2 * e + u]), c2, -s_l2[j])) : 0.f;
                             }
-                            zz[u] = v;
+                            z[q2 * 16 + e] = pack2<BF16>(zz[0], zz[1]);
                         }
-                        z[q2 * 16 + e] = pack2<BF16>(zz[0], zz[1]);
+                    }
+                } else {
+                    // dK / dQ: P of my 64 columns from X, kept as fp16 pairs until dP is read
+                    uint32_t pp[32];
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t x[32];
+                        tmem_ld32(tx + col0 + q2 * 32, x);
+                        tmem_ld_wait(x);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            float pv[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int j = col0 + q2 * 32 + 2 * e + u;
+                                const bool legal = full || (j >= j_lo && j < j_hi);
+                                const float l2 = T::kRowsQ ? l2_row : s_l2[j];
+                                pv[u] = legal ? ex2_approx(fmaf(__uint_as_float(x[2 * e + u]), c2, -l2)) : 0.f;
+                            }
+                            pp[q2 * 16 + e] = pack2<false>(pv[0], pv[1]);
+                        }
+                    }
+                    // X is read: the pair's next S product may start while dP is processed
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(lead_xfree0);
+                    if (!warp_ok(mbar_wait(&sh.x_full[1], s & 1, abort_flag, status, lim, PS_XFULL))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // dQ: dS = P (dP - delta) with the row's statistics;
+                    // dK: dS^T = P^T (dP^T - delta) with the columns' statistics
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t y[32];
+                        tmem_ld32(ty + col0 + q2 * 32, y);
+                        tmem_ld_wait(y);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 pv = unpack2<false>(pp[q2 * 16 + e]);
+                            const int j = col0 + q2 * 32 + 2 * e;
+                            const float d0v = T::kRowsQ ? dl_row : s_dl[j];
+                            const float d1v = T::kRowsQ ? dl_row : s_dl[j + 1];
+                            z[q2 * 16 + e] = pack2<BF16>(pv.x * (__uint_as_float(y[2 * e]) - d0v),
+                                                         pv.y * (__uint_as_float(y[2 * e + 1]) - d1v));
+                        }
                     }
                 }
             }
-            // X (and Y) are read: the pair's next score products into this buffer may start
+            // X (dK / dQ: Y) is read: the pair's next score product into this buffer may start
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(sb ? lead_xfree1 : lead_xfree0);
+            if (lane == 0) mbar_arrive_remote((T::kTwo || sb) ? lead_xfree1 : lead_xfree0);
             // Own buffer bb was last used at step s - nbuf: it may be rewritten once the
             // value MMAs of that step (acc, observed here at every step, in order)
             // and the copies of it (slot_free of every other pair: it consumed the

@@ -592,21 +592,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t z[32];  // my 64 columns of Z as packed pairs
             if constexpr (OP == XOP_FWD) {
                 const int limit = key_end - t * 128;  // legal columns [0, limit)
+                // row maximum over the other half's 64 columns, then over mine, which
+                // stay in registers for P (two batched loads, two waits)
+                uint32_t xa[32], xb[32];
+                const int colp = 64 - col0;
+                tmem_ld32(tx + colp, xa);
+                tmem_ld32(tx + colp + 32, xb);
+                tmem_ld_wait(xa, xb);
                 float mx = -INFINITY;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t x[32];
-                    tmem_ld32(tx + q4 * 32, x);
-                    tmem_ld_wait(x);
-                    if (limit >= 128) {
+                auto max32 = [&](const uint32_t (&x)[32], int c_first) {
+                    if (limit >= c_first + 32) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(x[j]));
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (q4 * 32 + j < limit) mx = fmaxf(mx, __uint_as_float(x[j]));
+                            if (c_first + j < limit) mx = fmaxf(mx, __uint_as_float(x[j]));
                     }
-                }
+                };
+                max32(xa, colp);
+                max32(xb, colp + 32);
+                tmem_ld32(tx + col0, xa);
+                tmem_ld32(tx + col0 + 32, xb);
+                tmem_ld_wait(xa, xb);
+                max32(xa, col0);
+                max32(xb, col0 + 32);
                 float m_tile = mx * c2;
                 if (C > 1) {
                     // agree on the row maximum with the CTAs of the other pairs holding
@@ -647,13 +657,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const int half_w = sw / 2;
-                    for (int cc = half * half_w; cc < (half + 1) * half_w; cc += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(t_acc + lane_off + cc, o);
+                    for (int cc = half * half_w; cc < (half + 1) * half_w; cc += 16) {
+                        uint32_t o[16];
+                        tmem_ld16(t_acc + lane_off + cc, o);
                         tmem_ld_wait(o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(t_acc + lane_off + cc, o);
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st16(t_acc + lane_off + cc, o);
                     }
                     tmem_st_wait();
                 }
@@ -663,9 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float sum = 0.f;
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
-                    uint32_t x[32];
-                    tmem_ld32(tx + col0 + q2 * 32, x);
-                    tmem_ld_wait(x);
+                    const uint32_t (&x)[32] = q2 ? xb : xa;
                     const int lim2 = limit - col0 - q2 * 32;
                     if (lim2 >= 32) {
 #pragma unroll
@@ -721,11 +729,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     // dK / dQ: P of my 64 columns from X, kept as fp16 pairs until dP is read
                     uint32_t pp[32];
+                    {
+                    uint32_t xa[32], xb[32];
+                    tmem_ld32(tx + col0, xa);
+                    tmem_ld32(tx + col0 + 32, xb);
+                    tmem_ld_wait(xa, xb);
 #pragma unroll
                     for (int q2 = 0; q2 < 2; ++q2) {
-                        uint32_t x[32];
-                        tmem_ld32(tx + col0 + q2 * 32, x);
-                        tmem_ld_wait(x);
+                        const uint32_t (&x)[32] = q2 ? xb : xa;
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             float pv[2];
@@ -739,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pp[q2 * 16 + e] = pack2<false>(pv[0], pv[1]);
                         }
                     }
+                    }
                     // X is read: the pair's next S product may start while dP is processed
                     tc_fence_before();
                     __syncwarp();
@@ -750,11 +762,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     // dQ: dS = P (dP - delta) with the row's statistics;
                     // dK: dS^T = P^T (dP^T - delta) with the columns' statistics
+                    uint32_t ya[32], yb[32];
+                    tmem_ld32(ty + col0, ya);
+                    tmem_ld32(ty + col0 + 32, yb);
+                    tmem_ld_wait(ya, yb);
 #pragma unroll
                     for (int q2 = 0; q2 < 2; ++q2) {
-                        uint32_t y[32];
-                        tmem_ld32(ty + col0 + q2 * 32, y);
-                        tmem_ld_wait(y);
+                        const uint32_t (&y)[32] = q2 ? yb : ya;
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const float2 pv = unpack2<false>(pp[q2 * 16 + e]);

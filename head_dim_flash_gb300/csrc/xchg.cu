@@ -100,8 +100,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ work unit
     // All CTAs of a cluster share blockIdx.y / blockIdx.z, hence the same unit.
-    const int n_rt = gridDim.y;
-    const int bz = blockIdx.z;
+    // Grid (cluster ranks, row tile, b*H), or (cluster ranks, b*H, row tile)
+    // under causal masking. The hardware starts clusters in linear block order:
+    // the first keeps the clusters that run together on few heads (their K/V
+    // tiles stay in L2); the second starts every head's longest tile before any
+    // head's next one, which balances the unequal causal tiles.
+    const int bz = pb.causal ? blockIdx.y : blockIdx.z;
+    const int tile = pb.causal ? blockIdx.z : blockIdx.y;
     int b, h = 0, hk;
     if (T::kRowsQ) {
         b = bz / pb.Hq;
@@ -122,10 +127,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         lk = pb.Nkv;
     }
     const int off = lk - lq;  // causal: key j legal for query i iff j <= i + off
-    const int rt = (T::kRowsQ && pb.causal) ? (n_rt - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
-    const int r0 = rt * 128;
     const int row_len = T::kRowsQ ? lq : lk;
-    if (r0 >= row_len) return;  // uniform over the cluster, before any cluster barrier
+    // causal, rows = queries: the last row tiles of a sequence see the most keys
+    // and go first; rows = keys: the first key tiles see the most queries
+    const int n_rt_seq = (row_len + 127) / 128;
+    const int rt = (T::kRowsQ && pb.causal) ? (n_rt_seq - 1 - tile) : tile;
+    const int r0 = rt * 128;
+    if (rt < 0 || r0 >= row_len) return;  // uniform over the cluster, before any cluster barrier
 
     int n_ct;            // column tiles of the unit
     int m_start = 0, n_mt = 0;
@@ -766,7 +774,7 @@ cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const Geo& gm, in
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(gm.C, n_rt, bz);
+    cfg.gridDim = a.pb.causal ? dim3(gm.C, bz, n_rt) : dim3(gm.C, n_rt, bz);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

@@ -115,8 +115,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = pb.Hq / pb.Hkv;
 
     // ------------------------------------------------------------ work unit
-    const int n_rt = gridDim.y;  // 256-row tiles
-    const int bz = blockIdx.z;
+    // Grid (cluster ranks, row tile, b*H), or (cluster ranks, b*H, row tile)
+    // under causal masking. The hardware starts clusters in linear block order:
+    // the first keeps the clusters that run together on few heads (their K/V
+    // tiles stay in L2); the second starts every head's longest tile before any
+    // head's next one, which balances the unequal causal tiles.
+    const int bz = pb.causal ? blockIdx.y : blockIdx.z;
+    const int tile = pb.causal ? blockIdx.z : blockIdx.y;
     int b, h = 0, hk;
     if (T::kRowsQ) {
         b = bz / pb.Hq;
@@ -137,11 +142,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         lk = pb.Nkv;
     }
     const int off = lk - lq;  // causal: key j legal for query i iff j <= i + off
-    const int rt = (T::kRowsQ && pb.causal) ? (n_rt - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
+    const int row_len = T::kRowsQ ? lq : lk;
+    // causal, rows = queries: the last row tiles of a sequence see the most keys
+    // and go first; rows = keys: the first key tiles see the most queries
+    const int n_rt_seq = (row_len + 255) / 256;
+    const int rt = (T::kRowsQ && pb.causal) ? (n_rt_seq - 1 - tile) : tile;
     const int R0 = rt * 256;            // first row of the cluster's tile
     const int r0 = R0 + 128 * rh;       // first row of this CTA
-    const int row_len = T::kRowsQ ? lq : lk;
-    if (R0 >= row_len) return;  // uniform over the cluster, before any cluster barrier
+    if (rt < 0 || R0 >= row_len) return;  // uniform over the cluster, before any cluster barrier
 
     // Column tiles of the unit, for all 256 rows (both CTAs of a pair run the
     // same MMAs; rows that a tile does not reach are masked element-wise).
@@ -191,11 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sh.a1, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.x_full[i], 1);
-            mbar_init(&sh.x_free[i], 16);     // 8 elementwise warps of each CTA of the pair
+            // X / Y read: the CTA's 8 elementwise warps (even rank: + 1 arrival forwarded by the odd rank)
+            mbar_init(&sh.x_free[i], leader ? 9 : 8);
             mbar_init(&sh.stat[i], 256);
             mbar_init(&sh.rmax[i], 1);
             mbar_init(&sh.z_full[i], 256);    // own elementwise threads wrote the own Z buffer
-            mbar_init(&sh.zpair_own[i], 8);   // (even rank) the odd rank's 8 elementwise warps did
+            mbar_init(&sh.zpair_own[i], 1);   // (even rank) the odd rank's own Z buffer is written
             mbar_init(&sh.zpair_peer[i], 1);  // (even rank) the odd rank received the other pairs' Z
             mbar_init(&sh.acc[i], 1);
             for (int j = 0; j < kMaxC; ++j) {
@@ -483,22 +492,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int dummy = 0;
                 mbar_wait(&sh.drain, 0, &dummy, status, lim, PS_DRAIN, false);
             }
-        } else if (C > 1) {
+        } else {
             // -------------------------------------------------- forwarder (odd rank)
-            // The other pairs' Z tiles land in this CTA's shared memory and complete
-            // on this CTA's barriers; the MMA thread of the even rank learns of them
-            // through one arrival per step.
+            // Relays this CTA's events to the even rank's MMA thread with one
+            // cluster-scope arrival each, so that the elementwise warps only ever
+            // arrive on barriers of their own CTA: X (and Y) read, own Z buffer
+            // written, and (C > 1) the other pairs' Z tiles landed here. Each kind
+            // of event is forwarded in step order; the kinds are polled together so
+            // that a late one does not hold back the others.
             if (elect_one()) {
-                for (int s = 0; s < n_steps; ++s) {
-                    const int bb = zbuf(s);
-                    bool ok = true;
-                    for (int p = 0; p < C && ok; ++p)
-                        if (p != c) {
-                            ok = mbar_wait_cluster(&sh.zpeer[slot_of(p, c)][bb], zpar(s), abort_flag, status, lim, PS_FWDR);
-                            if (ok) mbar_arrive_expect_tx(&sh.zpeer[slot_of(p, c)][bb], 32768);
+                const int n_x = T::kTwo ? 2 * n_steps : n_steps;
+                int nx = 0, nz = 0, np = 0, kp = 1;
+                uint64_t t_last = global_timer_ns();
+                for (uint32_t it = 1; nx < n_x || nz < n_steps || (C > 1 && np < n_steps); ++it) {
+                    bool progress = false;
+                    if (nx < n_x) {
+                        // event nx: X buffer nx & 1 of step nx (forward, dV), or X (even nx) /
+                        // Y (odd nx) of step nx / 2 (dK, dQ); both reach phase (nx / 2) & 1
+                        const int idx = nx & 1;
+                        const uint32_t par = static_cast<uint32_t>((nx >> 1) & 1);
+                        if (mbar_test(&sh.x_free[idx], par)) {
+                            mbar_arrive_remote(mapa_shared(smem_u32(&sh.x_free[idx]), lead_rank));
+                            ++nx;
+                            progress = true;
                         }
-                    if (!ok) break;
-                    mbar_arrive_remote(mapa_shared(smem_u32(&sh.zpair_peer[bb]), lead_rank));
+                    }
+                    if (nz < n_steps && mbar_test(&sh.z_full[zbuf(nz)], zpar(nz))) {
+                        mbar_arrive_remote(mapa_shared(smem_u32(&sh.zpair_own[zbuf(nz)]), lead_rank));
+                        ++nz;
+                        progress = true;
+                    }
+                    if (C > 1 && np < n_steps) {
+                        // the other pairs' tiles of step np, in pair order c+1, c+2, ...
+                        const int bb = zbuf(np);
+                        const int p = (c + kp) % C;
+                        uint64_t* zb = &sh.zpeer[slot_of(p, c)][bb];
+                        if (mbar_test_cluster(zb, zpar(np))) {
+                            mbar_arrive_expect_tx(zb, 32768);  // arm the buffer's next use
+                            progress = true;
+                            if (++kp == C) {
+                                mbar_arrive_remote(mapa_shared(smem_u32(&sh.zpair_peer[bb]), lead_rank));
+                                kp = 1;
+                                ++np;
+                            }
+                        }
+                    }
+                    if (progress) {
+                        t_last = global_timer_ns();
+                    } else if ((it & 63u) == 0) {
+                        if (*abort_flag || *reinterpret_cast<volatile uint32_t*>(status) != 0u) {
+                            *abort_flag = 1;
+                            break;
+                        }
+                        if (global_timer_ns() - t_last > lim) {
+                            *abort_flag = 1;
+                            const uint32_t blk = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+                            atomicCAS(status, 0u, DEV_TIMEOUT | (PS_FWDR << 8) | (blk << 16));
+                            break;
+                        }
+                    }
                 }
             }
         }
@@ -540,8 +592,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key_end = pb.causal ? min(lk, row + off + 1) : lk;
         const int i_min = pb.causal ? max(0, row - off) : 0;
         const bool row_ok = row < row_len;
-        const uint32_t lead_xfree0 = mapa_shared(smem_u32(&sh.x_free[0]), lead_rank);
-        const uint32_t lead_xfree1 = mapa_shared(smem_u32(&sh.x_free[1]), lead_rank);
         float l2_row = INFINITY, dl_row = 0.f;  // dQ: own row statistics
         if (OP == XOP_DQ && row_ok) {
             const size_t si = VARLEN ? static_cast<size_t>(h) * pb.total_q + tq0 + row
@@ -754,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // X is read: the pair's next S product may start while dP is processed
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(lead_xfree0);
+                    if (lane == 0) mbar_arrive(&sh.x_free[0]);
                     if (!warp_ok(mbar_wait(&sh.x_full[1], s & 1, abort_flag, status, lim, PS_XFULL))) {
                         ok = false;
                         break;
@@ -784,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // X (dK / dQ: Y) is read: the pair's next score product into this buffer may start
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote((T::kTwo || sb) ? lead_xfree1 : lead_xfree0);
+            if (lane == 0) mbar_arrive(&sh.x_free[(T::kTwo || sb) ? 1 : 0]);
             // Own buffer bb was last used at step s - nbuf: it may be rewritten once the
             // value MMAs of that step (acc, observed here at every step, in order)
             // and the copies of it (slot_free of every other pair: it consumed the
@@ -807,10 +857,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
             fence_proxy_async_smem();
             mbar_arrive(&sh.z_full[bb]);
-            if (!leader) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sh.zpair_own[bb]), lead_rank));
-            }
         }
         // ------------------------------------------------------ epilogue
         if (ok && n_steps > 0) {
@@ -922,7 +968,7 @@ cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const PGeo& gm, i
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * gm.C, n_rt, bz);
+    cfg.gridDim = a.pb.causal ? dim3(2 * gm.C, bz, n_rt) : dim3(2 * gm.C, n_rt, bz);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

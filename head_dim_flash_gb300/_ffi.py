@@ -19,8 +19,10 @@ BF16, FP16 = 0, 1
 # Every symbol the header declares (checked by the ABI tests).
 EXPORTS = (
     "ffpa_fwd",
+    "ffpa_fwd_strided",
     "ffpa_bwd_workspace_bytes",
     "ffpa_bwd",
+    "ffpa_bwd_strided",
     "ffpa_bwd_stages",
     "ffpa_bwd_noalloc",
     "ffpa_varlen_fwd",
@@ -43,9 +45,21 @@ _sz = ctypes.c_size_t
 _u64 = ctypes.c_uint64
 
 
+class View(ctypes.Structure):
+    """``ffpa_view``: data pointer and element strides of a [B, H, N, D] tensor."""
+
+    _fields_ = [("data", ctypes.c_void_p), ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64),
+                ("stride_n", ctypes.c_int64)]
+
+
 def _declare(lib):
     lib.ffpa_fwd.argtypes = [_i, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p]
     lib.ffpa_fwd.restype = _i
+    lib.ffpa_fwd_strided.argtypes = [_i, View, View, View, View, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p]
+    lib.ffpa_fwd_strided.restype = _i
+    lib.ffpa_bwd_strided.argtypes = [_i, View, View, View, View, _p, View, View, View, View, _p, _sz, _i, _i, _i, _i,
+                                     _i, _i, _i, _f, _p]
+    lib.ffpa_bwd_strided.restype = _i
     lib.ffpa_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
     lib.ffpa_bwd_workspace_bytes.restype = _sz
     lib.ffpa_bwd.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _p]
@@ -113,6 +127,14 @@ def raise_for(status: int, what: str) -> None:
 # Thin wrappers with the C names (pointers are ints).
 def ffpa_fwd(*args):
     return load().ffpa_fwd(*args)
+
+
+def ffpa_fwd_strided(*args):
+    return load().ffpa_fwd_strided(*args)
+
+
+def ffpa_bwd_strided(*args):
+    return load().ffpa_bwd_strided(*args)
 
 
 def ffpa_bwd_workspace_bytes(*args):

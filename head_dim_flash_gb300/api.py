@@ -10,7 +10,14 @@ ValueError, no silent fallback).
 Layouts (FFPA docs, "CuTe-DSL Backend" page): dense q [B, Hq, Nq, D],
 k/v [B, Hkv, Nkv, D]; packed varlen q [Tq, Hq, D], k/v [Tk, Hkv, D] with
 int32 cu_seqlens; LSE is fp32 [B, Hq, Nq] (dense) or [Hq, Tq] (varlen).
-Non-contiguous inputs are made contiguous first.
+
+Dense tensors are passed as strided views (ffpa_view) with no copy whenever
+the head dim is the innermost, unit-stride dimension and the other strides are
+multiples of 8 elements: contiguous [B, H, N, D] tensors, ``x.transpose(1, 2)``
+of a [B, N, H, D] projection output, slices of a fused QKV buffer. Any other
+layout is copied to a contiguous tensor first. Dense outputs default to the
+layout of the matching input (``torch.empty_like``). Varlen inputs are made
+contiguous.
 """
 from __future__ import annotations
 
@@ -42,6 +49,42 @@ def _prep(*xs):
     return out
 
 
+def _viewable(x: torch.Tensor) -> bool:
+    """True when the dense 4-D tensor can be handed to the kernels as an ffpa_view."""
+    if x.dim() != 4 or x.stride(-1) != 1 or x.data_ptr() % 16 != 0:
+        return False
+    for size, stride in zip(x.shape[:3], x.stride()[:3]):
+        if stride < 0 or stride % 8 != 0 or (size > 1 and stride == 0):
+            return False
+    return True
+
+
+def _dense(*xs):
+    """Dense inputs: checked, and copied only when no view of them fits the ABI."""
+    out = []
+    for x in xs:
+        if not x.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        out.append(x if _viewable(x) else x.contiguous())
+    dt = out[0].dtype
+    for x in out[1:]:
+        if x.dtype != dt:
+            raise ValueError(f"mixed dtypes {dt} and {x.dtype}")
+    return out
+
+
+def _out_like(x: torch.Tensor) -> torch.Tensor:
+    y = torch.empty_like(x)
+    return y if _viewable(y) else torch.empty(x.shape, dtype=x.dtype, device=x.device)
+
+
+def _view(x: torch.Tensor) -> _ffi.View:
+    if not _viewable(x):
+        raise ValueError(f"output of shape {tuple(x.shape)} and strides {x.stride()} is not an ffpa_view "
+                         "(head dim innermost with unit stride, other strides multiples of 8 elements)")
+    return _ffi.View(x.data_ptr(), x.stride(0), x.stride(1), x.stride(2))
+
+
 def _stream() -> int:
     return torch.cuda.current_stream().cuda_stream
 
@@ -52,19 +95,21 @@ def _scale(scale, D):
 
 # ----------------------------------------------------------------- dense
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
-    """Dense forward through ffpa_fwd. Returns (o, lse)."""
-    q, k, v = _prep(q, k, v)
+    """Dense forward through ffpa_fwd_strided (views, no copy). Returns (o, lse)."""
     if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
         raise ValueError("expected q [B,Hq,Nq,D], k and v [B,Hkv,Nkv,D]")
+    q, k, v = _dense(q, k, v)
     B, Hq, Nq, D = q.shape
     Bk, Hkv, Nkv, Dk = k.shape
     if Bk != B or Dk != D:
         raise ValueError("q and k/v disagree on B or D")
-    o = torch.empty_like(q) if out is None else out
+    o = _out_like(q) if out is None else out
     l = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
-    st = _ffi.ffpa_fwd(_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
-                       B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D), _stream())
-    _ffi.raise_for(st, "ffpa_fwd")
+    if not l.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, Hq, Nq] tensor")
+    st = _ffi.ffpa_fwd_strided(_dt(q), _view(q), _view(k), _view(v), _view(o), l.data_ptr(),
+                               B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D), _stream())
+    _ffi.raise_for(st, "ffpa_fwd_strided")
     return o, l
 
 
@@ -76,27 +121,32 @@ def bwd_workspace_bytes(q, k) -> int:
 
 def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None,
         dq=None, dk=None, dv=None, stages: int = 15):
-    """Dense backward through ffpa_bwd (or ffpa_bwd_stages for a subset of its
-    launches: bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK). Returns (dq, dk, dv)."""
-    q, k, v, o, dout = _prep(q, k, v, o, dout)
+    """Dense backward through ffpa_bwd_strided (views, no copy), or ffpa_bwd_stages
+    for a subset of its launches (bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK;
+    contiguous tensors). Returns (dq, dk, dv)."""
+    q, k, v, o, dout = _dense(q, k, v, o, dout)
     lse = lse.contiguous()
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape
     ws_bytes = bwd_workspace_bytes(q, k)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    args = (_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+    dq = _out_like(q) if dq is None else dq
+    dk = _out_like(k) if dk is None else dk
+    dv = _out_like(v) if dv is None else dv
+    tail = (workspace.data_ptr(), workspace.numel() * workspace.element_size(),
             B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D))
     if stages == 15:
-        st = _ffi.ffpa_bwd(*args, _stream())
-        _ffi.raise_for(st, "ffpa_bwd")
+        st = _ffi.ffpa_bwd_strided(_dt(q), _view(q), _view(k), _view(v), _view(o), lse.data_ptr(), _view(dout),
+                                   _view(dq), _view(dk), _view(dv), *tail, _stream())
+        _ffi.raise_for(st, "ffpa_bwd_strided")
     else:
-        st = _ffi.ffpa_bwd_stages(*args, int(stages), _stream())
+        ts = [x.contiguous() for x in (q, k, v, o, dout)]
+        for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
+            if not x.is_contiguous():
+                raise ValueError(f"{name} must be contiguous when stages != 15")
+        st = _ffi.ffpa_bwd_stages(_dt(q), *(x.data_ptr() for x in ts[:4]), lse.data_ptr(), ts[4].data_ptr(),
+                                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), *tail, int(stages), _stream())
         _ffi.raise_for(st, "ffpa_bwd_stages")
     return dq, dk, dv
 

@@ -109,6 +109,36 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 size_t ws_bytes(long rows) { return rows <= 0 ? 0 : 2 * align256(static_cast<size_t>(rows) * sizeof(float)); }
 
+// Strides of a contiguous [B, H, N, D] tensor, and of a packed [T, H, D] one.
+ffpa::View contiguous_view(int H, int N, int D)
+{
+    return ffpa::View{static_cast<long long>(H) * N * D, static_cast<long long>(N) * D, D};
+}
+
+ffpa::View packed_view(int H, int D) { return ffpa::View{0, D, static_cast<long long>(H) * D}; }
+
+// A strided view as the ABI describes it: strides are multiples of 8 elements
+// (16 bytes), non-negative, positive along every dimension with more than one
+// entry, and below 2^39 elements (the tensor-map limit of 2^40 bytes).
+ffpa_status check_view(const ffpa_view& v, bool needed, const char* name, int B, int H, int N)
+{
+    if (!needed) return FFPA_OK;
+    if (!v.data) return fail(FFPA_ERR_INVALID_VALUE, "%s: data is NULL", name);
+    if (reinterpret_cast<uintptr_t>(v.data) & 15u) return fail(FFPA_ERR_INVALID_VALUE, "%s: data is not 16-byte aligned", name);
+    const int64_t st[3] = {v.stride_b, v.stride_h, v.stride_n};
+    const int ext[3] = {B, H, N};
+    const char* dim[3] = {"stride_b", "stride_h", "stride_n"};
+    for (int i = 0; i < 3; ++i) {
+        if (st[i] < 0 || st[i] % 8 != 0 || st[i] >= (int64_t(1) << 39))
+            return fail(FFPA_ERR_INVALID_VALUE, "%s: %s=%lld must be a non-negative multiple of 8 below 2^39", name, dim[i],
+                        (long long)st[i]);
+        if (ext[i] > 1 && st[i] == 0) return fail(FFPA_ERR_INVALID_VALUE, "%s: %s is 0 for an extent of %d", name, dim[i], ext[i]);
+    }
+    return FFPA_OK;
+}
+
+ffpa::View to_view(const ffpa_view& v) { return ffpa::View{v.stride_b, v.stride_h, v.stride_n}; }
+
 ffpa::Problem dense_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale)
 {
     ffpa::Problem pb{};
@@ -122,6 +152,8 @@ ffpa::Problem dense_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int 
     pb.causal = causal ? 1 : 0;
     pb.scale = scale;
     pb.scale_log2 = scale * 1.4426950408889634f;
+    pb.vq = pb.vo = pb.vdo = pb.vdq = contiguous_view(Hq, Nq, D);
+    pb.vk = pb.vv = pb.vdk = pb.vdv = contiguous_view(Hkv, Nkv, D);
     return pb;
 }
 
@@ -222,6 +254,8 @@ ffpa::Problem varlen_problem(int batch, int total_q, int total_k, int max_q, int
     pb.total_k = total_k;
     pb.cu_q = cu_q;
     pb.cu_k = cu_k;
+    pb.vq = pb.vo = pb.vdo = pb.vdq = packed_view(Hq, D);
+    pb.vk = pb.vv = pb.vdk = pb.vdv = packed_view(Hkv, D);
     return pb;
 }
 
@@ -263,6 +297,25 @@ ffpa_status ffpa_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v,
     return run_fwd(dt, q, k, v, o, lse, dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, scale), q_rows, k_rows, stream);
 }
 
+ffpa_status ffpa_fwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o, float* lse, int B,
+                             int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale, ffpa_stream_t stream)
+{
+    FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
+    FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
+    const long q_rows = static_cast<long>(B) * Hq * Nq;
+    const long k_rows = static_cast<long>(B) * Hkv * Nkv;
+    FFPA_TRY(check_view(q, q_rows > 0, "q", B, Hq, Nq));
+    FFPA_TRY(check_view(o, q_rows > 0, "o", B, Hq, Nq));
+    FFPA_TRY(check_view(k, q_rows > 0 && k_rows > 0, "k", B, Hkv, Nkv));
+    FFPA_TRY(check_view(v, q_rows > 0 && k_rows > 0, "v", B, Hkv, Nkv));
+    ffpa::Problem pb = dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, scale);
+    pb.vq = to_view(q);
+    pb.vo = to_view(o);
+    pb.vk = to_view(k);
+    pb.vv = to_view(v);
+    return run_fwd(dt, q.data, k.data, v.data, o.data, lse, pb, q_rows, k_rows, stream);
+}
+
 size_t ffpa_bwd_workspace_bytes(ffpa_dtype, int B, int Hq, int, int Nq, int, int)
 {
     if (B < 0 || Hq < 0 || Nq < 0) return 0;
@@ -279,6 +332,36 @@ ffpa_status ffpa_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v,
     const long k_rows = static_cast<long>(B) * Hkv * Nkv;
     return run_bwd(dt, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes,
                    dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, scale), q_rows, k_rows, q_rows, 15u, stream);
+}
+
+ffpa_status ffpa_bwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o, const float* lse,
+                             ffpa_view dO, ffpa_view dq, ffpa_view dk, ffpa_view dv, void* workspace,
+                             size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal,
+                             float scale, ffpa_stream_t stream)
+{
+    FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
+    FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
+    const long q_rows = static_cast<long>(B) * Hq * Nq;
+    const long k_rows = static_cast<long>(B) * Hkv * Nkv;
+    FFPA_TRY(check_view(q, q_rows > 0, "q", B, Hq, Nq));
+    FFPA_TRY(check_view(o, q_rows > 0, "o", B, Hq, Nq));
+    FFPA_TRY(check_view(dO, q_rows > 0, "dO", B, Hq, Nq));
+    FFPA_TRY(check_view(dq, q_rows > 0, "dq", B, Hq, Nq));
+    FFPA_TRY(check_view(k, k_rows > 0, "k", B, Hkv, Nkv));
+    FFPA_TRY(check_view(v, k_rows > 0, "v", B, Hkv, Nkv));
+    FFPA_TRY(check_view(dk, k_rows > 0, "dk", B, Hkv, Nkv));
+    FFPA_TRY(check_view(dv, k_rows > 0, "dv", B, Hkv, Nkv));
+    ffpa::Problem pb = dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, scale);
+    pb.vq = to_view(q);
+    pb.vo = to_view(o);
+    pb.vdo = to_view(dO);
+    pb.vdq = to_view(dq);
+    pb.vk = to_view(k);
+    pb.vv = to_view(v);
+    pb.vdk = to_view(dk);
+    pb.vdv = to_view(dv);
+    return run_bwd(dt, q.data, k.data, v.data, o.data, lse, dO.data, dq.data, dk.data, dv.data, workspace,
+                   workspace_bytes, pb, q_rows, k_rows, q_rows, 15u, stream);
 }
 
 ffpa_status ffpa_bwd_stages(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,

@@ -19,14 +19,7 @@
 namespace ffpa {
 namespace {
 
-constexpr int kBwdThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 elementwise
-constexpr int kMaxStages = 12;
 constexpr float kLog2e = 1.4426950408889634f;
-
-enum BwdSite : uint32_t {
-    BSITE_PROD = 16, BSITE_MMA_FULL, BSITE_MMA_SEMPTY, BSITE_MMA_PFULL, BSITE_EW_SFULL, BSITE_EW_PDONE,
-    BSITE_EPI, BSITE_DRAIN
-};
 
 // ----------------------------------------------------------------- preprocess
 // One warp per query row: delta = dO . O (fp32) and lse2 = LSE*log2e
@@ -41,16 +34,21 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdArgs a, lo
     const int lane = threadIdx.x & 31;
     const int D = pb.D;
     for (long r = warp_global; r < rows; r += n_warps) {
-        // r indexes the LSE layout: dense [B*Hq, Nq], packed [Hq, T]
-        size_t off;
+        // r indexes the LSE layout: dense [B, Hq, Nq] (row i of head h of batch b),
+        // packed [Hq, T] (token t of head h); O and dO are read through their views
+        long bb = 0, h, i;
         if (pb.varlen) {
-            const long h = r / pb.total_q, t = r % pb.total_q;
-            off = (static_cast<size_t>(t) * pb.Hq + h) * D;
+            h = r / pb.total_q;
+            i = r % pb.total_q;
         } else {
-            off = static_cast<size_t>(r) * D;
+            bb = r / (static_cast<long>(pb.Hq) * pb.Nq);
+            h = (r / pb.Nq) % pb.Hq;
+            i = r % pb.Nq;
         }
-        const uint4* o4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.o) + off);
-        const uint4* d4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.dO) + off);
+        const size_t off_o = bb * pb.vo.sb + h * pb.vo.sh + i * pb.vo.sn;
+        const size_t off_d = bb * pb.vdo.sb + h * pb.vdo.sh + i * pb.vdo.sn;
+        const uint4* o4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.o) + off_o);
+        const uint4* d4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.dO) + off_d);
         float acc = 0.f;
         for (int i = lane; i < D / 8; i += lanes) {
             const uint4 x = o4[i], y = d4[i];
@@ -70,45 +68,6 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdArgs a, lo
             a.lse_log2[r] = (l == -INFINITY) ? INFINITY : l * kLog2e;
         }
     }
-}
-
-// Per-sequence geometry of a work unit.
-struct SeqGeom {
-    int b, lq, lk, tq0, tk0;
-};
-
-template <bool VARLEN>
-__device__ __forceinline__ SeqGeom seq_geom(const Problem& pb, int b)
-{
-    SeqGeom g;
-    g.b = b;
-    if constexpr (VARLEN) {
-        g.tq0 = pb.cu_q[b];
-        g.lq = pb.cu_q[b + 1] - g.tq0;
-        g.tk0 = pb.cu_k[b];
-        g.lk = pb.cu_k[b + 1] - g.tk0;
-    } else {
-        g.tq0 = g.tk0 = 0;
-        g.lq = pb.Nq;
-        g.lk = pb.Nkv;
-    }
-    return g;
-}
-
-// Index of a row statistic (lse2 / delta) of query i of head h.
-template <bool VARLEN>
-__device__ __forceinline__ size_t stat_index(const Problem& pb, const SeqGeom& g, int h, int i)
-{
-    if constexpr (VARLEN) return static_cast<size_t>(h) * pb.total_q + g.tq0 + i;
-    else return (static_cast<size_t>(g.b) * pb.Hq + h) * pb.Nq + i;
-}
-
-// Element offset of row `i` (of head h with H heads) of a dense or packed tensor.
-template <bool VARLEN>
-__device__ __forceinline__ size_t row_offset(const Problem& pb, int b, int H, int N, int t0, int h, int i)
-{
-    if constexpr (VARLEN) return (static_cast<size_t>(t0 + i) * H + h) * pb.D;
-    else return ((static_cast<size_t>(b) * H + h) * N + i) * pb.D;
 }
 
 template <bool BF16, bool VARLEN>

@@ -1,5 +1,5 @@
 // Host-side helpers: driver entry point for TMA descriptor encoding, tensor
-// maps over the dense and packed layouts, device queries.
+// maps over strided dense views and the packed varlen layout, device queries.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -23,80 +23,73 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Dense tensors [B, H, N, D] are described as 3-D (D, N, B*H) so that a box
-// never crosses from one head into the next (rows past N read as zero).
-// Packed tensors [T, H, D] are described as (D, H, T); a box of rows then
-// walks along tokens of one head.
-bool make_row_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int box_rows)
+namespace {
+
+// Extents and byte strides of a tensor seen as (rows, heads, batch).
+struct Geometry {
+    uint64_t rows, heads, batch;
+    uint64_t s_row, s_head, s_batch;  // bytes
+};
+
+Geometry geometry(const Problem& pb, bool kv_side, const View& v)
+{
+    Geometry g;
+    g.heads = static_cast<uint64_t>(kv_side ? pb.Hkv : pb.Hq);
+    if (pb.varlen) {
+        g.rows = static_cast<uint64_t>(kv_side ? pb.total_k : pb.total_q);
+        g.batch = 1;
+    } else {
+        g.rows = static_cast<uint64_t>(kv_side ? pb.Nkv : pb.Nq);
+        g.batch = static_cast<uint64_t>(pb.B);
+    }
+    g.s_row = static_cast<uint64_t>(v.sn) * 2;
+    g.s_head = static_cast<uint64_t>(v.sh) * 2;
+    g.s_batch = static_cast<uint64_t>(v.sb) * 2;
+    // A dimension with a single entry is never stepped over; give it a valid
+    // stride (a positive multiple of 16 bytes) whatever the caller passed.
+    const uint64_t any = static_cast<uint64_t>(pb.D) * 2;
+    if (g.rows <= 1 && g.s_row == 0) g.s_row = any;
+    if (g.heads <= 1 && g.s_head == 0) g.s_head = any;
+    if (g.batch <= 1 && g.s_batch == 0) g.s_batch = any;
+    if (g.rows == 0) g.rows = 1;
+    if (g.heads == 0) g.heads = 1;
+    if (g.batch == 0) g.batch = 1;
+    return g;
+}
+
+}  // namespace
+
+bool make_row_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int box_rows,
+                  const View& v)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const uint64_t D = static_cast<uint64_t>(pb.D);
-    const uint64_t H = static_cast<uint64_t>(kv_side ? pb.Hkv : pb.Hq);
-    cuuint64_t dims[3];
-    cuuint64_t strides[2];
-    cuuint32_t box[3];
-    const cuuint32_t es[3] = {1, 1, 1};
-    if (!pb.varlen) {
-        const uint64_t N = static_cast<uint64_t>(kv_side ? pb.Nkv : pb.Nq);
-        dims[0] = D;
-        dims[1] = N;
-        dims[2] = static_cast<uint64_t>(pb.B) * H;
-        strides[0] = D * 2;
-        strides[1] = N * D * 2;
-        box[0] = kChunk;
-        box[1] = static_cast<cuuint32_t>(box_rows);
-        box[2] = 1;
-    } else {
-        const uint64_t T = static_cast<uint64_t>(kv_side ? pb.total_k : pb.total_q);
-        dims[0] = D;
-        dims[1] = H;
-        dims[2] = T;
-        strides[0] = D * 2;
-        strides[1] = H * D * 2;
-        box[0] = kChunk;
-        box[1] = 1;
-        box[2] = static_cast<cuuint32_t>(box_rows);
-    }
-    const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+    const Geometry g = geometry(pb, kv_side, v);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(pb.D), g.rows, g.heads, g.batch};
+    const cuuint64_t strides[3] = {g.s_row, g.s_head, g.s_batch};
+    const cuuint32_t box[4] = {kChunk, static_cast<cuuint32_t>(box_rows), 1, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-// Tensor map that reads a D-slab of `rows` consecutive rows in ONE box: the
-// head dim is split into (64 elements, D/64 chunks) and the box is
-// 64 x rows x chunks, so shared memory receives [chunk][row][64] (128-byte
-// swizzled rows), i.e. `chunks` row-blocks of rows x 128 bytes back to back.
-// Dense: dims (64, N, D/64, B*H); packed: dims (64, T, D/64, H).
-bool make_slab_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int rows, int chunks)
+// The head dim is split into (64 elements, D/64 chunks) with a 128-byte chunk
+// stride, so one box of rows x chunks lands in shared memory as `chunks`
+// row-blocks of rows x 128 bytes back to back.
+bool make_slab_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int rows, int chunks,
+                   const View& v)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const uint64_t D = static_cast<uint64_t>(pb.D);
-    const uint64_t H = static_cast<uint64_t>(kv_side ? pb.Hkv : pb.Hq);
-    cuuint64_t dims[4];
-    cuuint64_t strides[3];
-    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(chunks), 1};
-    const cuuint32_t es[4] = {1, 1, 1, 1};
-    dims[0] = 64;
-    dims[2] = D / 64;
-    strides[1] = 128;  // next 64-element chunk of the same row
-    if (!pb.varlen) {
-        const uint64_t N = static_cast<uint64_t>(kv_side ? pb.Nkv : pb.Nq);
-        dims[1] = N;
-        dims[3] = static_cast<uint64_t>(pb.B) * H;
-        strides[0] = D * 2;
-        strides[2] = N * D * 2;
-    } else {
-        const uint64_t T = static_cast<uint64_t>(kv_side ? pb.total_k : pb.total_q);
-        dims[1] = T;
-        dims[3] = H;
-        strides[0] = H * D * 2;
-        strides[2] = D * 2;
-    }
-    const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+    const Geometry g = geometry(pb, kv_side, v);
+    const cuuint64_t dims[5] = {64, g.rows, static_cast<cuuint64_t>(pb.D / 64), g.heads, g.batch};
+    const cuuint64_t strides[4] = {g.s_row, 128, g.s_head, g.s_batch};
+    const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(chunks), 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
                            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -12,6 +12,13 @@ namespace ffpa {
 constexpr int kChunk = 64;     // head-dim elements per 128-byte swizzled row
 constexpr int kMaxSmem = 232448;
 
+// Element strides of a tensor seen as [B, H, N, D] (head-dim stride 1).
+// Dense tensors may be strided views; packed varlen tensors [T, H, D] are
+// described with sn = H*D (one token), sh = D and sb unused (one batch).
+struct View {
+    long long sb, sh, sn;
+};
+
 // Problem description shared by every kernel. Dense problems use B/Nq/Nkv;
 // varlen problems use cu_q/cu_k with Nq/Nkv holding the max sequence lengths.
 struct Problem {
@@ -23,6 +30,7 @@ struct Problem {
     int causal;
     float scale;        // softmax scale
     float scale_log2;   // scale * log2(e)
+    View vq, vk, vv, vo, vdo, vdq, vdk, vdv;  // layouts of the eight tensors
 };
 
 struct DeviceCtl {
@@ -80,13 +88,18 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_fn();
 
-// Tensor map over rows of head-dim vectors: dense [BH, N, D] or packed [T, H, D].
-// Box = 64 head-dim elements x `box_rows` rows, 128-byte swizzle.
-bool make_row_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int box_rows);
+// Tensor map over rows of head-dim vectors of a tensor with layout `v`,
+// 4-D (D, rows, heads, batch): rows are N (dense) or tokens (packed), batch
+// is B (dense) or 1 (packed). Box = 64 head-dim elements x `box_rows` rows,
+// 128-byte swizzle; coordinates (d, row or token, head, b or 0).
+bool make_row_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int box_rows,
+                  const View& v);
 
 // Tensor map reading `rows` rows x `chunks` 64-wide head-dim chunks in one box
-// (shared-memory layout [chunk][row][64], 128-byte swizzle).
-bool make_slab_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int rows, int chunks);
+// (shared-memory layout [chunk][row][64], 128-byte swizzle), 5-D
+// (64, rows, D/64, heads, batch); coordinates (0, row or token, chunk, head, b or 0).
+bool make_slab_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_side, bool bf16, int rows, int chunks,
+                   const View& v);
 
 // True when the query side / key side of a problem has no rows at all. Such a
 // side has no storage; tensor maps for it are built over the other side's

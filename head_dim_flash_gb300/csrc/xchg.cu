@@ -247,15 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tc = min(t, n_ct - 1);
         return T::kRowsQ ? tc * 128 : (m_start + tc % max(n_mt, 1)) * 128;
     };
-    // TMA coordinates. Dense maps: (d, row, b*H + head); packed maps: (d, head, token).
-    auto q_c1 = [&](int head, int row) { return VARLEN ? head : row; };
-    auto q_c2 = [&](int head, int row) { return VARLEN ? tq0 + row : b * pb.Hq + head; };
-    auto k_c1 = [&](int head, int row) { return VARLEN ? head : row; };
-    auto k_c2 = [&](int head, int row) { return VARLEN ? tk0 + row : b * pb.Hkv + head; };
-    auto row_c1 = [&](int row) { return T::kRowsQ ? q_c1(h, row) : k_c1(hk, row); };
-    auto row_c2 = [&](int row) { return T::kRowsQ ? q_c2(h, row) : k_c2(hk, row); };
-    auto col_c1 = [&](int head, int row) { return T::kRowsQ ? k_c1(head, row) : q_c1(head, row); };
-    auto col_c2 = [&](int head, int row) { return T::kRowsQ ? k_c2(head, row) : q_c2(head, row); };
+    // TMA coordinates: row maps (d, row or token, head, b or 0), slab maps
+    // (0, row or token, chunk, head, b or 0).
+    const int bco = VARLEN ? 0 : b;
+    const int row_head = T::kRowsQ ? h : hk;
+    auto row_co = [&](int row) { return VARLEN ? (T::kRowsQ ? tq0 : tk0) + row : row; };
+    auto col_co = [&](int row) { return VARLEN ? (T::kRowsQ ? tk0 : tq0) + row : row; };
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -266,30 +263,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             RingPos rp;
             int issued = 0;
             bool ok = true;
-            auto put = [&](const CUtensorMap* m, int boxes, int box_bytes, int x0, int y, int z) -> bool {
+            // one 64 x 128-row box of chunk d
+            auto put = [&](const CUtensorMap* m, int d, int row, int head) -> bool {
                 if (!mbar_wait(&bar_empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, XS_PROD)) return false;
                 uint8_t* dst = sRing + rp.slot * 16384;
-                mbar_arrive_expect_tx(&bar_full[rp.slot], boxes * box_bytes);
-                for (int i = 0; i < boxes; ++i) tma_load_3d(dst + i * box_bytes, m, &bar_full[rp.slot], x0 + i * 64, y, z);
+                mbar_arrive_expect_tx(&bar_full[rp.slot], 16384);
+                tma_load_4d(dst, m, &bar_full[rp.slot], d * 64, row, head, bco);
                 rp.advance(gm.stages);
                 ++issued;
                 return true;
             };
             if (gm.res > 0 && n_steps > 0) {
                 mbar_arrive_expect_tx(&bar_a1, gm.res * 16384);
-                for (int d = 0; d < gm.res; ++d) tma_load_3d(sA1 + d * 16384, &tA1, &bar_a1, d * 64, row_c1(r0), row_c2(r0));
+                for (int d = 0; d < gm.res; ++d) tma_load_4d(sA1 + d * 16384, &tA1, &bar_a1, d * 64, row_co(r0), row_head, bco);
             }
             auto load_score = [&](int s) -> bool {
                 const int t = s * C + c;
                 const int hh = col_head(t), cr = col_row0(t);
                 for (int d = 0; d < nd; ++d) {
-                    if (d >= gm.res && !put(&tA1, 1, 16384, d * 64, row_c1(r0), row_c2(r0))) return false;
-                    if (!put(&tB1, 1, 16384, d * 64, col_c1(hh, cr), col_c2(hh, cr))) return false;
+                    if (d >= gm.res && !put(&tA1, d, row_co(r0), row_head)) return false;
+                    if (!put(&tB1, d, col_co(cr), hh)) return false;
                 }
                 if (T::kTwo)
                     for (int d = 0; d < nd; ++d) {
-                        if (!put(&tA2, 1, 16384, d * 64, row_c1(r0), row_c2(r0))) return false;
-                        if (!put(&tB2, 1, 16384, d * 64, col_c1(hh, cr), col_c2(hh, cr))) return false;
+                        if (!put(&tA2, d, row_co(r0), row_head)) return false;
+                        if (!put(&tB2, d, col_co(cr), hh)) return false;
                     }
                 return true;
             };
@@ -304,14 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!mbar_wait(&bar_empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, XS_PROD)) return false;
                         uint8_t* dst = sRing + rp.slot * 16384;
                         mbar_arrive_expect_tx(&bar_full[rp.slot], wbytes);
-                        const int row = cr + vc * 32;
-                        if (VARLEN) {
-                            const int tok = T::kRowsQ ? tk0 + row : tq0 + row;
-                            tma_load_4d(dst, &tW, &bar_full[rp.slot], 0, tok, c_begin, hh);
-                        } else {
-                            const int bhh = T::kRowsQ ? b * pb.Hkv + hh : b * pb.Hq + hh;
-                            tma_load_4d(dst, &tW, &bar_full[rp.slot], 0, row, c_begin, bhh);
-                        }
+                        tma_load_5d(dst, &tW, &bar_full[rp.slot], 0, col_co(cr + vc * 32), c_begin, hh, bco);
                         rp.advance(gm.stages);
                         ++issued;
                     }
@@ -698,33 +689,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             float mul;
             void* out;
-            int out_heads, out_n, t0, head;
+            View ov;
             if (OP == XOP_FWD) {
                 mul = l_tot > 0.f ? 1.f / l_tot : 0.f;
                 out = a.o;
+                ov = pb.vo;
             } else if (OP == XOP_DQ) {
                 mul = pb.scale;
                 out = a.dq;
+                ov = pb.vdq;
             } else if (OP == XOP_DV) {
                 mul = 1.f;
                 out = a.dv;
+                ov = pb.vdv;
             } else {
                 mul = pb.scale;
                 out = a.dk;
+                ov = pb.vdk;
             }
-            if (T::kRowsQ) {
-                out_heads = pb.Hq;
-                out_n = pb.Nq;
-                t0 = tq0;
-                head = h;
-            } else {
-                out_heads = pb.Hkv;
-                out_n = pb.Nkv;
-                t0 = tk0;
-                head = hk;
-            }
-            const size_t orow = VARLEN ? (static_cast<size_t>(t0 + row) * out_heads + head) * pb.D
-                                       : ((static_cast<size_t>(b) * out_heads + head) * out_n + row) * pb.D;
+            // element offset of the output row in its (strided or packed) layout
+            const size_t orow = static_cast<size_t>(bco) * ov.sb + static_cast<size_t>(row_head) * ov.sh +
+                                static_cast<size_t>(row_co(row)) * ov.sn;
             uint16_t* dst = reinterpret_cast<uint16_t*>(out) + orow + d0;
             for (int cc = half * (sw / 2); cc < (half + 1) * (sw / 2); cc += 32) {
                 uint32_t v[32];
@@ -827,34 +812,39 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
     const int smem = fixed + gm.stages * 16384;
 
     // maps: A1, A2 (row side, 128-row boxes), B1, B2 (column side, 128-row boxes), W (32-row boxes)
-    const void* qp = q_empty ? a.k : a.q;
-    const void* dop = q_empty ? a.k : (a.dO ? a.dO : a.q);
-    const void* kp = kv_empty ? a.q : a.k;
-    const void* vp = kv_empty ? a.q : a.v;
-    const bool qs = !q_empty ? false : true;  // side flag of the q-side maps (kv side when q is empty)
-    const bool ks = !kv_empty;                // side flag of the kv-side maps
+    // An empty side has no storage: its maps are built over the other side's
+    // tensor (and layout) and are never loaded from.
+    struct Src {
+        const void* p;
+        View v;
+        bool kv_side;
+    };
+    const Src sq = q_empty ? Src{a.k, pb.vk, true} : Src{a.q, pb.vq, false};
+    const Src sdo = q_empty ? Src{a.k, pb.vk, true} : (a.dO ? Src{a.dO, pb.vdo, false} : sq);
+    const Src sk = kv_empty ? Src{a.q, pb.vq, false} : Src{a.k, pb.vk, true};
+    const Src sv = kv_empty ? Src{a.q, pb.vq, false} : Src{a.v, pb.vv, true};
     CUtensorMap m[5];
     bool okm = true;
-    auto mk = [&](int i, const void* p, bool kv_side, int rows) {
-        okm = okm && (rows == 32 ? make_slab_map(&m[i], p, pb, kv_side, a.bf16, 32, gm.slab_chunks)
-                                 : make_row_map(&m[i], p, pb, kv_side, a.bf16, rows));
+    auto mk = [&](int i, const Src& x, int rows) {
+        okm = okm && (rows == 32 ? make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 32, gm.slab_chunks, x.v)
+                                 : make_row_map(&m[i], x.p, pb, x.kv_side, a.bf16, rows, x.v));
     };
     int n_rt, bz;
     switch (op) {
     case XOP_FWD:
-        mk(0, qp, qs, 128); mk(1, qp, qs, 128); mk(2, kp, ks, 128); mk(3, kp, ks, 128); mk(4, vp, ks, 32);
+        mk(0, sq, 128); mk(1, sq, 128); mk(2, sk, 128); mk(3, sk, 128); mk(4, sv, 32);
         n_rt = (pb.Nq + 127) / 128; bz = pb.B * pb.Hq;
         break;
     case XOP_DQ:
-        mk(0, qp, qs, 128); mk(1, dop, qs, 128); mk(2, kp, ks, 128); mk(3, vp, ks, 128); mk(4, kp, ks, 32);
+        mk(0, sq, 128); mk(1, sdo, 128); mk(2, sk, 128); mk(3, sv, 128); mk(4, sk, 32);
         n_rt = (pb.Nq + 127) / 128; bz = pb.B * pb.Hq;
         break;
     case XOP_DV:
-        mk(0, kp, ks, 128); mk(1, kp, ks, 128); mk(2, qp, qs, 128); mk(3, qp, qs, 128); mk(4, dop, qs, 32);
+        mk(0, sk, 128); mk(1, sk, 128); mk(2, sq, 128); mk(3, sq, 128); mk(4, sdo, 32);
         n_rt = (pb.Nkv + 127) / 128; bz = pb.B * pb.Hkv;
         break;
     default:  // XOP_DK
-        mk(0, kp, ks, 128); mk(1, vp, ks, 128); mk(2, qp, qs, 128); mk(3, dop, qs, 128); mk(4, qp, qs, 32);
+        mk(0, sk, 128); mk(1, sv, 128); mk(2, sq, 128); mk(3, sdo, 128); mk(4, sq, 32);
         n_rt = (pb.Nkv + 127) / 128; bz = pb.B * pb.Hkv;
         break;
     }

@@ -269,17 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tc = min(t, n_ct - 1);
         return T::kRowsQ ? tc * 128 : (m_start + tc % max(n_mt, 1)) * 128;
     };
-    // TMA coordinates of the 4-D maps: dense (64, row, chunk, b*H + head), packed
-    // (64, token, chunk, head). On the column side:
-    auto col_slab_row = [&](int head, int row) {
-        return VARLEN ? (T::kRowsQ ? tk0 + row : tq0 + row) : row;
-    };
-    auto col_slab_head = [&](int head) {
-        return VARLEN ? head : (T::kRowsQ ? b * pb.Hkv + head : b * pb.Hq + head);
-    };
-    // ... and on the row side (the unit's own head)
-    auto row_slab_row = [&](int row) { return VARLEN ? (T::kRowsQ ? tq0 + row : tk0 + row) : row; };
-    auto row_slab_head = [&]() { return VARLEN ? (T::kRowsQ ? h : hk) : (T::kRowsQ ? b * pb.Hq + h : b * pb.Hkv + hk); };
+    // TMA coordinates of the 5-D maps: (0, row or token, chunk, head, b or 0).
+    const int bco = VARLEN ? 0 : b;
+    const int row_head = T::kRowsQ ? h : hk;
+    auto row_co = [&](int row) { return VARLEN ? (T::kRowsQ ? tq0 : tk0) + row : row; };
+    auto col_co = [&](int row) { return VARLEN ? (T::kRowsQ ? tk0 : tq0) + row : row; };
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producers
@@ -306,12 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             auto lead_full = [&](int slot) { return mapa_shared(smem_u32(&sh.full[slot]), lead_rank); };
             // one 4-D box into the next ring position, if that position is mine
-            auto put = [&](const CUtensorMap* m, int row_coord, int chunk, int head_coord) -> bool {
+            auto put = [&](const CUtensorMap* m, int row_coord, int chunk, int head) -> bool {
                 bool got = true;
                 if (pos % nprod == me) {
                     got = mbar_wait(&sh.empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, PS_PROD);
                     if (got)
-                        tma_load_4d_pair(sRing + rp.slot * kSlot, m, lead_full(rp.slot), 0, row_coord, chunk, head_coord);
+                        tma_load_5d_pair(sRing + rp.slot * kSlot, m, lead_full(rp.slot), 0, row_coord, chunk, head, bco);
                 }
                 rp.advance(gm.stages);
                 ++pos;
@@ -320,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (me == 0 && gm.res > 0 && n_steps > 0) {
                 const uint32_t a1 = mapa_shared(smem_u32(&sh.a1), lead_rank);
                 for (int j = 0; 2 * j < gm.res; ++j)
-                    tma_load_4d_pair(sA1 + j * kSlot, &tA1, a1, 0, row_slab_row(r0), 2 * j, row_slab_head());
+                    tma_load_5d_pair(sA1 + j * kSlot, &tA1, a1, 0, row_co(r0), 2 * j, row_head, bco);
             }
             // score operands of step s, per product and per group of four chunks q:
             // A(4q, 4q+1), B(4q .. 4q+3), A(4q+2, 4q+3)
@@ -331,11 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const CUtensorMap* mA = prod ? &tA2 : &tA1;
                     const CUtensorMap* mB = prod ? &tB2 : &tB1;
                     for (int q = 0; q < nb4; ++q) {
-                        if (!(prod == 0 && 4 * q < gm.res) && !put(mA, row_slab_row(r0), 4 * q, row_slab_head()))
-                            return false;
-                        if (!put(mB, col_slab_row(hh, cr), 4 * q, col_slab_head(hh))) return false;
-                        if (4 * q + 2 < nd && !(prod == 0 && 4 * q + 2 < gm.res) &&
-                            !put(mA, row_slab_row(r0), 4 * q + 2, row_slab_head()))
+                        if (!(prod == 0 && 4 * q < gm.res) && !put(mA, row_co(r0), 4 * q, row_head)) return false;
+                        if (!put(mB, col_co(cr), 4 * q, hh)) return false;
+                        if (4 * q + 2 < nd && !(prod == 0 && 4 * q + 2 < gm.res) && !put(mA, row_co(r0), 4 * q + 2, row_head))
                             return false;
                     }
                 }
@@ -347,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < C; ++k) {
                     const int t = s * C + (c + k) % C;
                     const int hh = col_head(t);
-                    if (!put(&tW, col_slab_row(hh, col_row0(t)), w_chunk, col_slab_head(hh))) return false;
+                    if (!put(&tW, col_co(col_row0(t)), w_chunk, hh)) return false;
                 }
                 return true;
             };
@@ -890,33 +882,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             float mul;
             void* out;
-            int out_heads, out_n, t0, head;
+            View ov;
             if (OP == XOP_FWD) {
                 mul = l_tot > 0.f ? 1.f / l_tot : 0.f;
                 out = a.o;
+                ov = pb.vo;
             } else if (OP == XOP_DQ) {
                 mul = pb.scale;
                 out = a.dq;
+                ov = pb.vdq;
             } else if (OP == XOP_DV) {
                 mul = 1.f;
                 out = a.dv;
+                ov = pb.vdv;
             } else {
                 mul = pb.scale;
                 out = a.dk;
+                ov = pb.vdk;
             }
-            if (T::kRowsQ) {
-                out_heads = pb.Hq;
-                out_n = pb.Nq;
-                t0 = tq0;
-                head = h;
-            } else {
-                out_heads = pb.Hkv;
-                out_n = pb.Nkv;
-                t0 = tk0;
-                head = hk;
-            }
-            const size_t orow = VARLEN ? (static_cast<size_t>(t0 + row) * out_heads + head) * pb.D
-                                       : ((static_cast<size_t>(b) * out_heads + head) * out_n + row) * pb.D;
+            // element offset of the output row in its (strided or packed) layout
+            const size_t orow = static_cast<size_t>(bco) * ov.sb + static_cast<size_t>(row_head) * ov.sh +
+                                static_cast<size_t>(row_co(row)) * ov.sn;
             uint16_t* dst = reinterpret_cast<uint16_t*>(out) + orow + d0;
             const int c_end = min((half + 1) * (sw / 2), pb.D - d0);  // columns past D are not stored
             for (int cc = half * (sw / 2); cc < c_end; cc += 32) {
@@ -1025,34 +1011,39 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
 
     // maps (one 32 KiB box each): A1, A2 (row side, 128 rows x 2 chunks), B1, B2
     // (column side, 64 rows x 4 chunks), W (column side, 128 rows x 2 chunks)
-    const void* qp = q_empty ? a.k : a.q;
-    const void* dop = q_empty ? a.k : (a.dO ? a.dO : a.q);
-    const void* kp = kv_empty ? a.q : a.k;
-    const void* vp = kv_empty ? a.q : a.v;
-    const bool qs = q_empty;   // side flag of the q-side maps (kv side when q is empty)
-    const bool ks = !kv_empty; // side flag of the kv-side maps
+    // An empty side has no storage: its maps are built over the other side's
+    // tensor (and layout) and are never loaded from.
+    struct Src {
+        const void* p;
+        View v;
+        bool kv_side;
+    };
+    const Src sq = q_empty ? Src{a.k, pb.vk, true} : Src{a.q, pb.vq, false};
+    const Src sdo = q_empty ? Src{a.k, pb.vk, true} : (a.dO ? Src{a.dO, pb.vdo, false} : sq);
+    const Src sk = kv_empty ? Src{a.q, pb.vq, false} : Src{a.k, pb.vk, true};
+    const Src sv = kv_empty ? Src{a.q, pb.vq, false} : Src{a.v, pb.vv, true};
     CUtensorMap m[5];
     bool okm = true;
-    auto row = [&](int i, const void* p, bool kv_side) { okm = okm && make_slab_map(&m[i], p, pb, kv_side, a.bf16, 128, 2); };
-    auto col = [&](int i, const void* p, bool kv_side) { okm = okm && make_slab_map(&m[i], p, pb, kv_side, a.bf16, 64, 4); };
-    auto val = [&](int i, const void* p, bool kv_side) { okm = okm && make_slab_map(&m[i], p, pb, kv_side, a.bf16, 128, 2); };
+    auto row = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 128, 2, x.v); };
+    auto col = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 64, 4, x.v); };
+    auto val = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 128, 2, x.v); };
     int n_rows;
     int bz;
     switch (op) {
     case XOP_FWD:
-        row(0, qp, qs); row(1, qp, qs); col(2, kp, ks); col(3, kp, ks); val(4, vp, ks);
+        row(0, sq); row(1, sq); col(2, sk); col(3, sk); val(4, sv);
         n_rows = pb.Nq; bz = pb.B * pb.Hq;
         break;
     case XOP_DQ:
-        row(0, qp, qs); row(1, dop, qs); col(2, kp, ks); col(3, vp, ks); val(4, kp, ks);
+        row(0, sq); row(1, sdo); col(2, sk); col(3, sv); val(4, sk);
         n_rows = pb.Nq; bz = pb.B * pb.Hq;
         break;
     case XOP_DV:
-        row(0, kp, ks); row(1, kp, ks); col(2, qp, qs); col(3, qp, qs); val(4, dop, qs);
+        row(0, sk); row(1, sk); col(2, sq); col(3, sq); val(4, sdo);
         n_rows = pb.Nkv; bz = pb.B * pb.Hkv;
         break;
     default:  // XOP_DK
-        row(0, kp, ks); row(1, vp, ks); col(2, qp, qs); col(3, dop, qs); val(4, qp, qs);
+        row(0, sk); row(1, sv); col(2, sq); col(3, sdo); val(4, sq);
         n_rows = pb.Nkv; bz = pb.B * pb.Hkv;
         break;
     }

@@ -20,7 +20,8 @@
  * with fp32 accumulation; P is rounded to the input type before P*V.
  *
  * Memory and ownership: every pointer argument is DEVICE memory owned by the
- * caller, 16-byte aligned, contiguous in the layout stated per call. The
+ * caller, 16-byte aligned, contiguous in the layout stated per call (the
+ * *_strided calls take strided views instead, see ffpa_view). The
  * library allocates nothing; backward scratch lives in a caller-provided
  * workspace of at least *_bwd_workspace_bytes(...) bytes.
  *
@@ -83,6 +84,35 @@ FFPA_API ffpa_status ffpa_fwd(ffpa_dtype dt, const void* q, const void* k, const
                      int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale,
                      ffpa_stream_t stream);
 
+/*
+ * A strided view of a dense [B, H, N, D] tensor for the *_strided calls:
+ * element (b, h, n, d) lives at data + (b*stride_b + h*stride_h + n*stride_n + d)
+ * elements (the head-dim stride is 1). Covers the contiguous [B, H, N, D]
+ * layout (stride_n = D, stride_h = N*D, stride_b = H*N*D), the [B, N, H, D]
+ * layout that QKV projections produce (stride_n = H*D, stride_h = D,
+ * stride_b = N*H*D) and views into fused QKV buffers, with no copy (FFPA
+ * docs, "CuTe-DSL Backend" page: the dense SDPA layout; zero-copy strided and
+ * fused-QKV inputs are the extension the FFPA pages list for later backends).
+ * Requirements: data 16-byte aligned; every stride a multiple of 8 elements
+ * (16 bytes) and positive when its dimension has more than one entry. Output
+ * views must not overlap themselves or any input; overlapping inputs (for
+ * example k and v in one fused buffer) are fine.
+ */
+typedef struct ffpa_view {
+    void* data;
+    int64_t stride_b, stride_h, stride_n;
+} ffpa_view;
+
+/*
+ * Dense forward on strided views (otherwise as ffpa_fwd). q, o: [B, Hq, Nq, D]
+ * views; k, v: [B, Hkv, Nkv, D] views; lse stays a contiguous fp32
+ * [B, Hq, Nq] array. Strides that break the requirements above return
+ * FFPA_ERR_INVALID_VALUE before any launch.
+ */
+FFPA_API ffpa_status ffpa_fwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o, float* lse,
+                                      int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale,
+                                      ffpa_stream_t stream);
+
 /* Workspace bytes ffpa_bwd needs for this problem (fp32 row statistics). */
 FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 
@@ -101,6 +131,17 @@ FFPA_API ffpa_status ffpa_bwd(ffpa_dtype dt, const void* q, const void* k, const
                      void* workspace, size_t workspace_bytes,
                      int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale,
                      ffpa_stream_t stream);
+
+/*
+ * Dense backward on strided views (otherwise as ffpa_bwd; the workspace is
+ * sized by ffpa_bwd_workspace_bytes). q, o, dO, dq: [B, Hq, Nq, D] views;
+ * k, v, dk, dv: [B, Hkv, Nkv, D] views; lse: contiguous fp32 [B, Hq, Nq].
+ */
+FFPA_API ffpa_status ffpa_bwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o,
+                                      const float* lse, ffpa_view dO, ffpa_view dq, ffpa_view dk, ffpa_view dv,
+                                      void* workspace, size_t workspace_bytes,
+                                      int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale,
+                                      ffpa_stream_t stream);
 
 /*
  * The launches of ffpa_bwd, selectable: bit 0 = preprocess (delta and scaled

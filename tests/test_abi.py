@@ -121,3 +121,49 @@ def test_python_api_rejects_unsupported_dtype_before_the_library():
 
     with pytest.raises(NotImplementedError):
         api._dt(torch.zeros(1, dtype=torch.float32))
+
+
+def _view(ptr=FAKE, sb=2 * 8 * 512, sh=8 * 512, sn=512):
+    from head_dim_flash_gb300 import _ffi
+
+    return _ffi.View(ptr, sb, sh, sn)
+
+
+@pytest.mark.parametrize("which,bad", [
+    ("q", dict(sn=100)),             # stride not a multiple of 8 elements
+    ("q", dict(sh=0)),               # zero stride along Hq = 2 heads
+    ("o", dict(ptr=FAKE + 8)),       # misaligned data
+    ("v", dict(sb=-8)),              # negative stride
+    ("k", dict(sn=1 << 39)),         # beyond the tensor-map stride limit
+    ("o", dict(ptr=0)),              # NULL with a non-empty problem
+])
+def test_invalid_strided_views_are_rejected(lib, which, bad):
+    views = {name: _view() for name in ("q", "k", "v", "o")}
+    views[which] = _view(**bad)
+    st = lib.ffpa_fwd_strided(0, views["q"], views["k"], views["v"], views["o"], FAKE, 1, 2, 1, 8, 8, 512, 0, 0.05,
+                              None)
+    assert st == 1
+    assert which.encode() in lib.ffpa_last_error()
+
+
+def test_strided_backward_checks_every_view(lib):
+    good = _view()
+    args = [good] * 4 + [FAKE] + [good, good, good, _view(sn=12)]  # dv stride not a multiple of 8
+    n = lib.ffpa_bwd_workspace_bytes(0, 1, 2, 1, 8, 8, 512)
+    assert lib.ffpa_bwd_strided(0, *args, FAKE, n, 1, 2, 1, 8, 8, 512, 0, 0.05, None) == 1
+    assert b"dv" in lib.ffpa_last_error()
+
+
+def test_python_views_are_zero_copy_for_common_layouts():
+    import torch
+
+    from head_dim_flash_gb300 import api
+
+    B, N, H, D = 2, 5, 3, 64
+    bnhd = torch.zeros(B, N, H, D, dtype=torch.bfloat16)
+    assert api._viewable(torch.zeros(B, H, N, D, dtype=torch.bfloat16))
+    assert api._viewable(bnhd.transpose(1, 2))                       # [B, N, H, D] storage
+    fused = torch.zeros(B, N, 3, H, D, dtype=torch.bfloat16)
+    assert api._viewable(fused[:, :, 1].transpose(1, 2))             # K slice of a fused QKV buffer
+    assert not api._viewable(torch.zeros(B, H, D, N, dtype=torch.bfloat16).transpose(2, 3))  # head dim strided
+    assert not api._viewable(torch.zeros(B, H, N, D + 4, dtype=torch.bfloat16)[..., :D])      # row stride 68

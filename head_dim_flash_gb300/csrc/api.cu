@@ -70,8 +70,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 ffpa_status check_common(ffpa_dtype dt, int Hq, int Hkv, int D, float scale)
 {
     if (dt != FFPA_BF16 && dt != FFPA_FP16) return fail(FFPA_ERR_NOT_SUPPORTED, "dtype %d: only bf16 (0) and fp16 (1)", (int)dt);
-    if (D < 64 || D > 1024 || D % 64 != 0)
-        return fail(FFPA_ERR_NOT_SUPPORTED, "head dim D=%d: supported D is a multiple of 64 in [64, 1024]", D);
+    if (D < 64 || D > 1024 || D % 32 != 0)
+        return fail(FFPA_ERR_NOT_SUPPORTED, "head dim D=%d: supported D is a multiple of 32 in [64, 1024]", D);
     if (Hq < 0 || Hkv < 0) return fail(FFPA_ERR_INVALID_VALUE, "negative head count Hq=%d Hkv=%d", Hq, Hkv);
     if (Hq > 0 && (Hkv == 0 || Hq % Hkv != 0))
         return fail(FFPA_ERR_INVALID_VALUE, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);

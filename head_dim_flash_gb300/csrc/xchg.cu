@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int n_steps = (n_ct + C - 1) / C;
 
-    const int nd = pb.D / 64;
+    const int nd = (pb.D + 63) / 64;  // 64-wide head-dim chunks (the last one half-filled when D % 64 = 32)
     const int c_begin = c * gm.slab_chunks;
     const int nb = min(gm.slab_chunks, nd - c_begin);  // 64-wide blocks in my slab
     const int sw = nb * 64;
@@ -301,8 +301,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int vc = 0; vc < 4; ++vc) {
                         if (!mbar_wait(&bar_empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, XS_PROD)) return false;
                         uint8_t* dst = sRing + rp.slot * 16384;
-                        mbar_arrive_expect_tx(&bar_full[rp.slot], wbytes);
-                        tma_load_5d(dst, &tW, &bar_full[rp.slot], 0, col_co(cr + vc * 32), c_begin, hh, bco);
+                        if (pb.D % 64 == 0) {
+                            mbar_arrive_expect_tx(&bar_full[rp.slot], wbytes);
+                            tma_load_5d(dst, &tW, &bar_full[rp.slot], 0, col_co(cr + vc * 32), c_begin, hh, bco);
+                        } else {
+                            // head dim not a multiple of 64: one 64 x 32 box per chunk of my
+                            // slab from a row map over the true D (the tail reads as zero)
+                            mbar_arrive_expect_tx(&bar_full[rp.slot], nb * 32 * 128);
+                            for (int i = 0; i < nb; ++i)
+                                tma_load_4d(dst + i * 32 * 128, &tW, &bar_full[rp.slot], (c_begin + i) * 64,
+                                            col_co(cr + vc * 32), hh, bco);
+                        }
                         rp.advance(gm.stages);
                         ++issued;
                     }
@@ -711,7 +720,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t orow = static_cast<size_t>(bco) * ov.sb + static_cast<size_t>(row_head) * ov.sh +
                                 static_cast<size_t>(row_co(row)) * ov.sn;
             uint16_t* dst = reinterpret_cast<uint16_t*>(out) + orow + d0;
-            for (int cc = half * (sw / 2); cc < (half + 1) * (sw / 2); cc += 32) {
+            const int c_end = min((half + 1) * (sw / 2), pb.D - d0);  // columns past D are not stored
+            for (int cc = half * (sw / 2); cc < c_end; cc += 32) {
                 uint32_t v[32];
                 if (n_steps > 0) {
                     tmem_ld32(t_acc + lane_off + cc, v);
@@ -791,7 +801,7 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
     const bool q_empty = q_side_empty(pb), kv_empty = kv_side_empty(pb);
     const bool rows_q = (op == XOP_FWD || op == XOP_DQ);
     if (rows_q ? q_empty : kv_empty) return cudaSuccess;  // no output rows
-    const int nd = pb.D / 64;
+    const int nd = (pb.D + 63) / 64;
     Geo gm;
     gm.C = (nd + 3) / 4;
     gm.slab_chunks = (nd + gm.C - 1) / gm.C;
@@ -826,8 +836,10 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
     CUtensorMap m[5];
     bool okm = true;
     auto mk = [&](int i, const Src& x, int rows) {
-        okm = okm && (rows == 32 ? make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 32, gm.slab_chunks, x.v)
-                                 : make_row_map(&m[i], x.p, pb, x.kv_side, a.bf16, rows, x.v));
+        // value operand: one box of 32 rows x the slab's chunks, or (D % 64 != 0) a
+        // row map read chunk by chunk
+        okm = okm && (rows == 32 && pb.D % 64 == 0 ? make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 32, gm.slab_chunks, x.v)
+                                                   : make_row_map(&m[i], x.p, pb, x.kv_side, a.bf16, rows, x.v));
     };
     int n_rt, bz;
     switch (op) {
@@ -865,7 +877,8 @@ cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
     // GB300); one CTA per slab otherwise. FFPA_KERNEL=pair|single overrides.
     const char* e = std::getenv("FFPA_KERNEL");
     const int forced = e == nullptr ? 0 : std::strcmp(e, "single") == 0 ? 1 : (std::strcmp(e, "pair") == 0 ? 2 : 0);
-    const bool pair = forced ? forced == 2 : (a.pb.D % 128 == 0 && a.pb.D <= 768);
+    // (head dims that are not a multiple of 64 only run in the one-CTA form)
+    const bool pair = a.pb.D % 64 == 0 && (forced ? forced == 2 : (a.pb.D % 128 == 0 && a.pb.D <= 768));
     return pair ? launch_pair(op, a, s) : launch_single(op, a, s);
 }
 

@@ -986,6 +986,7 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const bool q_empty = q_side_empty(pb), kv_empty = kv_side_empty(pb);
     const bool rows_q = (op == XOP_FWD || op == XOP_DQ);
     if (rows_q ? q_empty : kv_empty) return cudaSuccess;  // no output rows
+    if (pb.D % 64 != 0) return cudaErrorInvalidConfiguration;  // chunked 5-D maps need D % 64 == 0
     const int nd = pb.D / 64;
     const int d_pad = (pb.D + 127) & ~127;
     PGeo gm;

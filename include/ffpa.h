@@ -15,8 +15,9 @@
  *   query heads of each kv group).
  *
  * Element types: bf16 or fp16 for q, k, v, o, dO, dq, dk, dv (one type per
- * call); lse is fp32. Head dim D: a multiple of 64 in [64, 1024] (the FFPA
- * tuned range 320..1024 included). The arithmetic runs on tcgen05 tensor cores
+ * call); lse is fp32. Head dim D: a multiple of 32 in [64, 1024] (the FFPA
+ * tuned range 320..1024 included; head dims that are not a multiple of 64 read
+ * their last 64-wide chunk half from zero fill). The arithmetic runs on tcgen05 tensor cores
  * with fp32 accumulation; P is rounded to the input type before P*V.
  *
  * Memory and ownership: every pointer argument is DEVICE memory owned by the
@@ -35,7 +36,8 @@
  *                           non-finite scale, too small a workspace, bad
  *                           cu_seqlens sizes;
  *   FFPA_ERR_NOT_SUPPORTED  dtype other than bf16/fp16, D outside the range
- *                           above, a device that is not compute capability 10.3;
+ *                           above or not a multiple of 32, a device that is
+ *                           not compute capability 10.3;
  *   FFPA_ERR_CUDA           a CUDA runtime/driver call failed (launch error);
  * and nothing is launched. A problem with no work (B, H or N zero) returns
  * FFPA_OK without a launch. Every device-side wait in the kernels is bounded;

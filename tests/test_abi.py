@@ -79,6 +79,15 @@ def test_invalid_forward_calls_are_rejected(lib, kw, status):
     assert lib.ffpa_last_error()  # a message explains the rejection
 
 
+def test_head_dims_multiple_of_32_pass_the_dim_check(lib):
+    # D = 96, 160: accepted by the head-dim check (a later check, here the NaN
+    # scale, rejects the call before any device work); D = 100, 80: not
+    for D in (96, 160, 992):
+        assert fwd(lib, D=D, scale=float("nan")) == 1
+    for D in (100, 80, 1056):
+        assert fwd(lib, D=D, scale=float("nan")) == 2
+
+
 def test_empty_problem_is_ok_without_launch(lib):
     assert fwd(lib, B=0, q=0, k=0, v=0, o=0, lse=0) == 0
     assert fwd(lib, Nq=0, q=0, o=0, lse=0, k=0, v=0) == 0

@@ -86,6 +86,13 @@ def test_head_dims(D):
     run_dense(1, 2, 1, 200, 260, D, False, dtype=torch.float16, seed=D, amp=0.5)
 
 
+@pytest.mark.parametrize("D,causal,dtype", [(96, False, torch.float16), (160, True, torch.bfloat16),
+                                             (352, True, torch.float16), (736, False, torch.bfloat16)])
+def test_head_dims_multiple_of_32(D, causal, dtype):
+    # D % 64 = 32: the last 64-wide chunk is half zero fill
+    run_dense(1, 4, 2, 200, 260, D, causal, dtype=dtype, seed=D + 1, amp=0.5)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_cross_attention_gqa(causal):
     # Nq < Nkv bottom-right causal with a 4-way GQA group

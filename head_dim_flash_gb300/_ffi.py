@@ -23,6 +23,8 @@ EXPORTS = (
     "ffpa_bwd_workspace_bytes",
     "ffpa_bwd",
     "ffpa_bwd_strided",
+    "ffpa_decode_workspace_bytes",
+    "ffpa_decode_fwd",
     "ffpa_bwd_stages",
     "ffpa_bwd_noalloc",
     "ffpa_varlen_fwd",
@@ -60,6 +62,10 @@ def _declare(lib):
     lib.ffpa_bwd_strided.argtypes = [_i, View, View, View, View, _p, View, View, View, View, _p, _sz, _i, _i, _i, _i,
                                      _i, _i, _i, _f, _p]
     lib.ffpa_bwd_strided.restype = _i
+    lib.ffpa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+    lib.ffpa_decode_workspace_bytes.restype = _sz
+    lib.ffpa_decode_fwd.argtypes = [_i, View, View, View, View, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _p]
+    lib.ffpa_decode_fwd.restype = _i
     lib.ffpa_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
     lib.ffpa_bwd_workspace_bytes.restype = _sz
     lib.ffpa_bwd.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _p]
@@ -135,6 +141,14 @@ def ffpa_fwd_strided(*args):
 
 def ffpa_bwd_strided(*args):
     return load().ffpa_bwd_strided(*args)
+
+
+def ffpa_decode_workspace_bytes(*args):
+    return load().ffpa_decode_workspace_bytes(*args)
+
+
+def ffpa_decode_fwd(*args):
+    return load().ffpa_decode_fwd(*args)
 
 
 def ffpa_bwd_workspace_bytes(*args):

@@ -113,6 +113,36 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     return o, l
 
 
+DECODE_ROWS = 16  # (Hq / Hkv) * Nq query rows per kv head that the decode path takes
+
+
+def decode_supported(q, k) -> bool:
+    """True when ffpa_decode_fwd takes this problem (few query rows per kv head, D % 64 == 0)."""
+    B, Hq, Nq, D = q.shape
+    Hkv = k.shape[1]
+    return Hkv > 0 and Hq % Hkv == 0 and (Hq // Hkv) * Nq <= DECODE_ROWS and D % 64 == 0
+
+
+def decode_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, workspace=None):
+    """Decode / short-query forward through ffpa_decode_fwd (split over the keys).
+    Same result as fwd(); raises NotImplementedError outside decode_supported()."""
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,Hq,Nq,D], k and v [B,Hkv,Nkv,D]")
+    q, k, v = _dense(q, k, v)
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    o = _out_like(q) if out is None else out
+    l = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = int(_ffi.ffpa_decode_workspace_bytes(_dt(q), B, Hq, Hkv, Nq, Nkv, D))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = _ffi.ffpa_decode_fwd(_dt(q), _view(q), _view(k), _view(v), _view(o), l.data_ptr(), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), B, Hq, Hkv, Nq, Nkv, D,
+                              int(bool(causal)), _scale(scale, D), _stream())
+    _ffi.raise_for(st, "ffpa_decode_fwd")
+    return o, l
+
+
 def bwd_workspace_bytes(q, k) -> int:
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape

@@ -316,6 +316,52 @@ ffpa_status ffpa_fwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view 
     return run_fwd(dt, q.data, k.data, v.data, o.data, lse, pb, q_rows, k_rows, stream);
 }
 
+size_t ffpa_decode_workspace_bytes(ffpa_dtype, int B, int Hq, int Hkv, int Nq, int Nkv, int D)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nkv < 0 || D <= 0 || Hq % Hkv != 0) return 0;
+    return ffpa::decode_plan(dense_problem(B, Hq, Hkv, Nq, Nkv, D, 0, 1.f)).workspace_bytes;
+}
+
+ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o, float* lse,
+                            void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                            int causal, float scale, ffpa_stream_t stream)
+{
+    FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
+    FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
+    if (D % 64 != 0) return fail(FFPA_ERR_NOT_SUPPORTED, "decode path: D=%d must be a multiple of 64", D);
+    if (Hq > 0 && static_cast<long>(Hq / Hkv) * Nq > ffpa::kDecodeRows)
+        return fail(FFPA_ERR_NOT_SUPPORTED, "decode path: (Hq/Hkv)*Nq=%ld query rows per kv head exceed %d",
+                    static_cast<long>(Hq / Hkv) * Nq, ffpa::kDecodeRows);
+    const long q_rows = static_cast<long>(B) * Hq * Nq;
+    const long k_rows = static_cast<long>(B) * Hkv * Nkv;
+    FFPA_TRY(check_view(q, q_rows > 0, "q", B, Hq, Nq));
+    FFPA_TRY(check_view(o, q_rows > 0, "o", B, Hq, Nq));
+    FFPA_TRY(check_view(k, q_rows > 0 && k_rows > 0, "k", B, Hkv, Nkv));
+    FFPA_TRY(check_view(v, q_rows > 0 && k_rows > 0, "v", B, Hkv, Nkv));
+    FFPA_TRY(check_ptr(lse, q_rows > 0, "lse"));
+    if (q_rows == 0) return ok();
+    ffpa::Problem pb = dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, scale);
+    pb.vq = to_view(q);
+    pb.vo = to_view(o);
+    pb.vk = to_view(k);
+    pb.vv = to_view(v);
+    const size_t need = ffpa::decode_plan(pb).workspace_bytes;
+    if (workspace_bytes < need)
+        return fail(FFPA_ERR_INVALID_VALUE, "decode workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(FFPA_ERR_INVALID_VALUE, "decode workspace must be non-NULL and 256-byte aligned");
+    ffpa::FwdArgs a{};
+    a.pb = pb;
+    FFPA_TRY(device_ctl(&a.ctl));
+    a.bf16 = dt == FFPA_BF16;
+    a.q = q.data;
+    a.k = k.data;
+    a.v = v.data;
+    a.o = o.data;
+    a.lse = lse;
+    return launch_result(ffpa::launch_decode(a, workspace, reinterpret_cast<cudaStream_t>(stream)), "decode launch");
+}
+
 size_t ffpa_bwd_workspace_bytes(ffpa_dtype, int B, int Hq, int, int Nq, int, int)
 {
     if (B < 0 || Hq < 0 || Nq < 0) return 0;

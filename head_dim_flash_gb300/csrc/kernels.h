@@ -114,6 +114,17 @@ int num_sms();
 int set_error(int status, const char* fmt, ...);
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
+
+// Decode / short-query forward (split over the keys): dense problems with
+// (Hq / Hkv) * Nq <= kDecodeRows query rows per kv head and D % 64 == 0.
+constexpr int kDecodeRows = 16;
+constexpr int kDecodeMaxSplits = 64;
+struct DecodePlan {
+    int splits, tiles_per, kt, chunks;
+    size_t workspace_bytes;  // partial outputs and LSE of every split
+};
+DecodePlan decode_plan(const Problem& pb);
+cudaError_t launch_decode(const FwdArgs& a, void* workspace, cudaStream_t s);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
 
 }  // namespace ffpa

@@ -115,6 +115,25 @@ FFPA_API ffpa_status ffpa_fwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, f
                                       int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, float scale,
                                       ffpa_stream_t stream);
 
+/*
+ * Decode / short-query forward (SURVEY's split-KV path for few query rows per
+ * head; the operation is exactly ffpa_fwd_strided's): for problems with
+ * (Hq / Hkv) * Nq <= 16 query rows per kv head and D a multiple of 64, the key
+ * range is split over CTAs, every split reads its K/V tiles once for all
+ * query rows of the GQA group, and a second kernel combines the splits'
+ * partial outputs (O, LSE) from `workspace`.
+ *   q, o : [B, Hq, Nq, D] views; k, v : [B, Hkv, Nkv, D] views; lse: contiguous
+ *   fp32 [B, Hq, Nq]. workspace: device scratch of at least
+ *   ffpa_decode_workspace_bytes() bytes (256-byte aligned), sized for the
+ *   current device (the split count follows its SM count).
+ * Returns FFPA_ERR_NOT_SUPPORTED for problems outside the limits above (use
+ * ffpa_fwd_strided), otherwise as ffpa_fwd_strided.
+ */
+FFPA_API size_t ffpa_decode_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
+FFPA_API ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o, float* lse,
+                                     void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv,
+                                     int D, int causal, float scale, ffpa_stream_t stream);
+
 /* Workspace bytes ffpa_bwd needs for this problem (fp32 row statistics). */
 FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 

@@ -176,3 +176,58 @@ def test_python_views_are_zero_copy_for_common_layouts():
     assert api._viewable(fused[:, :, 1].transpose(1, 2))             # K slice of a fused QKV buffer
     assert not api._viewable(torch.zeros(B, H, D, N, dtype=torch.bfloat16).transpose(2, 3))  # head dim strided
     assert not api._viewable(torch.zeros(B, H, N, D + 4, dtype=torch.bfloat16)[..., :D])      # row stride 68
+
+
+def _decode(lib, Hq=8, Hkv=1, Nq=1, Nkv=4096, D=512, ws=FAKE, ws_bytes=None, q=None, lse=FAKE, scale=0.05):
+    vq = q if q is not None else _view(sb=Hq * Nq * D, sh=Nq * D, sn=D)
+    vk = _view(sb=Hkv * Nkv * D, sh=Nkv * D, sn=D)
+    vo = _view(sb=Hq * Nq * D, sh=Nq * D, sn=D)
+    if ws_bytes is None:
+        ws_bytes = lib.ffpa_decode_workspace_bytes(0, 1, Hq, Hkv, Nq, Nkv, D)
+    return lib.ffpa_decode_fwd(0, vq, vk, vk, vo, lse, ws, ws_bytes, 1, Hq, Hkv, Nq, Nkv, D, 0, scale, None)
+
+
+def test_decode_workspace_covers_every_split_partial():
+    from head_dim_flash_gb300 import _ffi
+
+    lib = _ffi.load()
+    for Hq, Hkv, Nq, Nkv, D in ((8, 1, 1, 4096, 512), (32, 4, 2, 100, 320), (4, 4, 16, 70000, 1024)):
+        n = lib.ffpa_decode_workspace_bytes(0, 2, Hq, Hkv, Nq, Nkv, D)
+        rows = 2 * Hq * Nq
+        assert n >= rows * (D + 1) * 4          # at least one split
+        assert n % (rows * (D + 1) * 4) == 0    # a whole number of splits
+        assert n // (rows * (D + 1) * 4) <= 64
+    assert lib.ffpa_decode_workspace_bytes(0, 1, 3, 2, 1, 8, 512) == 0  # Hq not a multiple of Hkv
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(Hq=32, Hkv=1, Nq=1), 2, "query rows"),      # 32 rows per kv head > 16
+    (dict(Hq=8, Hkv=1, Nq=3), 2, "query rows"),       # 24 rows
+    (dict(D=352), 2, "multiple of 64"),              # D % 64 == 32: tile kernels only
+    (dict(ws_bytes=16), 1, "workspace"),             # workspace too small
+    (dict(ws=FAKE + 16), 1, "aligned"),              # workspace not 256-byte aligned
+    (dict(ws=0), 1, "aligned"),
+    (dict(lse=0), 1, "lse"),
+    (dict(scale=float("nan")), 1, "scale"),
+])
+def test_invalid_decode_calls_are_rejected(lib, kw, status, msg):
+    assert _decode(lib, **kw) == status
+    assert msg in lib.ffpa_last_error().decode()
+
+
+def test_decode_checks_views(lib):
+    assert _decode(lib, q=_view(sn=12)) == 1  # row stride not a multiple of 8 elements
+    assert b"q" in lib.ffpa_last_error()
+
+
+def test_decode_supported_predicate():
+    import torch
+
+    from head_dim_flash_gb300 import api
+
+    q = torch.zeros(2, 8, 2, 512)
+    assert api.decode_supported(q, torch.zeros(2, 1, 9, 512))        # 16 rows per kv head
+    assert not api.decode_supported(q, torch.zeros(2, 0, 9, 512))    # no kv heads
+    assert not api.decode_supported(q, torch.zeros(2, 3, 9, 512))    # Hq not a multiple of Hkv
+    assert not api.decode_supported(torch.zeros(2, 8, 3, 512), torch.zeros(2, 1, 9, 512))  # 24 rows
+    assert not api.decode_supported(torch.zeros(2, 8, 1, 352), torch.zeros(2, 1, 9, 352))  # D % 64 != 0

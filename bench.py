@@ -10,7 +10,11 @@ same per-GPU workload (weak scaling; no data-path collective) and report the
 slowest rank's time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config headline|tiny|gqa|sweep320|sweep640|sweep1024]
+                  [--config headline|tiny|gqa|sweep320|sweep640|sweep1024|varlen|decode]
+
+--config decode times the split-KV decode forward instead (GB/s of the
+bytes it must move; a step of it takes well under a millisecond, so give it
+a few thousand --steps for the clock samples to fall inside the timed region).
 """
 from __future__ import annotations
 
@@ -50,7 +54,8 @@ def workload(name):
     from head_dim_flash_gb300 import workloads as W
 
     table = {"headline": W.HEADLINE, "tiny": W.TINY, "gqa": W.GQA_CAUSAL,
-             "sweep320": W.SWEEP[0], "sweep640": W.SWEEP[1], "sweep1024": W.SWEEP[2], "varlen": W.VARLEN}
+             "sweep320": W.SWEEP[0], "sweep640": W.SWEEP[1], "sweep1024": W.SWEEP[2], "varlen": W.VARLEN,
+             "decode": W.DECODE}
     if name not in table:
         raise SystemExit(f"unknown config {name}; choose from {sorted(table)}")
     return table[name]
@@ -247,6 +252,133 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+DECODE_METRIC = "decode forward (split-KV): algorithmic HBM GB/s (q, K/V cache, O, LSE), D=512 bf16 (1×GB300)"
+
+
+def decode_bytes(w):
+    """Bytes the decode forward must move: read q, K, V; write O (16-bit) and LSE (fp32)."""
+    q = w.B * w.Hq * w.Nq * w.D * 2
+    kv = 2 * w.B * w.Hkv * w.Nkv * w.D * 2
+    return q + kv + q + w.B * w.Hq * w.Nq * 4
+
+
+def run_decode(args, w):
+    """Decode workload: one ffpa_decode_fwd call per step (split kernel + combine)."""
+    import torch
+
+    from head_dim_flash_gb300 import api
+    from head_dim_flash_gb300 import workloads as W
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = W.make_inputs(w, with_grad_out=False)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+    from head_dim_flash_gb300 import _ffi
+
+    ws_bytes = _ffi.ffpa_decode_workspace_bytes(api._dt(q), w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.decode_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    api.get_status()
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for ev in events:
+            ev[0].record(stream)
+            step()
+            ev[1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    api.get_status()
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
+    ms_step = slowest_rank_ms(start.elapsed_time(end), world, dev) / args.steps
+    nbytes = decode_bytes(w)
+    value = world * nbytes / (ms_step / 1e3) / 1e9
+    pk = peaks()
+    achieved = nbytes / (call_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "kernel": "decode (split kernel + combine, one ffpa_decode_fwd call)",
+            "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+            "traffic": None, "peak_source": f"{pk['source']} copy bandwidth"}
+    e2e = None
+    if not args.no_e2e:
+        # the K/V cache stays resident (as in serving); each step copies the
+        # new query rows host->device and reads O and LSE back
+        qh = inp["q"].pin_memory()
+        oh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        qd = torch.empty_like(q)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            api.decode_fwd(qd, k, v, w.causal, w.scale, out=o, lse=lse, workspace=ws)
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n = max(1, args.steps)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(n):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ems = s0.elapsed_time(s1) / n
+        e2e = {"value": world * nbytes / (ems / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": qh.numel() * qh.element_size(),
+               "d2h_bytes_per_step": oh.numel() * oh.element_size() + lh.numel() * lh.element_size(),
+               "note": "K/V cache resident on the device"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = decode_cpu_baseline(w, inp)
+    if rank == 0:
+        line = {
+            "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "fp16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nkv": w.Nkv, "D": w.D,
+                       "causal": w.causal, "l2": "K/V cache larger than L2 (2.1 GB)"},
+            "rows_per_s": world * w.B * w.Hq * w.Nq / (ms_step / 1e3),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
+            "gpu_launches": 2 * args.steps,  # split kernel + combine per step
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def decode_cpu_baseline(w, inp):
+    """The fp64 oracle on the whole decode workload, one batch entry at a time."""
+    import oracle
+
+    oracle.build()
+    cores = oracle.num_threads()
+    t0 = time.perf_counter()
+    for b in range(w.B):
+        oracle.attention_fwd(inp["q"][b:b + 1], inp["k"][b:b + 1], inp["v"][b:b + 1], w.causal, w.scale)
+    dt = time.perf_counter() - t0
+    return {"value": decode_bytes(w) / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle", "seconds": dt,
+            "sample": f"the whole workload ({w.B} x {w.Hq} heads x {w.Nq} rows x {w.Nkv} keys, D={w.D}), "
+                      "fp64 C oracle, one batch entry per call"}
+
+
 def run_ours(args):
     import torch
 
@@ -257,6 +389,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workload(args.config)
+    if args.config == "decode":
+        return run_decode(args, w)
     if args.heads:
         import dataclasses
 

@@ -145,28 +145,33 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
     if (warp == 8) {
         // ------------------------------------------------------ producer
-        if (lane == 0 && n_tiles > 0) {
-            prefetch_tmap(&tK);
-            prefetch_tmap(&tV);
+        // lane 0 loads K, lane 1 loads V (one issuing thread serialises its
+        // boxes; two keep the SM's share of HBM bandwidth in flight)
+        if (lane < 2 && n_tiles > 0) {
+            prefetch_tmap(lane == 0 ? &tK : &tV);
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t) {
                 const int st = t % kDecStages;
                 const uint32_t ph = static_cast<uint32_t>((t / kDecStages) & 1);
-                if (!mbar_wait(&empty[st], ph ^ 1u, abort_p, status, lim, DS_PROD)) break;
+                if (!__all_sync(0x3u, mbar_wait(&empty[st], ph ^ 1u, abort_p, status, lim, DS_PROD))) break;
                 uint8_t* dst = smem + st * gm.stage_bytes;
-                mbar_arrive_expect_tx(&full[st], gm.stage_bytes);
+                if (lane == 0) mbar_arrive_expect_tx(&full[st], gm.stage_bytes);
+                __syncwarp(0x3u);
                 const int k0 = key_begin + t * KT;
-                tma_load_5d(dst, &tK, &full[st], 0, k0, 0, hk, b);
-                tma_load_5d(dst + half_bytes, &tV, &full[st], 0, k0, 0, hk, b);
+                if (lane == 0)
+                    tma_load_5d(dst, &tK, &full[st], 0, k0, 0, hk, b);
+                else
+                    tma_load_5d(dst + half_bytes, &tV, &full[st], 0, k0, 0, hk, b);
                 ++issued;
             }
             // no loads in flight when the CTA leaves: wait for the last ones to be consumed
-            for (int t = max(0, issued - kDecStages); t < issued; ++t) {
-                int dummy = 0;
-                if (!mbar_wait(&empty[t % kDecStages], static_cast<uint32_t>((t / kDecStages) & 1), &dummy, status, lim,
-                               DS_DRAIN, false))
-                    break;
-            }
+            if (lane == 0)
+                for (int t = max(0, issued - kDecStages); t < issued; ++t) {
+                    int dummy = 0;
+                    if (!mbar_wait(&empty[t % kDecStages], static_cast<uint32_t>((t / kDecStages) & 1), &dummy, status,
+                                   lim, DS_DRAIN, false))
+                        break;
+                }
         }
         return;
     }
@@ -216,41 +221,58 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) o_acc[cc][n][e] = 0.f;
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;  // log2-domain running max, sums
+    // legal keys of a fragment row: j < jlim (rows past R have none; causal
+    // rows stop at i + Nkv - Nq, bottom-right aligned)
+    auto key_limit = [&](int r) {
+        if (r >= R) return key_begin;
+        return pb.causal ? min(key_end, r % pb.Nq + off + 1) : key_end;
+    };
+    const int jlim_lo = key_limit(r_lo), jlim_hi = key_limit(r_hi);
     const float c2 = pb.scale_log2;
     const int nkt8 = KT / 8;  // n8 tiles of keys per tile (4 or 2)
     bool ok = true;
 
-    for (int t = 0; t < n_tiles; ++t) {
+    // Three steps per key tile, software-pipelined so that the score MMAs of
+    // tile t + 1 are issued before the P V MMAs of tile t (independent work
+    // for the tensor pipe while either waits):
+    //   scores(t): wait for the stage, partial S over my head-dim chunks;
+    //   softmax(t): reduce the partials across the eight warps, mask, online
+    //               softmax -> P (A fragments) and the rescale factors;
+    //   pv(t): rescale O, O += P V over my chunks, release the stage.
+    float s[4][4];
+    uint32_t pa[2][4];  // P of the current tile as A fragments: [k16 step][reg]
+    float al_lo = 1.f, al_hi = 1.f;
+
+    auto scores = [&](int t) {
         const int st = t % kDecStages;
         const uint32_t ph = static_cast<uint32_t>((t / kDecStages) & 1);
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_p, status, lim, DS_FULL));
         const uint32_t kbase = smem_u32(smem + st * gm.stage_bytes);
-        const uint32_t vbase = kbase + half_bytes;
-        // partial scores over my chunks: S[16 x KT]
-        float s[4][4];
 #pragma unroll
         for (int n = 0; n < 4; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
-        if (ok) {
-            for (int cc = 0; cc < my_chunks; ++cc) {
-                const uint32_t blk = kbase + (warp + 8 * cc) * KT * 128;
+        if (!ok) return;
+        for (int cc = 0; cc < my_chunks; ++cc) {
+            const uint32_t blk = kbase + (warp + 8 * cc) * KT * 128;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
+            for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-                    for (int np = 0; np < 2; ++np) {
-                        if (np * 2 >= nkt8) break;
-                        // keys 16 np .. 16 np + 15, head-dim units 2 ks, 2 ks + 1 of the chunk
-                        uint32_t kb[4];
-                        const int krow = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                        const int kunit = ks * 2 + ((lane >> 3) & 1);
-                        ldsm_x4(swz(blk, krow, kunit), kb);
-                        mma_bf16_16816(s[np * 2], qa[cc][ks], kb[0], kb[1], BF16);
-                        mma_bf16_16816(s[np * 2 + 1], qa[cc][ks], kb[2], kb[3], BF16);
-                    }
+                for (int np = 0; np < 2; ++np) {
+                    if (np * 2 >= nkt8) break;
+                    // keys 16 np .. 16 np + 15, head-dim units 2 ks, 2 ks + 1 of the chunk
+                    uint32_t kb[4];
+                    const int krow = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                    const int kunit = ks * 2 + ((lane >> 3) & 1);
+                    ldsm_x4(swz(blk, krow, kunit), kb);
+                    mma_bf16_16816(s[np * 2], qa[cc][ks], kb[0], kb[1], BF16);
+                    mma_bf16_16816(s[np * 2 + 1], qa[cc][ks], kb[2], kb[3], BF16);
                 }
             }
         }
+    };
+
+    auto softmax = [&](int t) {
         // sum the eight partials through shared memory as a reduce-scatter:
         // warp w stores its fragment as part[w][slot][lane] (slot j = 2 n + hi
         // holds the float2 of n-tile n, row r_lo or r_hi), thread (w', l) sums
@@ -281,18 +303,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
             if (n >= nkt8) break;
-            const int col = n * 8 + cpair;
             const float2 lo = fin[(2 * n) * 32 + lane], hi = fin[(2 * n + 1) * 32 + lane];
             const float acc[4] = {lo.x, lo.y, hi.x, hi.y};
-            // scale to log2 units and mask: rows past R, keys past the end, causal
+            // scale to log2 units and mask (keys at or past the row's limit)
+            const int j = key_begin + t * KT + n * 8 + cpair;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = (e < 2) ? r_lo : r_hi;
-                const int j = key_begin + t * KT + col + (e & 1);
-                const int i = r % pb.Nq;
-                const bool legal = r < R && j < key_end && (!pb.causal || j <= i + off);
-                x[n][e] = legal ? acc[e] * c2 : -INFINITY;
-            }
+            for (int e = 0; e < 4; ++e) x[n][e] = j + (e & 1) < (e < 2 ? jlim_lo : jlim_hi) ? acc[e] * c2 : -INFINITY;
         }
         // online softmax over this tile (the four lanes of a row hold its columns)
         float tmax_lo = -INFINITY, tmax_hi = -INFINITY;
@@ -307,13 +323,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         tmax_hi = fmaxf(tmax_hi, __shfl_xor_sync(0xffffffffu, tmax_hi, 1));
         tmax_hi = fmaxf(tmax_hi, __shfl_xor_sync(0xffffffffu, tmax_hi, 2));
         const float mn_lo = fmaxf(m_lo, tmax_lo), mn_hi = fmaxf(m_hi, tmax_hi);
-        const float al_lo = (mn_lo == -INFINITY) ? 1.f : ex2_approx(m_lo - mn_lo);
-        const float al_hi = (mn_hi == -INFINITY) ? 1.f : ex2_approx(m_hi - mn_hi);
+        al_lo = (mn_lo == -INFINITY) ? 1.f : ex2_approx(m_lo - mn_lo);
+        al_hi = (mn_hi == -INFINITY) ? 1.f : ex2_approx(m_hi - mn_hi);
         const float mu_lo = (mn_lo == -INFINITY) ? 0.f : mn_lo, mu_hi = (mn_hi == -INFINITY) ? 0.f : mn_hi;
         m_lo = mn_lo;
         m_hi = mn_hi;
         float ps_lo = 0.f, ps_hi = 0.f;
-        uint32_t pa[2][4];  // P as A fragments: [k16 step][reg]
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
             if (n >= nkt8) break;
@@ -327,7 +342,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         l_lo = l_lo * al_lo + ps_lo;
         l_hi = l_hi * al_hi + ps_hi;
-        // O += P V on my chunks
+    };
+
+    auto pv = [&](int t) {
+        const int st = t % kDecStages;
+        const uint32_t vbase = smem_u32(smem + st * gm.stage_bytes) + half_bytes;
         for (int cc = 0; cc < my_chunks; ++cc) {
 #pragma unroll
             for (int n = 0; n < 8; ++n) {
@@ -356,6 +375,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // K and V of this stage are read
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
+    };
+
+    // the trip counts are the same in every compute warp, so all of them pass
+    // the named barriers inside softmax() equally often
+    if (n_tiles > 0) {
+        scores(0);
+        softmax(0);
+    }
+    for (int t = 0; t < n_tiles; ++t) {
+        const bool more = t + 1 < n_tiles;
+        if (more) scores(t + 1);
+        pv(t);
+        if (more) softmax(t + 1);
     }
 
     // ------------------------------------------------------------ partial outputs

@@ -75,6 +75,10 @@ VARLEN = Workload("varlen 6 seqs H32 D512 bf16 causal", len(_VL), 32, 32, max(_V
 
 ALL = (TINY, HEADLINE, GQA_CAUSAL) + SWEEP + (VARLEN,)
 
+# Decode / short-query forward: one new query row per sequence against a long
+# key cache, eight query heads per kv head (the split-KV path).
+DECODE = Workload("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", 8, 32, 8, 1, 16384, 512, torch.bfloat16, False, 50)
+
 
 def make_inputs(w: Workload, with_grad_out: bool = True):
     """Returns dict with q, k, v (and dO) as CPU tensors of w.dtype (+ cu_seqlens for varlen)."""

@@ -196,21 +196,26 @@ def cpu_baseline(w, inp, n_rows=8192):
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
-# ncu capture of the kernel, keyed by (workload, kernel), with the hash of the
-# kernel sources the capture ran; the figure is reported only while the
-# sources still hash the same (the ncu summaries under profiles/ give the
-# commands and the raw counters).
+# ncu capture, keyed by (workload, kernel), with the hash of the sources the
+# capture ran; the figure is reported only while those sources still hash
+# the same (the ncu summaries under profiles/ give the commands and the raw
+# counters).
+PAIR_SOURCES = ("xchg.cu", "xchg2.cu", "ptx.cuh", "tile_common.cuh", "kernels.h", "bwd.cu", "fwd.cu")
+DECODE_SOURCES = ("decode.cu", "ptx.cuh", "tile_common.cuh", "kernels.h")
 TRAFFIC = {
-    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 1357692928, "sources": "2da5a6d776e78917"},
+    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 1343856128, "files": PAIR_SOURCES,
+                                             "sources": "3488af9ace94c242"},
+    # one ffpa_decode_fwd call: split kernel + combine
+    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2155079168, "files": DECODE_SOURCES,
+                                                                "sources": "849fec8fbaf221e6"},
 }
-KERNEL_SOURCES = ("xchg.cu", "xchg2.cu", "ptx.cuh", "tile_common.cuh", "kernels.h", "bwd.cu", "fwd.cu")
 
 
-def kernel_source_hash():
+def kernel_source_hash(files=PAIR_SOURCES):
     import hashlib
 
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in files:
         with open(os.path.join(ROOT, "head_dim_flash_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -218,7 +223,7 @@ def kernel_source_hash():
 
 def measured_traffic(w, kernel):
     rec = TRAFFIC.get((w.name, kernel))
-    if rec is None or rec["sources"] != kernel_source_hash():
+    if rec is None or rec["sources"] != kernel_source_hash(rec["files"]):
         return None
     return rec["bytes"]
 
@@ -314,7 +319,7 @@ def run_decode(args, w):
     achieved = nbytes / (call_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "kernel": "decode (split kernel + combine, one ffpa_decode_fwd call)",
             "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-            "traffic": None, "peak_source": f"{pk['source']} copy bandwidth"}
+            "traffic": measured_traffic(w, "decode"), "peak_source": f"{pk['source']} copy bandwidth"}
     e2e = None
     if not args.no_e2e:
         # the K/V cache stays resident (as in serving); each step copies the

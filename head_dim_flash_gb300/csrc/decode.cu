@@ -420,39 +420,34 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
 }
 
-// One warp per query row: combine the splits' partial outputs and LSE.
+// One CTA per query row, two head-dim columns per thread: combine the
+// splits' partial outputs and LSE (every thread reads the row's split LSEs,
+// which the CTA shares through L1; the partial O rows are read coalesced).
 template <bool BF16>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const FwdArgs a, const DecGeo gm)
+__global__ void __launch_bounds__(512) decode_combine_kernel(const FwdArgs a, const DecGeo gm)
 {
     const Problem& pb = a.pb;
     const long rows_total = static_cast<long>(pb.B) * pb.Hq * pb.Nq;
-    const long row = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
-    const int lane = threadIdx.x & 31;
-    if (row >= rows_total) return;
+    const long row = blockIdx.x;
+    const int c = 2 * threadIdx.x;
     float mx = -INFINITY;
     for (int s = 0; s < gm.splits; ++s) mx = fmaxf(mx, gm.lse_part[static_cast<size_t>(s) * rows_total + row]);
-    float wsum = 0.f;
-    for (int s = 0; s < gm.splits; ++s) {
-        const float l = gm.lse_part[static_cast<size_t>(s) * rows_total + row];
-        if (l > -INFINITY) wsum += __expf(l - mx);
-    }
-    const float lse = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+    float wsum = 0.f, v0 = 0.f, v1 = 0.f;
+    if (mx > -INFINITY)
+        for (int s = 0; s < gm.splits; ++s) {
+            const float l = gm.lse_part[static_cast<size_t>(s) * rows_total + row];
+            if (l == -INFINITY) continue;
+            const float w = __expf(l - mx);
+            const float2 p = *reinterpret_cast<const float2*>(gm.o_part + (static_cast<size_t>(s) * rows_total + row) * pb.D + c);
+            wsum += w;
+            v0 = fmaf(w, p.x, v0);
+            v1 = fmaf(w, p.y, v1);
+        }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     const long b = row / (static_cast<long>(pb.Hq) * pb.Nq), h = (row / pb.Nq) % pb.Hq, i = row % pb.Nq;
     uint16_t* out = reinterpret_cast<uint16_t*>(a.o) + b * pb.vo.sb + h * pb.vo.sh + i * pb.vo.sn;
-    for (int c = lane * 2; c < pb.D; c += 64) {
-        float v0 = 0.f, v1 = 0.f;
-        if (wsum > 0.f)
-            for (int s = 0; s < gm.splits; ++s) {
-                const float l = gm.lse_part[static_cast<size_t>(s) * rows_total + row];
-                if (l == -INFINITY) continue;
-                const float w = __expf(l - lse);
-                const float2 p = *reinterpret_cast<const float2*>(gm.o_part + (static_cast<size_t>(s) * rows_total + row) * pb.D + c);
-                v0 = fmaf(w, p.x, v0);
-                v1 = fmaf(w, p.y, v1);
-            }
-        *reinterpret_cast<uint32_t*>(out + c) = pack2<BF16>(v0, v1);
-    }
-    if (lane == 0) a.lse[row] = lse;
+    *reinterpret_cast<uint32_t*>(out + c) = pack2<BF16>(v0 * inv, v1 * inv);
+    if (threadIdx.x == 0) a.lse[row] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
 }
 
 }  // namespace
@@ -517,7 +512,8 @@ cudaError_t launch_variant(const FwdArgs& a, const DecGeo& gm, const CUtensorMap
     decode_kernel<BF16><<<grid, kDecThreads, smem, s>>>(tk, tv, a, gm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long rows = static_cast<long>(a.pb.B) * a.pb.Hq * a.pb.Nq;
-    decode_combine_kernel<BF16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(a, gm);
+    if (rows > 0x7fffffffL) return cudaErrorInvalidValue;
+    decode_combine_kernel<BF16><<<static_cast<unsigned>(rows), a.pb.D / 2, 0, s>>>(a, gm);
     return cudaGetLastError();
 }
 

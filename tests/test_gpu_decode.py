@@ -129,3 +129,22 @@ def test_decode_rejects_too_many_rows():
     k = torch.zeros(1, 1, 64, 512, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(NotImplementedError):
         api.decode_fwd(q, k, k, False, 0.05)
+
+
+def test_decode_full_size_workload():
+    # the benchmarked decode workload, in the launch configuration the
+    # benchmark times; every output against the oracle, one batch entry at a time
+    w = workloads.DECODE
+    inp = workloads.make_inputs(w, with_grad_out=False)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    og = Guarded(q.shape, w.dtype)
+    lg = Guarded((w.B, w.Hq, w.Nq), torch.float32)
+    api.decode_fwd(q, k, v, w.causal, w.scale, out=og.t, lse=lg.t)
+    api.get_status()
+    og.check_guards("o")
+    lg.check_guards("lse")
+    for b in range(w.B):
+        o_ref, lse_ref = oracle.attention_fwd(inp["q"][b:b + 1], inp["k"][b:b + 1], inp["v"][b:b + 1], w.causal,
+                                              w.scale)
+        check_o(og.t[b:b + 1], o_ref, f"O[b{b}]")
+        check_lse(lg.t[b:b + 1], lse_ref, f"LSE[b{b}]")

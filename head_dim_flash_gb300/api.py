@@ -113,14 +113,17 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     return o, l
 
 
-DECODE_ROWS = 16  # (Hq / Hkv) * Nq query rows per kv head that the decode path takes
+DECODE_ROWS = 16    # query rows of one kv head's group per decode CTA
+DECODE_MAX_NQ = 8   # attention() sends Nq below this to the decode path
 
 
 def decode_supported(q, k) -> bool:
-    """True when ffpa_decode_fwd takes this problem (few query rows per kv head, D % 64 == 0)."""
+    """True when ffpa_decode_fwd takes this problem (D % 64 == 0, grid within limits)."""
     B, Hq, Nq, D = q.shape
     Hkv = k.shape[1]
-    return Hkv > 0 and Hq % Hkv == 0 and (Hq // Hkv) * Nq <= DECODE_ROWS and D % 64 == 0
+    if Hkv <= 0 or Hq % Hkv != 0 or D % 64 != 0:
+        return False
+    return B * Hkv * -(-(Hq // Hkv) * Nq // DECODE_ROWS) <= 65535
 
 
 def decode_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, workspace=None):
@@ -184,7 +187,12 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
 class _Attention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, causal, scale):
-        o, lse = fwd(q, k, v, causal, scale)
+        # short queries (Nq < 8, decode) take the split-KV path; the backward
+        # is the same either way (O and LSE have the same meaning)
+        if q.dim() == 4 and 0 < q.shape[2] < DECODE_MAX_NQ and decode_supported(q, k):
+            o, lse = decode_fwd(q, k, v, causal, scale)
+        else:
+            o, lse = fwd(q, k, v, causal, scale)
         ctx.save_for_backward(q, k, v, o, lse)
         ctx.causal, ctx.scale = causal, scale
         return o, lse

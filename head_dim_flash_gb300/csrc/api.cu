@@ -329,9 +329,10 @@ ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v
     FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
     FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
     if (D % 64 != 0) return fail(FFPA_ERR_NOT_SUPPORTED, "decode path: D=%d must be a multiple of 64", D);
-    if (Hq > 0 && static_cast<long>(Hq / Hkv) * Nq > ffpa::kDecodeRows)
-        return fail(FFPA_ERR_NOT_SUPPORTED, "decode path: (Hq/Hkv)*Nq=%ld query rows per kv head exceed %d",
-                    static_cast<long>(Hq / Hkv) * Nq, ffpa::kDecodeRows);
+    if (Hq > 0 && static_cast<long>(B) * Hkv * ((static_cast<long>(Hq / Hkv) * Nq + ffpa::kDecodeRows - 1) /
+                                                ffpa::kDecodeRows) > 65535)
+        return fail(FFPA_ERR_NOT_SUPPORTED, "decode path: B*Hkv*ceil((Hq/Hkv)*Nq/%d) exceeds the grid limit 65535",
+                    ffpa::kDecodeRows);
     const long q_rows = static_cast<long>(B) * Hq * Nq;
     const long k_rows = static_cast<long>(B) * Hkv * Nkv;
     FFPA_TRY(check_view(q, q_rows > 0, "q", B, Hq, Nq));

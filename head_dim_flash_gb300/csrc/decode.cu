@@ -5,9 +5,10 @@
 // "Hard constraints": bottom-right causal mask, GQA/MQA head broadcast, empty
 // rows give O = 0 and LSE = -inf). With Nq small the work is reading K and V
 // once from HBM, so the layout differs from the tile kernels:
-//   - a CTA owns one (batch, kv head, key split) and all R = G * Nq query
-//     rows of that kv head's group (R <= 16: one m16 MMA tile), so every K/V
-//     byte is read once per split and serves all rows of the group;
+//   - a CTA owns one (batch, kv head, key split) and 16 of the R = G * Nq
+//     query rows of that kv head's group (one m16 MMA tile; R > 16 takes
+//     ceil(R / 16) row blocks), so every K/V byte is read once per split and
+//     row block and serves all rows of the block;
 //   - a producer warp streams K and V tiles of KT keys into a ring of shared
 //     memory stages with TMA (5-D chunked maps over the strided views);
 //   - eight compute warps each own 64-wide head-dim chunks: partial scores
@@ -48,7 +49,8 @@ struct __align__(1024) DecStatic {
 static_assert(sizeof(DecStatic) == 1024, "static shared block must be exactly 1 KiB");
 
 struct DecGeo {
-    int splits;       // key splits per (batch, kv head)
+    int splits;       // key splits per (batch, kv head, row block)
+    int rblocks;      // blocks of kDecRows query rows per kv head's group
     int tiles_per;    // key tiles per split
     int kt;           // keys per tile (32, or 16 when D > 512)
     int chunks;       // 64-wide head-dim chunks (ceil(D / 64))
@@ -103,10 +105,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 {
     const Problem& pb = a.pb;
     const int G = pb.Hq / pb.Hkv;
-    const int R = G * pb.Nq;            // query rows of the group (<= kDecRows)
+    const int R = G * pb.Nq;            // query rows of the group
+    const int rb = blockIdx.y % gm.rblocks;  // this CTA's block of kDecRows of them
+    const int unit = blockIdx.y / gm.rblocks;
+    const int r0 = rb * kDecRows;        // group row of the CTA's row 0
     const int split = blockIdx.x;
-    const int b = blockIdx.y / pb.Hkv;
-    const int hk = blockIdx.y % pb.Hkv;
+    const int b = unit / pb.Hkv;
+    const int hk = unit % pb.Hkv;
     const int KT = gm.kt;
     const int nch = gm.chunks;
     const int off = pb.Nkv - pb.Nq;      // causal: key j legal for query i iff j <= i + off
@@ -190,8 +195,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (int e = threadIdx.x; e < kDecRows * width / 8; e += 256) {
             const int r = e / (width / 8), u = e % (width / 8);
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < R && u * 8 < pb.D) {
-                const int g = r / pb.Nq, i = r % pb.Nq;
+            if (r0 + r < R && u * 8 < pb.D) {
+                const int g = (r0 + r) / pb.Nq, i = (r0 + r) % pb.Nq;
                 const size_t o = static_cast<size_t>(b) * pb.vq.sb + static_cast<size_t>(hk * G + g) * pb.vq.sh +
                                  static_cast<size_t>(i) * pb.vq.sn + static_cast<size_t>(u) * 8;
                 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + o);
@@ -224,8 +229,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // legal keys of a fragment row: j < jlim (rows past R have none; causal
     // rows stop at i + Nkv - Nq, bottom-right aligned)
     auto key_limit = [&](int r) {
-        if (r >= R) return key_begin;
-        return pb.causal ? min(key_end, r % pb.Nq + off + 1) : key_end;
+        if (r0 + r >= R) return key_begin;
+        return pb.causal ? min(key_end, (r0 + r) % pb.Nq + off + 1) : key_end;
     };
     const int jlim_lo = key_limit(r_lo), jlim_hi = key_limit(r_hi);
     const float c2 = pb.scale_log2;
@@ -398,10 +403,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const size_t rows_total = static_cast<size_t>(pb.B) * pb.Hq * pb.Nq;
     for (int hi = 0; hi < 2; ++hi) {
         const int r = hi ? r_hi : r_lo;
-        if (r >= R) continue;
+        if (r0 + r >= R) continue;
         const float l = hi ? l_hi : l_lo, m = hi ? m_hi : m_lo;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int g = r / pb.Nq, i = r % pb.Nq;
+        const int g = (r0 + r) / pb.Nq, i = (r0 + r) % pb.Nq;
         const size_t row = (static_cast<size_t>(b) * pb.Hq + hk * G + g) * pb.Nq + i;  // LSE layout [B, Hq, Nq]
         float* dst = gm.o_part + (static_cast<size_t>(split) * rows_total + row) * pb.D;
         for (int cc = 0; cc < my_chunks; ++cc) {
@@ -462,7 +467,8 @@ DecodePlan decode_plan(const Problem& pb)
     DecodePlan p{};
     p.chunks = (pb.D + 63) / 64;
     p.kt = p.chunks > 8 ? 16 : 32;
-    const long units = max(1, pb.B * pb.Hkv);
+    p.rblocks = max(1, (pb.Hq / max(1, pb.Hkv) * pb.Nq + kDecodeRows - 1) / kDecodeRows);
+    const long units = max(1L, static_cast<long>(pb.B) * pb.Hkv * p.rblocks);
     const int tiles = max(1, (pb.Nkv + p.kt - 1) / p.kt);
     const long sms = num_sms() > 0 ? num_sms() : 148;
     long best = -1;
@@ -495,6 +501,7 @@ DecGeo plan(const Problem& pb, float* ws)
     gm.stage_bytes = 2 * gm.kt * gm.chunks * 128;
     gm.tiles_per = p.tiles_per;
     gm.splits = p.splits;
+    gm.rblocks = p.rblocks;
     const size_t rows_total = static_cast<size_t>(pb.B) * pb.Hq * pb.Nq;
     gm.o_part = ws;
     gm.lse_part = ws + static_cast<size_t>(gm.splits) * rows_total * pb.D;
@@ -508,7 +515,7 @@ cudaError_t launch_variant(const FwdArgs& a, const DecGeo& gm, const CUtensorMap
     const int smem = kDecStages * gm.stage_bytes + kDecRedBytes;
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(gm.splits, a.pb.B * a.pb.Hkv);
+    const dim3 grid(gm.splits, a.pb.B * a.pb.Hkv * gm.rblocks);
     decode_kernel<BF16><<<grid, kDecThreads, smem, s>>>(tk, tv, a, gm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long rows = static_cast<long>(a.pb.B) * a.pb.Hq * a.pb.Nq;

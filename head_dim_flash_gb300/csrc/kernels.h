@@ -115,12 +115,13 @@ int set_error(int status, const char* fmt, ...);
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
 
-// Decode / short-query forward (split over the keys): dense problems with
-// (Hq / Hkv) * Nq <= kDecodeRows query rows per kv head and D % 64 == 0.
+// Decode / short-query forward (split over the keys), D % 64 == 0: a CTA
+// takes kDecodeRows query rows of one kv head's group (G * Nq rows in all)
+// and one split of its keys.
 constexpr int kDecodeRows = 16;
 constexpr int kDecodeMaxSplits = 64;
 struct DecodePlan {
-    int splits, tiles_per, kt, chunks;
+    int splits, rblocks, tiles_per, kt, chunks;
     size_t workspace_bytes;  // partial outputs and LSE of every split
 };
 DecodePlan decode_plan(const Problem& pb);

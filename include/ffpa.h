@@ -116,18 +116,21 @@ FFPA_API ffpa_status ffpa_fwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, f
                                       ffpa_stream_t stream);
 
 /*
- * Decode / short-query forward (SURVEY's split-KV path for few query rows per
- * head; the operation is exactly ffpa_fwd_strided's): for problems with
- * (Hq / Hkv) * Nq <= 16 query rows per kv head and D a multiple of 64, the key
- * range is split over CTAs, every split reads its K/V tiles once for all
- * query rows of the GQA group, and a second kernel combines the splits'
- * partial outputs (O, LSE) from `workspace`.
+ * Decode / short-query forward (the pages' split-KV two-stage decode path,
+ * FFPA docs "Backends Overview", feature support and fallback table; the
+ * operation is exactly ffpa_fwd_strided's). The keys are split over CTAs;
+ * a CTA takes 16 query rows of one kv head's group (G = Hq / Hkv heads x Nq
+ * rows) and reads each K/V byte of its split once for all of them; a second
+ * kernel combines the splits' partial outputs (O, LSE) from `workspace`.
+ * Meant for few query rows per kv head (G * Nq <= 16 reads K/V exactly once;
+ * larger groups re-read them once per 16 rows).
  *   q, o : [B, Hq, Nq, D] views; k, v : [B, Hkv, Nkv, D] views; lse: contiguous
- *   fp32 [B, Hq, Nq]. workspace: device scratch of at least
- *   ffpa_decode_workspace_bytes() bytes (256-byte aligned), sized for the
- *   current device (the split count follows its SM count).
- * Returns FFPA_ERR_NOT_SUPPORTED for problems outside the limits above (use
- * ffpa_fwd_strided), otherwise as ffpa_fwd_strided.
+ *   fp32 [B, Hq, Nq]. D must be a multiple of 64.
+ *   workspace: device scratch of at least ffpa_decode_workspace_bytes()
+ *   bytes, 256-byte aligned, sized on the current device (the split count
+ *   follows its SM count); one call at a time per workspace.
+ * Returns FFPA_ERR_NOT_SUPPORTED for D % 64 != 0 or B * Hkv * ceil(G * Nq /
+ * 16) > 65535 (use ffpa_fwd_strided), otherwise as ffpa_fwd_strided.
  */
 FFPA_API size_t ffpa_decode_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 FFPA_API ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o, float* lse,

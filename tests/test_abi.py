@@ -201,8 +201,7 @@ def test_decode_workspace_covers_every_split_partial():
 
 
 @pytest.mark.parametrize("kw,status,msg", [
-    (dict(Hq=32, Hkv=1, Nq=1), 2, "query rows"),      # 32 rows per kv head > 16
-    (dict(Hq=8, Hkv=1, Nq=3), 2, "query rows"),       # 24 rows
+    (dict(Hq=64, Hkv=64, Nq=16400, Nkv=64), 2, "grid limit"),  # 64 kv heads x 1025 row blocks > 65535
     (dict(D=352), 2, "multiple of 64"),              # D % 64 == 32: tile kernels only
     (dict(ws_bytes=16), 1, "workspace"),             # workspace too small
     (dict(ws=FAKE + 16), 1, "aligned"),              # workspace not 256-byte aligned
@@ -226,8 +225,10 @@ def test_decode_supported_predicate():
     from head_dim_flash_gb300 import api
 
     q = torch.zeros(2, 8, 2, 512)
-    assert api.decode_supported(q, torch.zeros(2, 1, 9, 512))        # 16 rows per kv head
+    assert api.decode_supported(q, torch.zeros(2, 1, 9, 512))        # 16 rows per kv head: one row block
+    assert api.decode_supported(torch.zeros(2, 8, 3, 512), torch.zeros(2, 1, 9, 512))  # 24 rows: two blocks
     assert not api.decode_supported(q, torch.zeros(2, 0, 9, 512))    # no kv heads
     assert not api.decode_supported(q, torch.zeros(2, 3, 9, 512))    # Hq not a multiple of Hkv
-    assert not api.decode_supported(torch.zeros(2, 8, 3, 512), torch.zeros(2, 1, 9, 512))  # 24 rows
     assert not api.decode_supported(torch.zeros(2, 8, 1, 352), torch.zeros(2, 1, 9, 352))  # D % 64 != 0
+    big = torch.zeros(1, 1, 1, 64).expand(1, 64, 16400, 64)          # 64 x 1025 row blocks (shape only)
+    assert not api.decode_supported(big, torch.zeros(1, 64, 9, 64))  # grid limit

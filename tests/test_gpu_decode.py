@@ -15,7 +15,7 @@ import torch
 import oracle
 from head_dim_flash_gb300 import api
 from head_dim_flash_gb300 import workloads
-from tests.gpu_utils import Guarded, check_lse, check_o
+from tests.gpu_utils import Guarded, check_grad, check_lse, check_o
 
 pytestmark = pytest.mark.gpu
 
@@ -124,11 +124,36 @@ def test_decode_strided_views():
     check_lse(lse, lse_ref)
 
 
-def test_decode_rejects_too_many_rows():
-    q = torch.zeros(1, 32, 1, 512, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(1, 1, 64, 512, dtype=torch.bfloat16, device="cuda")
+@pytest.mark.parametrize("G,Nq,causal", [(32, 1, False), (8, 3, True), (4, 7, True), (1, 40, True)])
+def test_decode_row_blocks(G, Nq, causal):
+    # G * Nq > 16: several 16-row blocks per kv head, each reading K/V itself
+    run_decode(1, 2 * G, 2, Nq, 777, 512, causal, seed=G + Nq)
+
+
+def test_decode_rejects_unsupported_head_dim():
+    q = torch.zeros(1, 4, 1, 352, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 1, 64, 352, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(NotImplementedError):
         api.decode_fwd(q, k, k, False, 0.05)
+
+
+@pytest.mark.parametrize("Nq", [1, 5])
+def test_attention_routes_short_queries_to_decode_with_gradients(Nq):
+    # attention(): forward through the split-KV path for Nq < 8, backward
+    # through the tile kernels; all against the oracle
+    B, Hq, Hkv, Nkv, D = 1, 8, 2, 600, 512
+    inp = workloads.random_dense(B, Hq, Hkv, Nq, Nkv, D, torch.bfloat16, seed=Nq)
+    q, k, v, do = (inp[n].cuda().requires_grad_(n != "dO") for n in ("q", "k", "v", "dO"))
+    scale = 1.0 / math.sqrt(D)
+    o = api.attention(q, k, v, True, scale)
+    o.backward(do)
+    api.get_status()
+    o_ref, _ = oracle.attention_fwd(inp["q"], inp["k"], inp["v"], True, scale)
+    check_o(o.detach(), o_ref)
+    dq_ref, dk_ref, dv_ref = oracle.attention_bwd(inp["q"], inp["k"], inp["v"], inp["dO"], True, scale)
+    check_grad(q.grad, dq_ref, "dQ")
+    check_grad(k.grad, dk_ref, "dK")
+    check_grad(v.grad, dv_ref, "dV")
 
 
 def test_decode_full_size_workload():

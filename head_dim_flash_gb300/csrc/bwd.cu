@@ -99,8 +99,20 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
     x.dk = a.dk;
     x.dv = a.dv;
     x.ctl = a.ctl;
-    if (!kv_empty && (a.stages & 2u) && (e = launch_xchg(XOP_DV, x, st)) != cudaSuccess) return e;
-    if (!kv_empty && (a.stages & 8u) && (e = launch_xchg(XOP_DK, x, st)) != cudaSuccess) return e;
+    // dV, dK and dQ read only the inputs and the preprocess output and write
+    // disjoint outputs: each after the first is a programmatic dependent of the
+    // one before, so it fills the SMs that the previous one's last wave leaves
+    // idle (the first waits for the preprocess as usual; the later ones start
+    // only once all of its CTAs have started, hence after the preprocess)
+    x.pdl = 0;
+    if (!kv_empty && (a.stages & 2u)) {
+        if ((e = launch_xchg(XOP_DV, x, st)) != cudaSuccess) return e;
+        x.pdl = 1;
+    }
+    if (!kv_empty && (a.stages & 8u)) {
+        if ((e = launch_xchg(XOP_DK, x, st)) != cudaSuccess) return e;
+        x.pdl = 1;
+    }
     if (!q_empty && (a.stages & 4u) && (e = launch_xchg(XOP_DQ, x, st)) != cudaSuccess) return e;
     return cudaSuccess;
 }

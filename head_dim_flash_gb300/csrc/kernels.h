@@ -72,6 +72,9 @@ struct XArgs {
     const float* lse_log2;             // backward: LSE * log2(e), +inf for empty rows
     void *dq, *dk, *dv;
     DeviceCtl ctl;
+    // launch as a programmatic dependent of the previous kernel of the stream
+    // (which must be one of these GEMM kernels that reads nothing this one writes)
+    int pdl;
 };
 
 // Runs one of the four GEMM kernels, in the CTA-pair form (2-SM MMAs,

@@ -243,6 +243,14 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// Programmatic dependent launch: this CTA lets the next kernel of the stream
+// (launched with programmatic stream serialization) start once every CTA of
+// this grid has signalled or exited; pdl_wait() blocks until the previous
+// grid of the stream (this grid's primary) has completed and its memory is
+// visible (a no-op in a kernel launched without the attribute).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar)
 {

@@ -92,6 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tB1, const __grid_constant__ CUtensorMap tB2,
                 const __grid_constant__ CUtensorMap tW, const XArgs a, const Geo gm)
 {
+    // the next GEMM kernel of a backward may take SMs as this grid's last CTAs start
+    pdl_trigger();
     using T = Traits<OP>;
     const Problem& pb = a.pb;
     const int C = gm.C;
@@ -759,6 +761,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // launched as a dependent: do not complete before the previous grid, so
+    // that work after this kernel in the stream also follows that grid
+    if (threadIdx.x == 0) pdl_wait();
 }
 
 template <int OP, bool BF16, bool VARLEN>
@@ -773,13 +778,15 @@ cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const Geo& gm, in
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = gm.C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = a.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], a, gm);
 }
 

@@ -25,6 +25,11 @@ EXPORTS = (
     "ffpa_bwd_strided",
     "ffpa_decode_workspace_bytes",
     "ffpa_decode_fwd",
+    "ffpa_fp8_workspace_bytes",
+    "ffpa_fp8_workspace_layout",
+    "ffpa_fp8_quantize",
+    "ffpa_fwd_fp8",
+    "ffpa_fwd_fp8_quantized",
     "ffpa_bwd_stages",
     "ffpa_bwd_noalloc",
     "ffpa_varlen_fwd",
@@ -62,6 +67,16 @@ def _declare(lib):
     lib.ffpa_bwd_strided.argtypes = [_i, View, View, View, View, _p, View, View, View, View, _p, _sz, _i, _i, _i, _i,
                                      _i, _i, _i, _f, _p]
     lib.ffpa_bwd_strided.restype = _i
+    lib.ffpa_fp8_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i]
+    lib.ffpa_fp8_workspace_bytes.restype = _sz
+    lib.ffpa_fp8_workspace_layout.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]
+    lib.ffpa_fp8_workspace_layout.restype = _sz
+    lib.ffpa_fp8_quantize.argtypes = [_i, View, View, View, _p, _sz, _i, _i, _i, _i, _i, _i, _p]
+    lib.ffpa_fp8_quantize.restype = _i
+    lib.ffpa_fwd_fp8.argtypes = [_i, View, View, View, View, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _p]
+    lib.ffpa_fwd_fp8.restype = _i
+    lib.ffpa_fwd_fp8_quantized.argtypes = [_i, View, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _p]
+    lib.ffpa_fwd_fp8_quantized.restype = _i
     lib.ffpa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
     lib.ffpa_decode_workspace_bytes.restype = _sz
     lib.ffpa_decode_fwd.argtypes = [_i, View, View, View, View, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _p]
@@ -141,6 +156,29 @@ def ffpa_fwd_strided(*args):
 
 def ffpa_bwd_strided(*args):
     return load().ffpa_bwd_strided(*args)
+
+
+def ffpa_fp8_workspace_bytes(*args):
+    return load().ffpa_fp8_workspace_bytes(*args)
+
+
+def ffpa_fp8_workspace_layout(B, Hq, Hkv, Nq, Nkv, D):
+    """Byte offsets (q8, k8, v8t, sq, sk, sv), ldv and the total size of the FP8 workspace."""
+    off = (_sz * 8)()
+    load().ffpa_fp8_workspace_layout(B, Hq, Hkv, Nq, Nkv, D, off)
+    return list(off)
+
+
+def ffpa_fp8_quantize(*args):
+    return load().ffpa_fp8_quantize(*args)
+
+
+def ffpa_fwd_fp8(*args):
+    return load().ffpa_fwd_fp8(*args)
+
+
+def ffpa_fwd_fp8_quantized(*args):
+    return load().ffpa_fwd_fp8_quantized(*args)
 
 
 def ffpa_decode_workspace_bytes(*args):

@@ -146,6 +146,80 @@ def decode_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=No
     return o, l
 
 
+FP8_HEAD_DIMS = (256, 512, 768)
+
+
+def fp8_workspace(q, k):
+    """Device scratch for fwd_fp8 (uint8, 256-byte aligned by the allocator)."""
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    n = int(_ffi.ffpa_fp8_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def _fp8_args(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,Hq,Nq,D], k and v [B,Hkv,Nkv,D]")
+    return _dense(q, k, v)
+
+
+def fp8_quantize(q, k, v, workspace=None):
+    """Runs only the e4m3 quantization; returns (workspace, {name: view}) with
+    q8, k8 (uint8 codes), v8t ([B, Hkv, D, ldv] codes of V^T) and the fp32 scales sq, sk, sv."""
+    q, k, v = _fp8_args(q, k, v)
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    ws = fp8_workspace(q, k) if workspace is None else workspace
+    st = _ffi.ffpa_fp8_quantize(_dt(q), _view(q), _view(k), _view(v), ws.data_ptr(), ws.numel(),
+                                B, Hq, Hkv, Nq, Nkv, D, _stream())
+    _ffi.raise_for(st, "ffpa_fp8_quantize")
+    off = _ffi.ffpa_fp8_workspace_layout(B, Hq, Hkv, Nq, Nkv, D)
+    ldv = off[6]
+
+    def region(i, n, shape, dtype=torch.uint8):
+        t = ws[off[i]:off[i] + n * (4 if dtype == torch.float32 else 1)]
+        return t.view(dtype).view(shape)
+
+    views = {
+        "q8": region(0, B * Hq * Nq * D, (B, Hq, Nq, D)),
+        "k8": region(1, B * Hkv * Nkv * D, (B, Hkv, Nkv, D)),
+        "v8t": region(2, B * Hkv * D * ldv, (B, Hkv, D, ldv)),
+        "sq": region(3, B * Hq, (B, Hq), torch.float32),
+        "sk": region(4, B * Hkv, (B, Hkv), torch.float32),
+        "sv": region(5, B * Hkv, (B, Hkv), torch.float32),
+    }
+    return ws, views
+
+
+def fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, workspace=None):
+    """FP8 (e4m3) forward through ffpa_fwd_fp8: bf16/fp16 in, O in the input
+    dtype and fp32 LSE out. D in FP8_HEAD_DIMS. Returns (o, lse)."""
+    q, k, v = _fp8_args(q, k, v)
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    o = _out_like(q) if out is None else out
+    l = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = fp8_workspace(q, k) if workspace is None else workspace
+    st = _ffi.ffpa_fwd_fp8(_dt(q), _view(q), _view(k), _view(v), _view(o), l.data_ptr(), ws.data_ptr(), ws.numel(),
+                           B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D), _stream())
+    _ffi.raise_for(st, "ffpa_fwd_fp8")
+    return o, l
+
+
+def fwd_fp8_quantized(workspace, shape_q, shape_k, dtype, causal: bool = False, scale: float | None = None,
+                      out=None, lse=None):
+    """The FP8 attention alone, on a workspace that fp8_quantize filled for q of
+    shape_q and k/v of shape_k (inputs quantized once, attended many times)."""
+    B, Hq, Nq, D = shape_q
+    _, Hkv, Nkv, _ = shape_k
+    o = torch.empty(shape_q, dtype=dtype, device=workspace.device) if out is None else out
+    l = torch.empty((B, Hq, Nq), dtype=torch.float32, device=workspace.device) if lse is None else lse
+    st = _ffi.ffpa_fwd_fp8_quantized(_dt(o), _view(o), l.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                     B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), _scale(scale, D), _stream())
+    _ffi.raise_for(st, "ffpa_fwd_fp8_quantized")
+    return o, l
+
+
 def bwd_workspace_bytes(q, k) -> int:
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape

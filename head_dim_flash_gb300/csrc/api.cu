@@ -363,6 +363,133 @@ ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v
     return launch_result(ffpa::launch_decode(a, workspace, reinterpret_cast<cudaStream_t>(stream)), "decode launch");
 }
 
+size_t ffpa_fp8_workspace_layout(int B, int Hq, int Hkv, int Nq, int Nkv, int D, size_t* offsets)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nkv < 0 || D <= 0 || Hq % Hkv != 0 || D % 128 != 0) return 0;
+    const ffpa::Fp8Layout L = ffpa::fp8_layout(B, Hq, Hkv, Nq, Nkv, D);
+    if (offsets) {
+        offsets[0] = L.q8;
+        offsets[1] = L.k8;
+        offsets[2] = L.v8t;
+        offsets[3] = L.sq;
+        offsets[4] = L.sk;
+        offsets[5] = L.sv;
+        offsets[6] = static_cast<size_t>(L.ldv);
+        offsets[7] = L.total;
+    }
+    return L.total;
+}
+
+size_t ffpa_fp8_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D)
+{
+    return ffpa_fp8_workspace_layout(B, Hq, Hkv, Nq, Nkv, D, nullptr);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validation shared by the FP8 entry points; fills `pb` on success.
+ffpa_status check_fp8(ffpa_dtype dt, const ffpa_view& q, const ffpa_view& k, const ffpa_view& v, const void* ws,
+                      size_t ws_bytes, int B, int Hq, int Hkv, int Nq, int Nkv, int D, float scale, ffpa::Problem* pb)
+{
+    FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
+    FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
+    if (D % 256 != 0 || D > 768)
+        return fail(FFPA_ERR_NOT_SUPPORTED, "fp8 forward: D=%d must be 256, 512 or 768", D);
+    const long q_rows = static_cast<long>(B) * Hq * Nq;
+    if (q_rows > 0 && Nkv < 1) return fail(FFPA_ERR_NOT_SUPPORTED, "fp8 forward: Nkv must be >= 1");
+    FFPA_TRY(check_view(q, q_rows > 0, "q", B, Hq, Nq));
+    FFPA_TRY(check_view(k, q_rows > 0, "k", B, Hkv, Nkv));
+    FFPA_TRY(check_view(v, q_rows > 0, "v", B, Hkv, Nkv));
+    if (q_rows > 0) {
+        const size_t need = ffpa::fp8_layout(B, Hq, Hkv, Nq, Nkv, D).total;
+        if (ws_bytes < need)
+            return fail(FFPA_ERR_INVALID_VALUE, "fp8 workspace too small: %zu < %zu bytes", ws_bytes, need);
+        if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u))
+            return fail(FFPA_ERR_INVALID_VALUE, "fp8 workspace must be non-NULL and 256-byte aligned");
+    }
+    *pb = dense_problem(B, Hq, Hkv, Nq, Nkv, D, 0, scale);
+    pb->vq = to_view(q);
+    pb->vk = to_view(k);
+    pb->vv = to_view(v);
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+ffpa_status ffpa_fp8_quantize(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, void* workspace,
+                              size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                              ffpa_stream_t stream)
+{
+    ffpa::Problem pb;
+    FFPA_TRY(check_fp8(dt, q, k, v, workspace, workspace_bytes, B, Hq, Hkv, Nq, Nkv, D, 1.f, &pb));
+    if (static_cast<long>(B) * Hq * Nq == 0) return ok();
+    ffpa::FwdArgs a{};
+    a.pb = pb;
+    FFPA_TRY(device_ctl(&a.ctl));
+    a.bf16 = dt == FFPA_BF16;
+    a.q = q.data;
+    a.k = k.data;
+    a.v = v.data;
+    return launch_result(ffpa::launch_fp8_quantize(a, workspace, reinterpret_cast<cudaStream_t>(stream)),
+                         "fp8 quantize launch");
+}
+
+ffpa_status ffpa_fwd_fp8(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o, float* lse,
+                         void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                         int causal, float scale, ffpa_stream_t stream)
+{
+    ffpa::Problem pb;
+    FFPA_TRY(check_fp8(dt, q, k, v, workspace, workspace_bytes, B, Hq, Hkv, Nq, Nkv, D, scale, &pb));
+    const long q_rows = static_cast<long>(B) * Hq * Nq;
+    FFPA_TRY(check_view(o, q_rows > 0, "o", B, Hq, Nq));
+    FFPA_TRY(check_ptr(lse, q_rows > 0, "lse"));
+    if (q_rows == 0) return ok();
+    pb.causal = causal != 0;
+    pb.vo = to_view(o);
+    ffpa::FwdArgs a{};
+    a.pb = pb;
+    FFPA_TRY(device_ctl(&a.ctl));
+    a.bf16 = dt == FFPA_BF16;
+    a.q = q.data;
+    a.k = k.data;
+    a.v = v.data;
+    a.o = o.data;
+    a.lse = lse;
+    return launch_result(ffpa::launch_fwd_fp8(a, workspace, reinterpret_cast<cudaStream_t>(stream), true),
+                         "fp8 launch");
+}
+
+ffpa_status ffpa_fwd_fp8_quantized(ffpa_dtype dt, ffpa_view o, float* lse, const void* workspace,
+                                   size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal,
+                                   float scale, ffpa_stream_t stream)
+{
+    // the views of q/k/v are not read: validate with dense views over the workspace
+    void* ws = const_cast<void*>(workspace);
+    const ffpa_view vq{ws, static_cast<long long>(Hq) * Nq * D, static_cast<long long>(Nq) * D, D};
+    const ffpa_view vk{ws, static_cast<long long>(Hkv) * Nkv * D, static_cast<long long>(Nkv) * D, D};
+    ffpa::Problem pb;
+    FFPA_TRY(check_fp8(dt, vq, vk, vk, workspace, workspace_bytes, B, Hq, Hkv, Nq, Nkv, D, scale, &pb));
+    const long q_rows = static_cast<long>(B) * Hq * Nq;
+    FFPA_TRY(check_view(o, q_rows > 0, "o", B, Hq, Nq));
+    FFPA_TRY(check_ptr(lse, q_rows > 0, "lse"));
+    if (q_rows == 0) return ok();
+    pb.causal = causal != 0;
+    pb.vo = to_view(o);
+    ffpa::FwdArgs a{};
+    a.pb = pb;
+    FFPA_TRY(device_ctl(&a.ctl));
+    a.bf16 = dt == FFPA_BF16;
+    a.o = o.data;
+    a.lse = lse;
+    return launch_result(ffpa::launch_fwd_fp8(a, const_cast<void*>(workspace),
+                                              reinterpret_cast<cudaStream_t>(stream), false),
+                         "fp8 launch");
+}
+
 size_t ffpa_bwd_workspace_bytes(ffpa_dtype, int B, int Hq, int, int Nq, int, int)
 {
     if (B < 0 || Hq < 0 || Nq < 0) return 0;

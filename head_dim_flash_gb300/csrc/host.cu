@@ -96,6 +96,41 @@ bool make_slab_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_
     return r == CUDA_SUCCESS;
 }
 
+// e4m3 codes of a contiguous [B, H, N, D] tensor as (128 bytes, N, D/128
+// chunks, H, B): one box of rows x chunks lands as `chunks` row-blocks of
+// rows x 128 bytes, as for the 16-bit maps.
+bool make_u8_slab_map(CUtensorMap* m, const void* base, int B, int H, int N, int D, int rows, int chunks)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || N <= 0 || D % 128 != 0) return false;
+    const cuuint64_t dims[5] = {128, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(D / 128),
+                                static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[4] = {static_cast<cuuint64_t>(D), 128, static_cast<cuuint64_t>(N) * D,
+                                   static_cast<cuuint64_t>(H) * N * D};
+    const cuuint32_t box[5] = {128, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(chunks), 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// e4m3 V^T [B, Hkv, D, ldv] as (keys, D, Hkv, B) with boxes of 128 keys x
+// box_rows head-dim rows (keys past N read as zero).
+bool make_vt_map(CUtensorMap* m, const void* base, int B, int Hkv, int D, int N, int ldv, int box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || N <= 0 || ldv % 16 != 0) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(D),
+                                static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(ldv), static_cast<cuuint64_t>(D) * ldv,
+                                   static_cast<cuuint64_t>(Hkv) * D * ldv};
+    const cuuint32_t box[4] = {128, static_cast<cuuint32_t>(box_rows), 1, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms()
 {
     int dev = 0, n = 0;

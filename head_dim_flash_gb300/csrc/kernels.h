@@ -75,7 +75,23 @@ struct XArgs {
     // launch as a programmatic dependent of the previous kernel of the stream
     // (which must be one of these GEMM kernels that reads nothing this one writes)
     int pdl;
+    // FP8 forward: e4m3 q8 / k8 (q, k above point at them), V transposed
+    // [B, Hkv, D, ldv], and the fp32 dequantization scales per (batch, head)
+    int f8;
+    const void* v8t;
+    int ldv;
+    const float *f8_sq, *f8_sk, *f8_sv;
 };
+
+// Workspace of the FP8 forward (byte offsets, 256-byte aligned regions).
+struct Fp8Layout {
+    size_t q8, k8, v8t, sq, sk, sv, part, total;
+    int ldv;
+};
+Fp8Layout fp8_layout(int B, int Hq, int Hkv, int Nq, int Nkv, int D);
+cudaError_t launch_fp8_quantize(const FwdArgs& a, void* workspace, cudaStream_t s);
+// (quantization pass, then) the CTA-pair forward on the e4m3 operands in `workspace`
+cudaError_t launch_fwd_fp8(const FwdArgs& a, void* workspace, cudaStream_t s, bool quantize);
 
 // Runs one of the four GEMM kernels, in the CTA-pair form (2-SM MMAs,
 // clusters of 2C CTAs, head dims that are multiples of 128 up to 768) or the
@@ -110,6 +126,8 @@ bool make_slab_map(CUtensorMap* m, const void* base, const Problem& pb, bool kv_
 inline bool q_side_empty(const Problem& pb) { return pb.varlen ? pb.total_q == 0 : (pb.Nq == 0 || pb.B == 0); }
 inline bool kv_side_empty(const Problem& pb) { return pb.varlen ? pb.total_k == 0 : (pb.Nkv == 0 || pb.B == 0); }
 
+bool make_u8_slab_map(CUtensorMap* m, const void* base, int B, int H, int N, int D, int rows, int chunks);
+bool make_vt_map(CUtensorMap* m, const void* base, int B, int Hkv, int D, int N, int ldv, int box_rows);
 int num_sms();
 
 // Records `fmt` as the thread's last-error message (ffpa_last_error) and

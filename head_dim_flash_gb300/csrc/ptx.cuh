@@ -439,6 +439,30 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// The same pair MMA on 8-bit operands (kind::f8f6f4; with format code 0 in
+// the descriptor's A and B fields both are e4m3, fp32 accumulate): K = 32
+// elements, i.e. the same 32 bytes per instruction as the 16-bit form.
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// two fp32 values -> two e4m3 bytes (lo in the low byte), nearest even, saturating
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Arrive once on the mbarrier at this offset in every CTA of `cta_mask` when
 // all pair MMAs issued by this thread so far have completed.
 __device__ __forceinline__ void umma_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask)

@@ -99,7 +99,12 @@ __host__ __device__ inline int pair_stats_bytes(int op, int C)
     return (b + 1023) & ~1023;
 }
 
-template <int OP, bool BF16, bool VARLEN>
+// F8 (forward only): Q, K and P are e4m3 and the value operand is the e4m3
+// transpose of V (K-major); 128-byte chunks hold 128 elements, the Z tile is
+// 16 KiB, the MMAs are kind::f8f6f4 (the same 32 bytes per instruction), and
+// the per-head dequantization scales enter the softmax exponent (Q, K) and
+// the epilogue (V). BF16 is then the output type.
+template <int OP, bool BF16, bool VARLEN, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     pair_kernel(const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tA2,
                 const __grid_constant__ CUtensorMap tB1, const __grid_constant__ CUtensorMap tB2,
@@ -170,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int n_steps = (n_ct + C - 1) / C;
 
-    const int nd = pb.D / 64;          // 64-wide head-dim chunks
+    constexpr int kZ = F8 ? 16384 : 32768;  // bytes of one Z tile half (128 rows x 128 columns)
+    const int nd = F8 ? pb.D / 128 : pb.D / 64;  // 128-byte head-dim chunks (64 or 128 elements)
     const int nb4 = (nd + 3) / 4;      // groups of four chunks (one column-operand box each)
     const int d0 = c * 256;            // first column of my pair's slab
     const int d_pad = (pb.D + 127) & ~127;
@@ -184,8 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem[];
     const int nbuf = gm.nbuf;
     uint8_t* sA1 = smem;                          // resident row-operand chunks, two per 32 KiB
-    uint8_t* sZ = sA1 + (gm.res / 2) * kSlot;     // Z slots, 32 KiB each: [C-1 other pairs + own][nbuf]
-    float* stats = reinterpret_cast<float*>(sZ + C * nbuf * 32768);
+    uint8_t* sZ = sA1 + (gm.res / 2) * kSlot;     // Z slots, kZ bytes each: [C-1 other pairs + own][nbuf]
+    float* stats = reinterpret_cast<float*>(sZ + C * nbuf * kZ);
     uint8_t* sRing = reinterpret_cast<uint8_t*>(stats) + pair_stats_bytes(OP, C);
     if (smem_u32(smem) & 1023u) {  // uniform over the cluster: report, do not run misaligned
         if (threadIdx.x == 0) atomicCAS(a.ctl.status, 0u, 5u | (0xffu << 8));
@@ -229,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (C > 1) {
             for (int i = 0; i < C - 1; ++i)
-                for (int bb = 0; bb < nbuf; ++bb) mbar_arrive_expect_tx(&sh.zpeer[i][bb], 32768);
+                for (int bb = 0; bb < nbuf; ++bb) mbar_arrive_expect_tx(&sh.zpeer[i][bb], kZ);
             if (OP == XOP_FWD) {
                 mbar_arrive_expect_tx(&sh.rmax[0], 512 * (C - 1));
                 mbar_arrive_expect_tx(&sh.rmax[1], 512 * (C - 1));
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the CTA of pair p that holds my rows has rank 2p + rh.
     auto slot_of = [&](int writer, int consumer) { return writer < consumer ? writer : writer - 1; };
     auto xrank = [&](int p) { return 2 * p + rh; };
-    auto zslot = [&](int slot, int bb) { return sZ + (slot * nbuf + bb) * 32768; };  // slot C-1 = own
+    auto zslot = [&](int slot, int bb) { return sZ + (slot * nbuf + bb) * kZ; };  // slot C-1 = own
     // Step s uses Z buffer s % nbuf for the (s / nbuf)-th time.
     auto zbuf = [&](int s) { return s % nbuf; };
     auto zpar = [&](int s) { return static_cast<uint32_t>((s / nbuf) & 1); };
@@ -337,13 +343,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // value operand of step s: per column tile (own pair's tile first), one
             // box of the tile's 128 keys x my two 64-wide chunks of the slab
+            // (F8: one 16 KiB box of my 128 head-dim rows of V^T x the tile's 128
+            // keys, two tiles per slot, the second repeated when C is odd)
             auto load_value = [&](int s) -> bool {
-                for (int k = 0; k < C; ++k) {
-                    const int t = s * C + (c + k) % C;
-                    const int hh = col_head(t);
-                    if (!put(&tW, col_co(col_row0(t)), w_chunk, hh)) return false;
+                if constexpr (F8) {
+                    const int vt_row = d0 + rh * 128;
+                    for (int k = 0; k < C; k += 2) {
+                        const int ta = s * C + (c + k) % C;
+                        const int tb = s * C + (c + min(k + 1, C - 1)) % C;
+                        bool got = true;
+                        if (pos % nprod == me) {
+                            got = mbar_wait(&sh.empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, PS_PROD);
+                            if (got) {
+                                uint8_t* dst = sRing + rp.slot * kSlot;
+                                tma_load_4d_pair(dst, &tW, lead_full(rp.slot), col_co(col_row0(ta)), vt_row,
+                                                 col_head(ta), bco);
+                                tma_load_4d_pair(dst + 16384, &tW, lead_full(rp.slot), col_co(col_row0(tb)), vt_row,
+                                                 col_head(tb), bco);
+                            }
+                        }
+                        rp.advance(gm.stages);
+                        ++pos;
+                        if (!got) return false;
+                    }
+                    return true;
+                } else {
+                    for (int k = 0; k < C; ++k) {
+                        const int t = s * C + (c + k) % C;
+                        const int hh = col_head(t);
+                        if (!put(&tW, col_co(col_row0(t)), w_chunk, hh)) return false;
+                    }
+                    return true;
                 }
-                return true;
             };
             if (n_steps > 0) ok = load_score(0);
             for (int s = 0; ok && s < n_steps; ++s) {
@@ -365,8 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
             // -------------------------------------------------- MMA issuer (pair)
             if (elect_one()) {
-                const uint32_t idesc_s = idesc_f16(256, 128, BF16, false, false);
-                const uint32_t idesc_v = idesc_f16(256, sw, BF16, false, true);
+                // (F8: format code 0 = e4m3 in both operand fields; V^T is K-major)
+                const uint32_t idesc_s = idesc_f16(256, 128, F8 ? false : BF16, false, false);
+                const uint32_t idesc_v = idesc_f16(256, sw, F8 ? false : BF16, false, !F8);
+                auto mma = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t id, uint32_t acc) {
+                    if constexpr (F8)
+                        umma_f8_pair(d, ad, bd, id, acc);
+                    else
+                        umma_f16_pair(d, ad, bd, id, acc);
+                };
                 RingPos rp;
                 bool ok = true;
                 if (gm.res > 0 && n_steps > 0) {
@@ -422,9 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (d >= nd) break;
 #pragma unroll
                                     for (int kk = 0; kk < 4; ++kk)
-                                        umma_f16_pair(dst, sdesc_sw128(smem_u32(A + u2 * 16384 + kk * 32), 16, 1024),
-                                                      sdesc_sw128(smem_u32(B + (2 * h2 + u2) * 8192 + kk * 32), 16, 1024),
-                                                      idesc_s, (d | kk) != 0);
+                                        mma(dst, sdesc_sw128(smem_u32(A + u2 * 16384 + kk * 32), 16, 1024),
+                                            sdesc_sw128(smem_u32(B + (2 * h2 + u2) * 8192 + kk * 32), 16, 1024),
+                                            idesc_s, (d | kk) != 0);
                                 }
                                 if (a_slot >= 0) give(a_slot);
                             }
@@ -438,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 auto issue_value = [&](int s) -> bool {
                     const int bb = zbuf(s);
+                    const uint8_t* w8 = nullptr;  // F8: the slot holding V^T of two tiles
                     const uint32_t par = zpar(s);
                     // own tile: written by both CTAs' elementwise threads
                     if (!mbar_wait(&sh.z_full[bb], par, abort_flag, status, lim, PS_ZFULL)) return false;
@@ -451,12 +490,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!mbar_wait_cluster(&sh.zpeer[slot_of(cc, c)][bb], par, abort_flag, status, lim, PS_ZPEER))
                                 return false;
                             // arm the buffer's next use before this step's slot_free lets the writer in
-                            mbar_arrive_expect_tx(&sh.zpeer[slot_of(cc, c)][bb], 32768);
+                            mbar_arrive_expect_tx(&sh.zpeer[slot_of(cc, c)][bb], kZ);
                             if (k == 1 && !mbar_wait_cluster(&sh.zpair_peer[bb], par, abort_flag, status, lim, PS_ZPAIR))
                                 return false;
                             tc_fence_after();
                         }
-                        {
+                        if constexpr (F8) {
+                            // two tiles per slot: V^T of tile k at byte (k & 1) * 16 KiB
+                            if ((k & 1) == 0) {
+                                w8 = take();
+                                if (!w8) return false;
+                            }
+                            const uint8_t* W = w8 + (k & 1) * 16384;
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                // keys 32 t of the tile: 32 bytes into Z's and V^T's 128-byte rows
+                                const uint32_t acc = (s | k | t) != 0;
+                                mma(t_acc, sdesc_sw128(smem_u32(zs + t * 32), 16, 1024),
+                                    sdesc_sw128(smem_u32(W + t * 32), 16, 1024), idesc_v, acc);
+                            }
+                            if ((k & 1) == 1 || k == C - 1) {
+                                give(rp.slot);
+                                rp.advance(gm.stages);
+                            }
+                        } else {
                             const uint8_t* W = take();
                             if (!W) return false;
 #pragma unroll
@@ -522,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int p = (c + kp) % C;
                         uint64_t* zb = &sh.zpeer[slot_of(p, c)][bb];
                         if (mbar_test_cluster(zb, zpar(np))) {
-                            mbar_arrive_expect_tx(zb, 32768);  // arm the buffer's next use
+                            mbar_arrive_expect_tx(zb, kZ);  // arm the buffer's next use
                             progress = true;
                             if (++kp == C) {
                                 mbar_arrive_remote(mapa_shared(smem_u32(&sh.zpair_peer[bb]), lead_rank));
@@ -564,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = mbar_wait_cluster(&sh.slot_free[p][bb], zpar(s) ^ 1u, abort_flag, status, lim, PS_SLOT);
                     if (ok)
                         bulk_copy_s2cluster(mapa_shared(smem_u32(zslot(slot_of(c, p), bb)), xrank(p)), zslot(C - 1, bb),
-                                            32768, mapa_shared(smem_u32(&sh.zpeer[slot_of(c, p)][bb]), xrank(p)));
+                                            kZ, mapa_shared(smem_u32(&sh.zpeer[slot_of(c, p)][bb]), xrank(p)));
                 }
                 if (!ok) break;
             }
@@ -580,7 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = ew >> 7;
         const int col0 = half * 64;                // my columns [col0, col0 + 64)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const float c2 = pb.scale_log2;
+        // F8: S = sq * sk * (Q8 K8^T), so the dequantization scales join the exponent
+        const float c2 = F8 ? pb.scale_log2 * a.f8_sq[static_cast<size_t>(b) * pb.Hq + h] *
+                                  a.f8_sk[static_cast<size_t>(b) * pb.Hkv + hk]
+                            : pb.scale_log2;
         const int row = r0 + r;  // query (rows = queries) or key (rows = keys)
         // rows = queries: legal keys [0, key_end); rows = keys: legal queries [i_min, lq)
         const int key_end = pb.causal ? min(lk, row + off + 1) : lk;
@@ -715,6 +775,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = new_ref;
                 const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
                 float sum = 0.f;
+                // 16-bit P: z[q2 * 16 + e] holds columns 2e, 2e+1 of my q2-th 32; e4m3 P
+                // (F8): z[q2 * 8 + e / 2] holds columns 4(e/2) .. 4(e/2)+3, low byte first
+                uint32_t pend = 0;  // F8: the low half of z[q2 * 8 + e / 2], written at odd e
+                auto put_p = [&](int q2, int e, float p0, float p1) {
+                    if constexpr (F8) {
+                        const uint32_t v = cvt_e4m3x2(p0, p1);
+                        if (e & 1)
+                            z[q2 * 8 + (e >> 1)] = pend | (v << 16);
+                        else
+                            pend = v;
+                    } else {
+                        z[q2 * 16 + e] = pack2<BF16>(p0, p1);
+                    }
+                };
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
                     const uint32_t (&x)[32] = q2 ? xb : xa;
@@ -725,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float p0 = ex2_approx(fmaf(__uint_as_float(x[2 * e]), c2, -mu));
                             const float p1 = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), c2, -mu));
                             sum += p0 + p1;
-                            z[q2 * 16 + e] = pack2<BF16>(p0, p1);
+                            put_p(q2, e, p0, p1);
                         }
                     } else {
 #pragma unroll
@@ -733,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float p0 = (2 * e < lim2) ? ex2_approx(fmaf(__uint_as_float(x[2 * e]), c2, -mu)) : 0.f;
                             const float p1 = (2 * e + 1 < lim2) ? ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), c2, -mu)) : 0.f;
                             sum += p0 + p1;
-                            z[q2 * 16 + e] = pack2<BF16>(p0, p1);
+                            put_p(q2, e, p0, p1);
                         }
                     }
                 }
@@ -845,10 +919,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             uint8_t* zown = zslot(C - 1, bb);
+            if constexpr (F8) {
+                // one 128-byte row of 128 e4m3 values: my 64 columns are 16-byte units 4 half .. 4 half + 3
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<uint4*>(zown + half * 16384 + sw128_offset(r, u)) =
-                    make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4*>(zown + sw128_offset(r, 4 * half + u)) =
+                        make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<uint4*>(zown + half * 16384 + sw128_offset(r, u)) =
+                        make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
+            }
             fence_proxy_async_smem();
             mbar_arrive(&sh.z_full[bb]);
         }
@@ -887,6 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             View ov;
             if (OP == XOP_FWD) {
                 mul = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                if constexpr (F8) mul *= a.f8_sv[static_cast<size_t>(b) * pb.Hkv + hk];  // O = sv * (P V8) / l
                 out = a.o;
                 ov = pb.vo;
             } else if (OP == XOP_DQ) {
@@ -951,11 +1034,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) pdl_wait();
 }
 
-template <int OP, bool BF16, bool VARLEN>
+template <int OP, bool BF16, bool VARLEN, bool F8 = false>
 cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const PGeo& gm, int n_rt, int bz, int smem,
                       cudaStream_t s)
 {
-    auto kern = pair_kernel<OP, BF16, VARLEN>;
+    auto kern = pair_kernel<OP, BF16, VARLEN, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -994,15 +1077,19 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const bool rows_q = (op == XOP_FWD || op == XOP_DQ);
     if (rows_q ? q_empty : kv_empty) return cudaSuccess;  // no output rows
     if (pb.D % 64 != 0) return cudaErrorInvalidConfiguration;  // chunked 5-D maps need D % 64 == 0
-    const int nd = pb.D / 64;
+    // FP8 forward: dense, head dims with whole 256-column slabs (2 or 3 pairs, or 1)
+    const bool f8 = a.f8 != 0;
+    if (f8 && (op != XOP_FWD || pb.varlen || pb.D % 256 != 0 || pb.D > 768)) return cudaErrorInvalidConfiguration;
+    const int nd = f8 ? pb.D / 128 : pb.D / 64;  // 128-byte chunks
+    const int zb = f8 ? 16384 : 32768;           // bytes of one Z tile half
     const int d_pad = (pb.D + 127) & ~127;
     PGeo gm;
     gm.C = (d_pad + 255) / 256;
     if (gm.C > kMaxC) return cudaErrorInvalidConfiguration;
     const int budget = kMaxSmem - static_cast<int>(sizeof(StaticSmem));
     // double-buffer the Z slots when that leaves a ring of >= 4 stages
-    gm.nbuf = (budget - 2 * gm.C * 32768 - pair_stats_bytes(op, gm.C) >= 4 * kSlot) ? 2 : 1;
-    const int slots_bytes = gm.nbuf * gm.C * 32768;
+    gm.nbuf = (budget - 2 * gm.C * zb - pair_stats_bytes(op, gm.C) >= 4 * kSlot) ? 2 : 1;
+    const int slots_bytes = gm.nbuf * gm.C * zb;
     gm.nprod = 2;  // measured on GB300: 2 lanes beat 1, 3 and 4 with 32 KiB boxes
     // keep as many leading chunk pairs of the first row operand resident as leave
     // a ring of >= 5 stages (they are reused by every step of the work unit)
@@ -1037,6 +1124,20 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     auto val = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 128, 2, x.v); };
     int n_rows;
     int bz;
+    if (f8) {
+        // e4m3 codes: q8 (rows), k8 (columns), V^T (value operand, 128 head-dim rows per CTA)
+        okm = make_u8_slab_map(&m[0], a.q, pb.B, pb.Hq, pb.Nq, pb.D, 128, 2) &&
+              make_u8_slab_map(&m[2], a.k, pb.B, pb.Hkv, pb.Nkv, pb.D, 64, 4) &&
+              make_vt_map(&m[4], a.v8t, pb.B, pb.Hkv, pb.D, pb.Nkv, a.ldv, 128);
+        m[1] = m[0];
+        m[3] = m[2];
+        if (!okm) return cudaErrorInvalidValue;
+        const int n_rt8 = (pb.Nq + 255) / 256;
+        const int bz8 = pb.B * pb.Hq;
+        if (n_rt8 == 0 || bz8 == 0) return cudaSuccess;
+        return a.bf16 ? launch_op<XOP_FWD, true, false, true>(a, m, gm, n_rt8, bz8, smem, s)
+                      : launch_op<XOP_FWD, false, false, true>(a, m, gm, n_rt8, bz8, smem, s);
+    }
     switch (op) {
     case XOP_FWD:
         row(0, sq); row(1, sq); col(2, sk); col(3, sk); val(4, sv);

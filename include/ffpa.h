@@ -137,6 +137,38 @@ FFPA_API ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ff
                                      void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv,
                                      int D, int causal, float scale, ffpa_stream_t stream);
 
+/*
+ * FP8 forward (FFPA docs, "Backends Overview" page: the FP8 forward takes
+ * fp16/bf16 Q/K/V and quantizes them for the kernel). The inputs are
+ * quantized to e4m3 with one fp32 scale per (batch, head) and tensor
+ * (amax / 448; codes = round-to-nearest-even, saturating, of x * 448 / amax),
+ * then O = softmax(scale * S) V runs on the e4m3 operands with fp32
+ * accumulation; P is rounded to e4m3 for the P V product. O (bf16/fp16 as
+ * the inputs) and LSE (fp32 [B, Hq, Nq]) as in ffpa_fwd_strided.
+ *   D must be 256, 512 or 768 and Nkv >= 1 (else FFPA_ERR_NOT_SUPPORTED);
+ *   dense views only. workspace: device scratch of at least
+ *   ffpa_fp8_workspace_bytes() bytes, 256-byte aligned; it holds the codes
+ *   and scales afterwards, at the offsets ffpa_fp8_workspace_layout() gives:
+ *   offsets[0] q8 [B, Hq, Nq, D], [1] k8 [B, Hkv, Nkv, D], [2] V^T codes
+ *   [B, Hkv, D, ldv], [3] sq fp32 [B*Hq], [4] sk fp32 [B*Hkv], [5] sv fp32
+ *   [B*Hkv], [6] ldv (Nkv rounded up to 16), [7] total bytes.
+ * ffpa_fp8_quantize runs only the quantization into the workspace.
+ */
+FFPA_API size_t ffpa_fp8_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D);
+FFPA_API size_t ffpa_fp8_workspace_layout(int B, int Hq, int Hkv, int Nq, int Nkv, int D, size_t* offsets);
+FFPA_API ffpa_status ffpa_fp8_quantize(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, void* workspace,
+                                       size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                                       ffpa_stream_t stream);
+FFPA_API ffpa_status ffpa_fwd_fp8(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o, float* lse,
+                                  void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv,
+                                  int D, int causal, float scale, ffpa_stream_t stream);
+/* The attention of ffpa_fwd_fp8 alone, on a workspace that ffpa_fp8_quantize
+ * (or ffpa_fwd_fp8) filled for the same sizes: for inputs quantized once and
+ * attended many times (a cached e4m3 K/V). No q/k/v pointers are read. */
+FFPA_API ffpa_status ffpa_fwd_fp8_quantized(ffpa_dtype dt, ffpa_view o, float* lse, const void* workspace,
+                                            size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                                            int causal, float scale, ffpa_stream_t stream);
+
 /* Workspace bytes ffpa_bwd needs for this problem (fp32 row statistics). */
 FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 

@@ -136,7 +136,8 @@ def p_rounding_bound(qd, kd, vd, causal: bool = False, scale: float | None = Non
             s = np.where(legal, s, -np.inf)
             mx = s.max(axis=1, keepdims=True)
             has = np.isfinite(mx[:, 0])
-            el = np.where(legal & has[:, None], np.exp(np.where(has[:, None], s - mx, -np.inf)), 0.0)
+            ok = legal & has[:, None]
+            el = np.where(ok, np.exp(np.where(ok, s - np.where(has[:, None], mx, 0.0), -np.inf)), 0.0)
             L = el.sum(axis=1)
             vsum = legal.astype(np.float64) @ np.abs(vd[b, h // G])   # sum over legal keys of |v|
             with np.errstate(divide="ignore", invalid="ignore"):

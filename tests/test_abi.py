@@ -232,3 +232,44 @@ def test_decode_supported_predicate():
     assert not api.decode_supported(torch.zeros(2, 8, 1, 352), torch.zeros(2, 1, 9, 352))  # D % 64 != 0
     big = torch.zeros(1, 1, 1, 64).expand(1, 64, 16400, 64)          # 64 x 1025 row blocks (shape only)
     assert not api.decode_supported(big, torch.zeros(1, 64, 9, 64))  # grid limit
+
+
+def _fp8(lib, fn="fwd", D=512, Nq=8, Nkv=8, ws=FAKE, ws_bytes=None, Hq=2, Hkv=1, lse=FAKE):
+    vq = _view(sb=Hq * Nq * D, sh=Nq * D, sn=D)
+    vk = _view(sb=Hkv * Nkv * D, sh=Nkv * D, sn=D)
+    if ws_bytes is None:
+        ws_bytes = lib.ffpa_fp8_workspace_bytes(1, Hq, Hkv, Nq, Nkv, D)
+    if fn == "fwd":
+        return lib.ffpa_fwd_fp8(0, vq, vk, vk, vq, lse, ws, ws_bytes, 1, Hq, Hkv, Nq, Nkv, D, 0, 0.05, None)
+    return lib.ffpa_fp8_quantize(0, vq, vk, vk, ws, ws_bytes, 1, Hq, Hkv, Nq, Nkv, D, None)
+
+
+@pytest.mark.parametrize("fn", ["fwd", "quantize"])
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(D=320), 2, "256, 512 or 768"),
+    (dict(D=1024), 2, "256, 512 or 768"),
+    (dict(Nkv=0), 2, "Nkv"),
+    (dict(ws_bytes=1024), 1, "workspace too small"),
+    (dict(ws=FAKE + 64), 1, "aligned"),
+])
+def test_invalid_fp8_calls_are_rejected(lib, fn, kw, status, msg):
+    assert _fp8(lib, fn, **kw) == status
+    assert msg in lib.ffpa_last_error().decode()
+
+
+def test_fp8_forward_checks_lse(lib):
+    assert _fp8(lib, "fwd", lse=0) == 1
+    assert b"lse" in lib.ffpa_last_error()
+
+
+def test_fp8_workspace_layout():
+    from head_dim_flash_gb300 import _ffi
+
+    B, Hq, Hkv, Nq, Nkv, D = 2, 8, 2, 300, 777, 512
+    off = _ffi.ffpa_fp8_workspace_layout(B, Hq, Hkv, Nq, Nkv, D)
+    q8, k8, v8t, sq, sk, sv, ldv, total = off
+    assert ldv == 784  # Nkv rounded up to 16
+    assert all(o % 256 == 0 for o in (q8, k8, v8t, sq, sk, sv, total))
+    assert k8 >= q8 + B * Hq * Nq * D and v8t >= k8 + B * Hkv * Nkv * D and sq >= v8t + B * Hkv * D * ldv
+    assert sk >= sq + 4 * B * Hq and sv >= sk + 4 * B * Hkv and total > sv
+    assert _ffi.ffpa_fp8_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D) == total

@@ -1,0 +1,119 @@
+"""GPU parity of the FP8 (e4m3) forward against the oracle's FP8 reference.
+
+* Quantization: the e4m3 codes of Q, K and V (V transposed) and the fp32
+  per-(batch, head) scales are compared bit for bit (+0 and -0 count as the
+  same code).
+* Forward: O against the plain attention of the dequantized inputs (fp64),
+  element by element within
+      bound (the e4m3 rounding of P, oracle.fp8.p_rounding_bound)
+      + 2^-8 |O| (rounding of the 16-bit output)
+      + 1e-3 max|V| (fp32 accumulation order, exp2 approximation),
+  and LSE within 1e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8 as ofp8
+from head_dim_flash_gb300 import api
+from head_dim_flash_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from head_dim_flash_gb300 import build
+
+    build.build()
+    oracle.build()
+
+
+def same_codes(got, ref):
+    got = np.asarray(got, dtype=np.uint8)
+    ref = np.asarray(ref, dtype=np.uint8)
+    both_zero = ((got & 0x7F) == 0) & ((ref & 0x7F) == 0)
+    return np.all((got == ref) | both_zero)
+
+
+def check_quantization(inp, q, k, v):
+    _, views = api.fp8_quantize(q, k, v)
+    torch.cuda.synchronize()
+    for name, src in (("q", inp["q"]), ("k", inp["k"]), ("v", inp["v"])):
+        codes, scale = ofp8.quantize(src)
+        got_s = views["s" + name].cpu().numpy()
+        assert np.array_equal(got_s, scale), f"{name}: scales differ"
+        if name == "v":
+            n = codes.shape[2]
+            got = views["v8t"].cpu().numpy()[..., :n]
+            ref = codes.transpose(0, 1, 3, 2)
+        else:
+            got = views[name + "8"].cpu().numpy()
+            ref = codes
+        assert same_codes(got, ref), f"{name}: {int((got != ref).sum())} codes differ"
+
+
+def run_fp8(B, Hq, Hkv, Nq, Nkv, D, causal, dtype=torch.bfloat16, seed=0, amp=1.0, strided=False):
+    inp = workloads.random_dense(B, Hq, Hkv, Nq, Nkv, D, dtype, seed=seed, amplitude=amp, with_grad_out=False)
+    if strided:
+        # [B, N, H, D] storage seen as [B, H, N, D]
+        q, k, v = (inp[n].transpose(1, 2).contiguous().cuda().transpose(1, 2) for n in ("q", "k", "v"))
+    else:
+        q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    scale = 1.0 / math.sqrt(D)
+    check_quantization(inp, q, k, v)
+    o, lse = api.fwd_fp8(q, k, v, causal, scale)
+    api.get_status()
+    o_ref, lse_ref, (qd, kd, vd) = ofp8.attention_fwd_fp8(inp["q"], inp["k"], inp["v"], causal, scale)
+    bound = ofp8.p_rounding_bound(qd, kd, vd, causal, scale)
+    og = o.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(og))
+    vmax = np.abs(vd).max()
+    tol = bound + 2.0 ** -8 * np.abs(o_ref) + 1e-3 * vmax
+    err = np.abs(og - o_ref)
+    ratio = float((err / tol).max())
+    assert np.all(err <= tol), f"O: max err {err.max():.3e}, max err/tol {ratio:.3f}"
+    lg = lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.abs(lg[fin] - lse_ref[fin]) <= 1e-3), f"LSE max err {np.abs(lg[fin] - lse_ref[fin]).max():.3e}"
+    return ratio
+
+
+@pytest.mark.parametrize("D", [256, 512, 768])
+def test_fp8_head_dims(D):
+    run_fp8(1, 2, 2, 300, 300, D, False, seed=D)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nkv", [(1, 129), (256, 256), (257, 1000), (700, 333)])
+def test_fp8_ragged_and_causal(Nq, Nkv, causal):
+    run_fp8(1, 2, 1, Nq, Nkv, 512, causal, seed=Nq + Nkv)
+
+
+def test_fp8_gqa_fp16():
+    run_fp8(2, 8, 2, 200, 700, 512, True, dtype=torch.float16, seed=7, amp=0.5)
+
+
+def test_fp8_large_logits():
+    run_fp8(1, 2, 2, 256, 512, 512, False, seed=8, amp=3.0)
+
+
+def test_fp8_strided_views():
+    run_fp8(2, 4, 2, 130, 260, 512, False, seed=9, strided=True)
+
+
+def test_fp8_prequantized_matches_one_call():
+    # quantize once, attend from the workspace: bit-identical to ffpa_fwd_fp8
+    inp = workloads.random_dense(1, 4, 2, 200, 333, 512, torch.bfloat16, seed=12, with_grad_out=False)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o1, l1 = api.fwd_fp8(q, k, v, True, 0.05)
+    ws, _ = api.fp8_quantize(q, k, v)
+    o2, l2 = api.fwd_fp8_quantized(ws, q.shape, k.shape, q.dtype, True, 0.05)
+    api.get_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

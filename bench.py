@@ -10,11 +10,12 @@ same per-GPU workload (weak scaling; no data-path collective) and report the
 slowest rank's time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config headline|tiny|gqa|sweep320|sweep640|sweep1024|varlen|decode]
+                  [--config headline|tiny|gqa|sweep320|sweep640|sweep1024|varlen|decode|fp8]
 
 --config decode times the split-KV decode forward instead (GB/s of the
 bytes it must move; a step of it takes well under a millisecond, so give it
 a few thousand --steps for the clock samples to fall inside the timed region).
+--config fp8 times the e4m3 forward (ffpa_fwd_fp8: quantization + attention).
 """
 from __future__ import annotations
 
@@ -55,7 +56,7 @@ def workload(name):
 
     table = {"headline": W.HEADLINE, "tiny": W.TINY, "gqa": W.GQA_CAUSAL,
              "sweep320": W.SWEEP[0], "sweep640": W.SWEEP[1], "sweep1024": W.SWEEP[2], "varlen": W.VARLEN,
-             "decode": W.DECODE}
+             "decode": W.DECODE, "fp8": W.FP8}
     if name not in table:
         raise SystemExit(f"unknown config {name}; choose from {sorted(table)}")
     return table[name]
@@ -384,6 +385,144 @@ def decode_cpu_baseline(w, inp):
                       "fp64 C oracle, one batch entry per call"}
 
 
+FP8_METRIC = "fp8 (e4m3) forward TFLOPS, D=512 N=8192, bf16 in/out (1×GB300), % of the fp8 tensor peak"
+
+
+def run_fp8(args, w):
+    """FP8 workload: one ffpa_fwd_fp8 call per step (quantization pass + attention)."""
+    import torch
+
+    from head_dim_flash_gb300 import api
+    from head_dim_flash_gb300 import workloads as W
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = W.make_inputs(w, with_grad_out=False)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+    ws = api.fp8_workspace(q, k)
+    stream = torch.cuda.current_stream(dev)
+    f_fwd = flops(w)[0]
+
+    def step():
+        api.fwd_fp8(q, k, v, w.causal, w.scale, out=o, lse=lse, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    api.get_status()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    api.get_status()
+    ms_step = slowest_rank_ms(start.elapsed_time(end), world, dev) / args.steps
+    value = job_throughput(f_fwd, world, ms_step)
+
+    # per-kernel pass: the quantization alone, the attention alone (from the workspace)
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a_, b_ in evs:
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+
+    n_k = min(args.steps, 10)
+    quant_ms = timed(lambda: api.fp8_quantize(q, k, v, workspace=ws), n_k)
+    attn_ms = timed(lambda: api.fwd_fp8_quantized(ws, q.shape, k.shape, q.dtype, w.causal, w.scale, out=o, lse=lse),
+                    n_k)
+    api.get_status()
+    pk = peaks()
+    peak8 = 2.0 * pk["bf16_tflops_sustained"]
+    achieved = f_fwd / (attn_ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "kernel": "fp8 pair forward (attention, from the quantized workspace)",
+            "achieved": achieved, "peak": peak8, "unit": "TFLOP/s", "frac": achieved / peak8,
+            "traffic": measured_traffic(w, "fp8"),
+            "peak_source": f"{pk['source']} sustained bf16 x 2 (nominal e4m3 / bf16 dense ratio 4.5 / 2.25)"}
+    qbytes = 3 * w.B * w.Hq * w.Nq * w.D * 2 * 2 + 3 * w.B * w.Hq * w.Nq * w.D  # read twice, write codes
+
+    e2e = None
+    if not args.no_e2e:
+        host = {n: inp[n].pin_memory() for n in ("q", "k", "v")}
+        dev_t = {n: torch.empty_like(q if n == "q" else k) for n in host}
+        oh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+        def e2e_step():
+            for n in host:
+                dev_t[n].copy_(host[n], non_blocking=True)
+            api.fwd_fp8(dev_t["q"], dev_t["k"], dev_t["v"], w.causal, w.scale, out=o, lse=lse, workspace=ws)
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n = max(1, min(args.steps, 5))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(n):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ems = s0.elapsed_time(s1) / n
+        e2e = {"value": world * f_fwd / (ems / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ems,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+               "d2h_bytes_per_step": oh.numel() * oh.element_size() + lh.numel() * lh.element_size()}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = fp8_cpu_baseline(w, inp)
+    if rank == 0:
+        line = {
+            "metric": FP8_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate; bf16 in/out)", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nkv": w.Nkv, "D": w.D,
+                       "causal": w.causal, "l2": "inputs larger than L2 (each of q/k/v 268 MB)"},
+            "kernel_ms": {"quantize": quant_ms, "attention": attn_ms},
+            "quantize_gbs": qbytes / (quant_ms / 1e3) / 1e9,
+            "pct_peak_fp8": 100 * value / world / peak8,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
+            "gpu_launches": 4 * args.steps,  # amax, q/k codes, V^T codes, attention per step
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def fp8_cpu_baseline(w, inp, n_rows=1024):
+    """The oracle's FP8 reference on a bounded sample: quantization of head 0
+    and the attention of `n_rows` of its query rows against all keys."""
+    import oracle
+    from oracle import fp8 as ofp8
+
+    oracle.build()
+    cores = oracle.num_threads()
+    rows = list(range(min(n_rows, w.Nq)))
+    t0 = time.perf_counter()
+    qd = ofp8.dequantize(*ofp8.quantize(inp["q"][0:1, 0:1]))
+    kd = ofp8.dequantize(*ofp8.quantize(inp["k"][0:1, 0:1]))
+    vd = ofp8.dequantize(*ofp8.quantize(inp["v"][0:1, 0:1]))
+    oracle.attention_fwd_rows(qd[0, 0], kd[0, 0], vd[0, 0], rows, w.causal, w.scale)
+    dt = time.perf_counter() - t0
+    f = 4.0 * len(rows) * w.Nkv * w.D
+    return {"value": f / dt / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "seconds": dt,
+            "sample": f"e4m3 quantization of head 0 and the fp64 attention of {len(rows)} of its query rows x "
+                      f"{w.Nkv} keys (D={w.D})"}
+
+
 def run_ours(args):
     import torch
 
@@ -396,6 +535,8 @@ def run_ours(args):
     w = workload(args.config)
     if args.config == "decode":
         return run_decode(args, w)
+    if args.config == "fp8":
+        return run_fp8(args, w)
     if args.heads:
         import dataclasses
 

@@ -79,6 +79,10 @@ ALL = (TINY, HEADLINE, GQA_CAUSAL) + SWEEP + (VARLEN,)
 # key cache, eight query heads per kv head (the split-KV path).
 DECODE = Workload("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", 8, 32, 8, 1, 16384, 512, torch.bfloat16, False, 50)
 
+# FP8 forward: the dense headline shape and inputs, quantized to e4m3 for the kernel.
+FP8 = Workload("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", 1, 32, 32, 8192, 8192, 512,
+               torch.bfloat16, False, 1)
+
 
 def make_inputs(w: Workload, with_grad_out: bool = True):
     """Returns dict with q, k, v (and dO) as CPU tensors of w.dtype (+ cu_seqlens for varlen)."""

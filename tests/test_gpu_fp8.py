@@ -117,3 +117,34 @@ def test_fp8_prequantized_matches_one_call():
     o2, l2 = api.fwd_fp8_quantized(ws, q.shape, k.shape, q.dtype, True, 0.05)
     api.get_status()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_fp8_full_size_workload_sampled():
+    # the benchmarked FP8 workload in the benchmark's launch configuration:
+    # codes of sampled heads bit for bit, sampled query rows of those heads
+    # against the oracle within the bound (rows are independent: non-causal)
+    w = workloads.FP8
+    inp = workloads.make_inputs(w, with_grad_out=False)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    ws = api.fp8_workspace(q, k)
+    o, lse = api.fwd_fp8(q, k, v, w.causal, w.scale, workspace=ws)
+    api.get_status()
+    _, views = api.fp8_quantize(q, k, v, workspace=ws)
+    rng = np.random.default_rng(0)
+    for h in (0, 17, 31):
+        sl = slice(h, h + 1)
+        cq, sq = ofp8.quantize(inp["q"][:, sl])
+        ck, sk = ofp8.quantize(inp["k"][:, sl])
+        cv, sv = ofp8.quantize(inp["v"][:, sl])
+        assert same_codes(views["q8"][:, sl].cpu().numpy(), cq)
+        assert same_codes(views["k8"][:, sl].cpu().numpy(), ck)
+        assert same_codes(views["v8t"][:, sl, :, : w.Nkv].cpu().numpy(), cv.transpose(0, 1, 3, 2))
+        assert views["sq"][0, h].item() == sq[0, 0] and views["sv"][0, h].item() == sv[0, 0]
+        qd, kd, vd = ofp8.dequantize(cq, sq), ofp8.dequantize(ck, sk), ofp8.dequantize(cv, sv)
+        rows = sorted(set([0, w.Nq - 1]) | set(int(x) for x in rng.integers(0, w.Nq, 24)))
+        o_ref, lse_ref = oracle.attention_fwd_rows(qd[0, 0], kd[0, 0], vd[0, 0], rows, False, w.scale)
+        bound = ofp8.p_rounding_bound(qd[:, :, rows], kd, vd, False, w.scale)[0, 0]
+        og = o[0, h, rows].float().cpu().numpy().astype(np.float64)
+        tol = bound + 2.0 ** -8 * np.abs(o_ref) + 1e-3 * np.abs(vd).max()
+        assert np.all(np.abs(og - o_ref) <= tol), f"head {h}: max err {np.abs(og - o_ref).max():.3e}"
+        assert np.all(np.abs(lse[0, h, rows].cpu().numpy() - lse_ref) <= 1e-3)

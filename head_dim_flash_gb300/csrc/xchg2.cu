@@ -85,6 +85,7 @@ struct __align__(1024) StaticSmem {
     uint64_t zpeer[kMaxC][2], slot_free[kMaxC][2], stat[2], rmax[2], lsum, drain, half;
     uint32_t tmem_base;
     int abort_flag;
+    uint32_t relay_sink[4];  // (even rank) target of the odd rank's 4-byte relay stores
 };
 static_assert(sizeof(StaticSmem) == 1024, "static shared block must be exactly 1 KiB");
 
@@ -207,13 +208,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sh.a1, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.x_full[i], 1);
-            // X / Y read: the CTA's 8 elementwise warps (even rank: + 1 arrival forwarded by the odd rank)
+            // X / Y read: the CTA's 8 elementwise warps (even rank: + the MMA thread's arming
+            // arrival, whose 4 transaction bytes the odd rank's relay store completes)
             mbar_init(&sh.x_free[i], leader ? 9 : 8);
             mbar_init(&sh.stat[i], 256);
             mbar_init(&sh.rmax[i], 1);
             mbar_init(&sh.z_full[i], 256);    // own elementwise threads wrote the own Z buffer
-            mbar_init(&sh.zpair_own[i], 1);   // (even rank) the odd rank's own Z buffer is written
-            mbar_init(&sh.zpair_peer[i], 1);  // (even rank) the odd rank received the other pairs' Z
+            // (even rank) the odd rank's own Z buffer is written / it received the other
+            // pairs' Z: the MMA thread's arming arrival + 4 bytes of a relay store
+            mbar_init(&sh.zpair_own[i], 1);
+            mbar_init(&sh.zpair_peer[i], 1);
             mbar_init(&sh.acc[i], 1);
             for (int j = 0; j < kMaxC; ++j) {
                 mbar_init(&sh.zpeer[j][i], 1);
@@ -231,6 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // and live in the even rank.
         if (leader) {
             for (int i = 0; i < gm.stages; ++i) mbar_arrive_expect_tx(&sh.full[i], 2 * kSlot);
+            // the relayed events of the odd rank complete 4 transaction bytes each
+            for (int i = 0; i < 2; ++i) {
+                mbar_arrive_expect_tx(&sh.x_free[i], 4);
+                mbar_arrive_expect_tx(&sh.zpair_own[i], 4);
+                mbar_arrive_expect_tx(&sh.zpair_peer[i], 4);
+            }
             if (gm.res > 0 && n_steps > 0) mbar_arrive_expect_tx(&sh.a1, 2 * (gm.res / 2) * kSlot);
         }
         if (C > 1) {
@@ -428,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (T::kXdb ? s >= 2 : s >= 1) {
                             const uint32_t par = T::kXdb ? (((s - 2) >> 1) & 1) : ((s - 1) & 1);
                             if (!mbar_wait_cluster(&sh.x_free[fb], par, abort_flag, status, lim, PS_XFREE)) return false;
+                            mbar_arrive_expect_tx(&sh.x_free[fb], 4);  // arm the next phase's relay
                             tc_fence_after();
                         }
                         const uint32_t dst = t_x0 + (T::kXdb ? sb * 128 : prod * 128);
@@ -481,6 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // own tile: written by both CTAs' elementwise threads
                     if (!mbar_wait(&sh.z_full[bb], par, abort_flag, status, lim, PS_ZFULL)) return false;
                     if (!mbar_wait_cluster(&sh.zpair_own[bb], par, abort_flag, status, lim, PS_ZPAIR)) return false;
+                    mbar_arrive_expect_tx(&sh.zpair_own[bb], 4);  // arm the next phase's relay
                     tc_fence_after();
                     for (int k = 0; k < C; ++k) {
                         const int cc = (c + k) % C;
@@ -491,8 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 return false;
                             // arm the buffer's next use before this step's slot_free lets the writer in
                             mbar_arrive_expect_tx(&sh.zpeer[slot_of(cc, c)][bb], kZ);
-                            if (k == 1 && !mbar_wait_cluster(&sh.zpair_peer[bb], par, abort_flag, status, lim, PS_ZPAIR))
-                                return false;
+                            if (k == 1) {
+                                if (!mbar_wait_cluster(&sh.zpair_peer[bb], par, abort_flag, status, lim, PS_ZPAIR))
+                                    return false;
+                                mbar_arrive_expect_tx(&sh.zpair_peer[bb], 4);  // arm the next phase's relay
+                            }
                             tc_fence_after();
                         }
                         if constexpr (F8) {
@@ -545,13 +560,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else {
             // -------------------------------------------------- forwarder (odd rank)
-            // Relays this CTA's events to the even rank's MMA thread with one
-            // cluster-scope arrival each, so that the elementwise warps only ever
-            // arrive on barriers of their own CTA: X (and Y) read, own Z buffer
-            // written, and (C > 1) the other pairs' Z tiles landed here. Each kind
-            // of event is forwarded in step order; the kinds are polled together so
-            // that a late one does not hold back the others.
+            // Relays this CTA's events to the even rank's MMA thread, so that the
+            // elementwise warps only ever arrive on barriers of their own CTA: X
+            // (and Y) read, own Z buffer written, and (C > 1) the other pairs' Z
+            // tiles landed here. Each kind of event is forwarded in step order; the
+            // kinds are polled together so that a late one does not hold back the
+            // others. A relay is a 4-byte st.async into the even rank, whose
+            // complete-tx (release at cluster scope, after this thread's acquire of
+            // the local event) finishes the phase that the MMA thread armed; unlike
+            // a remote arrive it does not hold this thread until it lands.
             if (elect_one()) {
+                const uint32_t sink = mapa_shared(smem_u32(&sh.relay_sink[0]), lead_rank);
+                auto relay = [&](uint64_t* bar) { st_async_f32(sink, 0.f, mapa_shared(smem_u32(bar), lead_rank)); };
                 const int n_x = T::kTwo ? 2 * n_steps : n_steps;
                 int nx = 0, nz = 0, np = 0, kp = 1;
                 uint64_t t_last = global_timer_ns();
@@ -563,13 +583,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int idx = nx & 1;
                         const uint32_t par = static_cast<uint32_t>((nx >> 1) & 1);
                         if (mbar_test(&sh.x_free[idx], par)) {
-                            mbar_arrive_remote(mapa_shared(smem_u32(&sh.x_free[idx]), lead_rank));
+                            relay(&sh.x_free[idx]);
                             ++nx;
                             progress = true;
                         }
                     }
                     if (nz < n_steps && mbar_test(&sh.z_full[zbuf(nz)], zpar(nz))) {
-                        mbar_arrive_remote(mapa_shared(smem_u32(&sh.zpair_own[zbuf(nz)]), lead_rank));
+                        relay(&sh.zpair_own[zbuf(nz)]);
                         ++nz;
                         progress = true;
                     }
@@ -582,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_arrive_expect_tx(zb, kZ);  // arm the buffer's next use
                             progress = true;
                             if (++kp == C) {
-                                mbar_arrive_remote(mapa_shared(smem_u32(&sh.zpair_peer[bb]), lead_rank));
+                                relay(&sh.zpair_peer[bb]);
                                 kp = 1;
                                 ++np;
                             }

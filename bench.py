@@ -203,12 +203,17 @@ def cpu_baseline(w, inp, n_rows=8192):
 # counters).
 PAIR_SOURCES = ("xchg.cu", "xchg2.cu", "ptx.cuh", "tile_common.cuh", "kernels.h", "bwd.cu", "fwd.cu")
 DECODE_SOURCES = ("decode.cu", "ptx.cuh", "tile_common.cuh", "kernels.h")
+FP8_SOURCES = ("xchg2.cu", "fp8.cu", "ptx.cuh", "tile_common.cuh", "kernels.h", "host.cu")
 TRAFFIC = {
-    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 1343856128, "files": PAIR_SOURCES,
-                                             "sources": "3488af9ace94c242"},
+    # dK at 16 heads (551,807,488 + 118,287,616 bytes) scaled to 32
+    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 1340190208, "files": PAIR_SOURCES, "sources": "be2e8df3e0e29dd3"},
     # one ffpa_decode_fwd call: split kernel + combine
-    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2155079168, "files": DECODE_SOURCES,
-                                                                "sources": "849fec8fbaf221e6"},
+    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2155992576, "files": DECODE_SOURCES,
+                                                                "sources": "b33805713eaf2184"},
+    # the e4m3 attention kernel (reads q8, k8, V^T codes; writes O, LSE)
+    ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 639071232,
+                                                                             "files": FP8_SOURCES,
+                                                                             "sources": "fba59967d0e005de"},
 }
 
 

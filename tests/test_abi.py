@@ -273,3 +273,15 @@ def test_fp8_workspace_layout():
     assert k8 >= q8 + B * Hq * Nq * D and v8t >= k8 + B * Hkv * Nkv * D and sq >= v8t + B * Hkv * D * ldv
     assert sk >= sq + 4 * B * Hq and sv >= sk + 4 * B * Hkv and total > sv
     assert _ffi.ffpa_fp8_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D) == total
+
+
+def test_fp8_prequantized_entry_validates_before_any_launch(lib):
+    n = lib.ffpa_fp8_workspace_bytes(1, 2, 1, 8, 8, 512)
+    vo = _view(sb=2 * 8 * 512, sh=8 * 512, sn=512)
+    # workspace too small, misaligned, unsupported head dim, missing lse
+    assert lib.ffpa_fwd_fp8_quantized(0, vo, FAKE, FAKE, 64, 1, 2, 1, 8, 8, 512, 0, 0.05, None) == 1
+    assert lib.ffpa_fwd_fp8_quantized(0, vo, FAKE, FAKE + 32, n, 1, 2, 1, 8, 8, 512, 0, 0.05, None) == 1
+    assert lib.ffpa_fwd_fp8_quantized(0, _view(sb=2 * 8 * 320, sh=8 * 320, sn=320), FAKE, FAKE, n,
+                                      1, 2, 1, 8, 8, 320, 0, 0.05, None) == 2
+    assert lib.ffpa_fwd_fp8_quantized(0, vo, 0, FAKE, n, 1, 2, 1, 8, 8, 512, 0, 0.05, None) == 1
+    assert b"lse" in lib.ffpa_last_error()

@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--config", default="headline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--all", action="store_true", help="one line per workload (parity-size cases excluded)")
+    ap.add_argument("--all", action="store_true",
+                    help="one line per workload, decode and fp8 included (parity-size cases excluded)")
     ap.add_argument("--heads", type=int, default=0,
                     help="override Hq=Hkv (profiling a smaller case of the same kernels)")
     return ap.parse_args()
@@ -741,7 +742,7 @@ def main():
 
     build.build()
     if args.all:
-        for name in ("headline", "gqa", "sweep320", "sweep640", "sweep1024", "varlen"):
+        for name in ("headline", "gqa", "sweep320", "sweep640", "sweep1024", "varlen", "decode", "fp8"):
             args.config = name
             run_ours(args)
         return

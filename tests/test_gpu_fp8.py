@@ -96,6 +96,10 @@ def test_fp8_ragged_and_causal(Nq, Nkv, causal):
     run_fp8(1, 2, 1, Nq, Nkv, 512, causal, seed=Nq + Nkv)
 
 
+def test_fp8_d768_causal_gqa():
+    run_fp8(1, 6, 2, 300, 520, 768, True, seed=17)
+
+
 def test_fp8_gqa_fp16():
     run_fp8(2, 8, 2, 200, 700, 512, True, dtype=torch.float16, seed=7, amp=0.5)
 

@@ -152,3 +152,19 @@ def test_fp8_full_size_workload_sampled():
         tol = bound + 2.0 ** -8 * np.abs(o_ref) + 1e-3 * np.abs(vd).max()
         assert np.all(np.abs(og - o_ref) <= tol), f"head {h}: max err {np.abs(og - o_ref).max():.3e}"
         assert np.all(np.abs(lse[0, h, rows].cpu().numpy() - lse_ref) <= 1e-3)
+
+
+def test_fp8_all_zero_heads():
+    # an all-zero K head (scale 1, zero codes: uniform weights) and an all-zero V head
+    inp = workloads.random_dense(1, 4, 2, 130, 260, 512, torch.bfloat16, seed=21, with_grad_out=False)
+    inp["k"][:, 0] = 0
+    inp["v"][:, 1] = 0
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    check_quantization(inp, q, k, v)
+    o, lse = api.fwd_fp8(q, k, v, False, 0.05)
+    api.get_status()
+    o_ref, lse_ref, (qd, kd, vd) = ofp8.attention_fwd_fp8(inp["q"], inp["k"], inp["v"], False, 0.05)
+    tol = ofp8.p_rounding_bound(qd, kd, vd, False, 0.05) + 2.0 ** -8 * np.abs(o_ref) + 1e-3 * np.abs(vd).max()
+    assert np.all(np.abs(o.float().cpu().numpy() - o_ref) <= tol)
+    assert np.all(o[:, 2:4].float().cpu().numpy() == 0.0)   # heads of the zero V head
+    assert np.all(np.abs(lse.cpu().numpy() - lse_ref) <= 1e-3)

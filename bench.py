@@ -573,7 +573,10 @@ def run_ours(args):
                 ev[2].record(stream)
     else:
         lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
-        ws = torch.empty(max(api.bwd_workspace_bytes(q, k), 1), dtype=torch.uint8, device=dev)
+        ws = api.bwd_workspace(q, k, w.causal)
+        # the stored-dS backward (dQ as one GEMM over the dS the dK launch wrote) when the workspace holds it
+        ds_path = ws.numel() >= api.bwd_workspace_bytes(q, k, w.causal) > api.bwd_workspace_bytes(q, k)
+        dq_bit = 16 if ds_path else 4
         # the user's path: one forward call and one backward call per step (the
         # backward's dV, dK and dQ kernels overlap their neighbours' tails)
         names = ("fwd", "bwd")
@@ -589,13 +592,14 @@ def run_ours(args):
                 ev[2].record(stream)
 
         # per-kernel durations (a second timed pass, one launch per call:
-        # preprocess | dV | dK | dQ are ffpa_bwd_stages bits 0, 1, 3, 2)
+        # preprocess | dV | dK | dQ are ffpa_bwd_stages bits 0, 1, 3, then 2, or 4
+        # for the dQ GEMM over the dS that the dK launch just stored)
         kernel_names = ("fwd", "preprocess", "dv", "dk", "dq")
 
         def kernel_step(ev):
             ev[0].record(stream)
             api.fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
-            for i, bit in enumerate((1, 2, 8, 4)):
+            for i, bit in enumerate((1, 2, 8, dq_bit)):
                 ev[i + 1].record(stream)
                 api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=bit)
             ev[5].record(stream)
@@ -653,7 +657,7 @@ def run_ours(args):
     if w.varlen:
         algo = {"fwd": 2 * gemm, "bwd": 8 * gemm}  # bwd: preprocess + dV (2) + dK (3) + dQ (3) units
     else:
-        algo = {"fwd": 2 * gemm, "dv": 2 * gemm, "dk": 3 * gemm, "dq": 3 * gemm}
+        algo = {"fwd": 2 * gemm, "dv": 2 * gemm, "dk": 3 * gemm, "dq": (1 if ds_path else 3) * gemm}
     dom = max(algo, key=lambda n: per_ms[n])
     achieved = algo[dom] / (per_ms[dom] / 1e3) / 1e12
     peak = pk["bf16_tflops_sustained"]
@@ -684,6 +688,8 @@ def run_ours(args):
             "bwd": {"tflops": world * f_bwd / (bwd_ms / 1e3) / 1e12, "ms": bwd_ms,
                     "pct_peak_burst": 100 * f_bwd / (bwd_ms / 1e3) / 1e12 / pk["bf16_tflops"]},
             "kernel_ms": per_ms,
+            "dq_path": ("one GEMM over the dS stored by the dK launch" if not w.varlen and ds_path
+                        else "S and dP recomputed"),
             "kernel_ms_note": "each kernel launched alone (one call per stage), after the timed region"
             if not w.varlen else "fwd and bwd calls of the timed region",
             "pct_peak_burst": 100 * value / world / pk["bf16_tflops"],

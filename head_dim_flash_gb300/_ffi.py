@@ -25,6 +25,7 @@ EXPORTS = (
     "ffpa_bwd_strided",
     "ffpa_decode_workspace_bytes",
     "ffpa_decode_fwd",
+    "ffpa_bwd_workspace_bytes_ds",
     "ffpa_fp8_workspace_bytes",
     "ffpa_fp8_workspace_layout",
     "ffpa_fp8_quantize",
@@ -67,6 +68,8 @@ def _declare(lib):
     lib.ffpa_bwd_strided.argtypes = [_i, View, View, View, View, _p, View, View, View, View, _p, _sz, _i, _i, _i, _i,
                                      _i, _i, _i, _f, _p]
     lib.ffpa_bwd_strided.restype = _i
+    lib.ffpa_bwd_workspace_bytes_ds.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i]
+    lib.ffpa_bwd_workspace_bytes_ds.restype = _sz
     lib.ffpa_fp8_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i]
     lib.ffpa_fp8_workspace_bytes.restype = _sz
     lib.ffpa_fp8_workspace_layout.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]
@@ -156,6 +159,10 @@ def ffpa_fwd_strided(*args):
 
 def ffpa_bwd_strided(*args):
     return load().ffpa_bwd_strided(*args)
+
+
+def ffpa_bwd_workspace_bytes_ds(*args):
+    return load().ffpa_bwd_workspace_bytes_ds(*args)
 
 
 def ffpa_fp8_workspace_bytes(*args):

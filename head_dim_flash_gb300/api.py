@@ -220,24 +220,45 @@ def fwd_fp8_quantized(workspace, shape_q, shape_k, dtype, causal: bool = False, 
     return o, l
 
 
-def bwd_workspace_bytes(q, k) -> int:
+def bwd_workspace_bytes(q, k, causal: bool | None = None) -> int:
+    """Backward workspace bytes: the row statistics only (causal None), or with
+    room for the stored dS where that path applies (ffpa_bwd_workspace_bytes_ds)."""
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape
-    return int(_ffi.ffpa_bwd_workspace_bytes(_dt(q), B, Hq, Hkv, Nq, Nkv, D))
+    if causal is None:
+        return int(_ffi.ffpa_bwd_workspace_bytes(_dt(q), B, Hq, Hkv, Nq, Nkv, D))
+    return int(_ffi.ffpa_bwd_workspace_bytes_ds(_dt(q), B, Hq, Hkv, Nq, Nkv, D, int(bool(causal))))
+
+
+DS_WORKSPACE_FRACTION = 0.25  # largest share of free device memory bwd() spends on the stored dS
+
+
+def bwd_workspace(q, k, causal: bool):
+    """A backward workspace: with the stored-dS room when it applies and takes at
+    most DS_WORKSPACE_FRACTION of the free device memory, else the small one."""
+    small = bwd_workspace_bytes(q, k)
+    big = bwd_workspace_bytes(q, k, causal)
+    n = small
+    if big > small:
+        free, _ = torch.cuda.mem_get_info(q.device)
+        if big <= DS_WORKSPACE_FRACTION * free:
+            n = big
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
 
 
 def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None,
         dq=None, dk=None, dv=None, stages: int = 15):
     """Dense backward through ffpa_bwd_strided (views, no copy), or ffpa_bwd_stages
-    for a subset of its launches (bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK;
-    contiguous tensors). Returns (dq, dk, dv)."""
+    for a subset of its launches (bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK,
+    bit 4 dQ from the dS a dK stage stored; contiguous tensors). Without a
+    workspace, one with room for the stored dS is allocated where that path
+    applies (bwd_workspace). Returns (dq, dk, dv)."""
     q, k, v, o, dout = _dense(q, k, v, o, dout)
     lse = lse.contiguous()
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape
-    ws_bytes = bwd_workspace_bytes(q, k)
     if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+        workspace = bwd_workspace(q, k, causal)
     dq = _out_like(q) if dq is None else dq
     dk = _out_like(k) if dk is None else dk
     dv = _out_like(v) if dv is None else dv

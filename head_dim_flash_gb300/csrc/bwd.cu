@@ -104,16 +104,36 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
     // one before, so it fills the SMs that the previous one's last wave leaves
     // idle (the first waits for the preprocess as usual; the later ones start
     // only once all of its CTAs have started, hence after the preprocess)
+    // dQ from stored dS: the dK launch also writes dS^T into a.ds, then a plain
+    // GEMM forms dQ (dense non-causal, D = 256 / 512, with the buffer given);
+    // stage bit 4 runs that GEMM alone on a buffer an earlier dK launch filled
+    const bool use_ds = a.ds != nullptr && !q_empty && !kv_empty && dsq_supported(pb);
     x.pdl = 0;
     if (!kv_empty && (a.stages & 2u)) {
         if ((e = launch_xchg(XOP_DV, x, st)) != cudaSuccess) return e;
         x.pdl = 1;
     }
     if (!kv_empty && (a.stages & 8u)) {
-        if ((e = launch_xchg(XOP_DK, x, st)) != cudaSuccess) return e;
+        XArgs xk = x;
+        xk.store_ds = use_ds ? 1 : 0;
+        xk.ds = a.ds;
+        if ((e = launch_xchg(XOP_DK, xk, st)) != cudaSuccess) return e;
         x.pdl = 1;
     }
-    if (!q_empty && (a.stages & 4u) && (e = launch_xchg(XOP_DQ, x, st)) != cudaSuccess) return e;
+    const bool dq_from_ds = use_ds && ((a.stages & 16u) || ((a.stages & 4u) && (a.stages & 8u)));
+    if (!q_empty && dq_from_ds) {
+        DsqArgs d{};
+        d.pb = pb;
+        d.bf16 = BF16;
+        d.ds = a.ds;
+        d.k = a.k;
+        d.dq = a.dq;
+        d.ctl = a.ctl;
+        // a plain launch: the GEMM reads what the dK launch wrote
+        if ((e = launch_dsq(d, st)) != cudaSuccess) return e;
+    } else if (!q_empty && (a.stages & 4u) && (e = launch_xchg(XOP_DQ, x, st)) != cudaSuccess) {
+        return e;
+    }
     return cudaSuccess;
 }
 

@@ -1,0 +1,253 @@
+// dQ from the stored dS: dQ = scale * dS K, a plain GEMM per (batch, query
+// head), for dense non-causal problems whose dS the dK kernel wrote to the
+// backward workspace (FFPA docs, "CuTe-DSL Backend" page, "Blackwell status":
+// the backward as a preprocess plus separate gradient launches; here the dQ
+// launch reuses the dS tiles of the dK launch instead of recomputing S and
+// dP, which turns 3 GEMM units into 1).
+//
+// The dK kernel stores dS^T, [B, Hq, Nkv, ldq] (keys x queries, queries
+// contiguous), tile by tile. A CTA pair owns 256 query rows (128 per CTA, in
+// its TMEM lanes) and the whole head dim (D <= 512 fp32 columns of TMEM), and
+// walks the keys in blocks of 64:
+//   A = dS for my 128 queries x 64 keys, read from dS^T as an MN-major
+//       operand (two 64-query boxes of 64 key rows x 128 bytes);
+//   B = K for 64 keys x my 128 columns of each 256-column half of D, also
+//       MN-major (the forward's value-operand form);
+//   acc[:, 256 j .. 256 j + 255] += A B_j as M=256, N=256 pair MMAs.
+// Warp 0 lanes 0 / 1 load A / B with TMA into a 4-stage ring, warp 1 of the
+// even rank issues the MMAs, warps 2..5 scale and store dQ rows.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_common.cuh"
+
+namespace ffpa {
+namespace {
+
+constexpr int kQThreads = 192;
+constexpr int kQStages = 4;
+
+enum QSite : uint32_t { QS_PROD = 112, QS_RING, QS_ACC, QS_DRAIN };
+
+struct __align__(1024) QStatic {
+    uint64_t full[kQStages], empty[kQStages], acc;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(QStatic) == 1024, "static shared block must be exactly 1 KiB");
+
+struct QGeo {
+    int nj;           // N = 256 pair MMAs across the head dim (D / 256)
+    int stage_bytes;  // per CTA: A (16 KiB) + B (nj x 16 KiB)
+    int n_kb;         // key blocks of 64
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kQThreads, 1)
+    dsq_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB, const DsqArgs a,
+               const QGeo gm)
+{
+    const Problem& pb = a.pb;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int rh = rank & 1;
+    const bool leader = rh == 0;
+    const int G = pb.Hq / pb.Hkv;
+    const int b = blockIdx.z / pb.Hq, h = blockIdx.z % pb.Hq, hk = h / G;
+    const int qc = blockIdx.y * 256 + 128 * rh;  // my first query row
+    const int tcols = gm.nj * 256;
+
+    __shared__ QStatic sh;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // uniform over the cluster: report, do not run misaligned
+        if (threadIdx.x == 0) atomicCAS(a.ctl.status, 0u, 5u | (0xffu << 8));
+        return;
+    }
+    const int warp = threadIdx.x / 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kQStages; ++i) {
+            mbar_init(&sh.full[i], 1);
+            mbar_init(&sh.empty[i], 1);
+        }
+        mbar_init(&sh.acc, 1);
+        sh.abort_flag = 0;
+        // the even rank's full barriers count both CTAs' bytes
+        if (leader)
+            for (int i = 0; i < kQStages; ++i) mbar_arrive_expect_tx(&sh.full[i], 2 * gm.stage_bytes);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&sh.tmem_base, tcols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    volatile int* abort_flag = &sh.abort_flag;
+    uint32_t* status = a.ctl.status;
+    const uint64_t lim = a.ctl.limit_ns;
+    const int lead_rank = rank & ~1;
+    const uint16_t pair_mask = static_cast<uint16_t>(3u << lead_rank);
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producers
+        const int lane = static_cast<int>(lane_id());
+        if (lane < 2) {
+            if (lane == 0) {
+                prefetch_tmap(&tA);
+                prefetch_tmap(&tB);
+            }
+            RingPos rp;
+            int issued = 0;
+            for (int kb = 0; kb < gm.n_kb; ++kb) {
+                const bool got = mbar_wait(&sh.empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, QS_PROD);
+                if (!__all_sync(0x3u, got)) break;
+                uint8_t* st = smem + rp.slot * gm.stage_bytes;
+                const uint32_t fb = mapa_shared(smem_u32(&sh.full[rp.slot]), lead_rank);
+                if (lane == 0) {
+                    // A: dS^T rows = keys [64 kb, +64), my 128 queries as two 64-query boxes
+                    tma_load_4d_pair(st, &tA, fb, qc, kb * 64, h, b);
+                    tma_load_4d_pair(st + 8192, &tA, fb, qc + 64, kb * 64, h, b);
+                } else {
+                    // B: K rows = keys [64 kb, +64), my 128 columns of each 256-column half
+                    for (int j = 0; j < gm.nj; ++j)
+                        tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, kb * 64, (j * 256 + rh * 128) / 64, hk, b);
+                }
+                rp.advance(kQStages);
+                ++issued;
+            }
+            // no loads in flight when the CTA leaves
+            if (lane == 0) {
+                RingPos dp = rp;
+                for (int i = 0; i < min(issued, kQStages); ++i) {
+                    dp.retreat(kQStages);
+                    int dummy = 0;
+                    if (!mbar_wait(&sh.empty[dp.slot], dp.phase, &dummy, status, lim, QS_DRAIN, false)) break;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer (pair)
+        if (leader && elect_one()) {
+            const uint32_t idesc = idesc_f16(256, 256, BF16, true, true);
+            RingPos rp;
+            for (int kb = 0; kb < gm.n_kb; ++kb) {
+                if (!mbar_wait_cluster(&sh.full[rp.slot], rp.phase, abort_flag, status, lim, QS_RING)) break;
+                mbar_arrive_expect_tx(&sh.full[rp.slot], 2 * gm.stage_bytes);  // arm the slot's next fill
+                tc_fence_after();
+                const uint8_t* st = smem + rp.slot * gm.stage_bytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    // 16 keys per MMA: 16 rows x 128 bytes into both operands; 64-element
+                    // chunks along M (A) and N (B) are 64 key rows x 128 bytes apart
+                    const uint64_t ad = sdesc_sw128(smem_u32(st + kk * 2048), 8192, 1024);
+                    for (int j = 0; j < gm.nj; ++j) {
+                        const uint64_t bd = sdesc_sw128(smem_u32(st + 16384 * (1 + j) + kk * 2048), 8192, 1024);
+                        umma_f16_pair(tmem + j * 256, ad, bd, idesc, (kb | kk) != 0);
+                    }
+                }
+                umma_commit_pair_multicast(&sh.empty[rp.slot], pair_mask);
+                rp.advance(kQStages);
+            }
+            umma_commit_pair_multicast(&sh.acc, pair_mask);
+        }
+    } else {
+        // ------------------------------------------------------ epilogue (warps 2..5)
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + static_cast<int>(lane_id());
+        const int q = qc + r;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&sh.acc, 0, abort_flag, status, lim, QS_ACC));
+        tc_fence_after();
+        if (ok) {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(a.dq) + static_cast<size_t>(b) * pb.vdq.sb +
+                            static_cast<size_t>(h) * pb.vdq.sh + static_cast<size_t>(q) * pb.vdq.sn;
+            for (int cc = 0; cc < pb.D; cc += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + cc, v);
+                tmem_ld_wait(v);
+                if (q < pb.Nq) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * pb.scale, __uint_as_float(v[2 * e + 1]) * pb.scale);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                }
+            }
+        }
+    }
+
+    // -------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, tcols);
+    }
+}
+
+}  // namespace
+
+bool dsq_supported(const Problem& pb)
+{
+    return !pb.varlen && !pb.causal && (pb.D == 256 || pb.D == 512) && pb.Nq > 0 && pb.Nkv > 0;
+}
+
+size_t dsq_ds_bytes(const Problem& pb)
+{
+    const size_t ldq = (static_cast<size_t>(pb.Nq) + 7) & ~static_cast<size_t>(7);
+    return static_cast<size_t>(pb.B) * pb.Hq * pb.Nkv * ldq * 2;
+}
+
+bool make_ds_map(CUtensorMap* m, const void* ds, const Problem& pb, bool bf16, int box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t ldq = (static_cast<cuuint64_t>(pb.Nq) + 7) & ~static_cast<cuuint64_t>(7);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(pb.Nq), static_cast<cuuint64_t>(pb.Nkv),
+                                static_cast<cuuint64_t>(pb.Hq), static_cast<cuuint64_t>(pb.B)};
+    const cuuint64_t strides[3] = {ldq * 2, static_cast<cuuint64_t>(pb.Nkv) * ldq * 2,
+                                   static_cast<cuuint64_t>(pb.Hq) * pb.Nkv * ldq * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ds),
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s)
+{
+    const Problem& pb = a.pb;
+    if (!dsq_supported(pb)) return cudaErrorInvalidConfiguration;
+    CUtensorMap tA, tB;
+    if (!make_ds_map(&tA, a.ds, pb, a.bf16, 64) || !make_slab_map(&tB, a.k, pb, true, a.bf16, 64, 2, pb.vk))
+        return cudaErrorInvalidValue;
+    QGeo gm{};
+    gm.nj = pb.D / 256;
+    gm.stage_bytes = 16384 * (1 + gm.nj);
+    gm.n_kb = (pb.Nkv + 63) / 64;
+    const int smem = kQStages * gm.stage_bytes;
+    const dim3 grid(2, (pb.Nq + 255) / 256, pb.B * pb.Hq);
+    if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
+    auto kern = a.bf16 ? dsq_kernel<true> : dsq_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kQThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tA, tB, a, gm);
+}
+
+}  // namespace ffpa

@@ -55,7 +55,8 @@ struct BwdArgs {
     void *dq, *dk, *dv;
     float* delta;      // workspace [rows] fp32: rowsum(dO * O)
     float* lse_log2;   // workspace [rows] fp32: LSE * log2(e), +inf for empty rows
-    unsigned stages;   // bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK
+    unsigned stages;   // bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK, bit 4 dQ from the stored dS
+    void* ds;          // dS^T buffer of dsq_ds_bytes() bytes, or null (dQ recomputes S and dP)
     DeviceCtl ctl;
 };
 
@@ -81,7 +82,25 @@ struct XArgs {
     const void* v8t;
     int ldv;
     const float *f8_sq, *f8_sk, *f8_sv;
+    // dK: also store every dS^T tile to ds ([B, Hq, Nkv, ldq], ldq = Nq rounded up to 8)
+    int store_ds;
+    void* ds;
 };
+
+// dQ = scale * dS K from the dS^T the dK kernel stored (dense, non-causal,
+// D = 256 or 512); dsq_ds_bytes is the size of that dS^T buffer.
+struct DsqArgs {
+    Problem pb;
+    int bf16;
+    const void* ds;
+    const void* k;
+    void* dq;
+    DeviceCtl ctl;
+};
+bool dsq_supported(const Problem& pb);
+size_t dsq_ds_bytes(const Problem& pb);
+bool make_ds_map(CUtensorMap* m, const void* ds, const Problem& pb, bool bf16, int box_rows);
+cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s);
 
 // Workspace of the FP8 forward (byte offsets, 256-byte aligned regions).
 struct Fp8Layout {

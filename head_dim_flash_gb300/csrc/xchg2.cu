@@ -86,6 +86,7 @@ struct __align__(1024) StaticSmem {
     uint32_t tmem_base;
     int abort_flag;
     uint32_t relay_sink[4];  // (even rank) target of the odd rank's 4-byte relay stores
+    uint64_t stored[2];      // (dK storing dS) the store of the own Z buffer has read it
 };
 static_assert(sizeof(StaticSmem) == 1024, "static shared block must be exactly 1 KiB");
 
@@ -109,7 +110,8 @@ template <int OP, bool BF16, bool VARLEN, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     pair_kernel(const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tA2,
                 const __grid_constant__ CUtensorMap tB1, const __grid_constant__ CUtensorMap tB2,
-                const __grid_constant__ CUtensorMap tW, const XArgs a, const PGeo gm)
+                const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tS, const XArgs a,
+                const PGeo gm)
 {
     // the next GEMM kernel of a backward may take SMs as this grid's last CTAs start
     pdl_trigger();
@@ -225,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         mbar_init(&sh.half, 256);
+        mbar_init(&sh.stored[0], 1);
+        mbar_init(&sh.stored[1], 1);
         mbar_init(&sh.lsum, 1);
         mbar_init(&sh.drain, 1);
         sh.abort_flag = 0;
@@ -630,11 +634,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Ships the own Z tile of every step, once all 256 elementwise threads
         // wrote it, into the CTA of every other pair that holds my rows, as one
         // bulk copy each, once that pair's value products consumed the previous
-        // copy in the target buffer.
-        if (C > 1 && elect_one()) {
+        // copy in the target buffer. The dK kernel that stores dS also writes the
+        // tile (dS^T: my 128 key rows x the tile's 128 queries) to the dS buffer
+        // with two TMA stores and reports when they have read it.
+        const bool store = OP == XOP_DK && a.store_ds != 0;
+        if ((C > 1 || store) && elect_one()) {
+            if (store) prefetch_tmap(&tS);
             for (int s = 0; s < n_steps; ++s) {
                 const int bb = zbuf(s);
                 bool ok = mbar_wait(&sh.z_full[bb], zpar(s), abort_flag, status, lim, PS_COPY);
+                if (ok && store) {
+                    const int t = s * C + c;
+                    if (t < n_ct) {
+                        const uint8_t* zown = zslot(C - 1, bb);
+                        tma_store_4d(&tS, zown, col_row0(t), row_co(r0), col_head(t), bco);
+                        tma_store_4d(&tS, zown + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                    }
+                    mbar_arrive(&sh.stored[bb]);
+                }
                 for (int k = 1; k < C && ok; ++k) {
                     const int p = (c + k) % C;
                     if (s >= nbuf)
@@ -645,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
             }
+            if (store) bulk_wait_all();  // the dS stores are complete before the CTA leaves
         }
     } else {
         // ------------------------------------------------------ elementwise
@@ -933,6 +953,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool got = mbar_wait(&sh.acc[sp & 1], accpar(sp), abort_flag, status, lim, PS_ACC);
                 for (int p = 0; p < C && got; ++p)
                     if (p != c) got = mbar_wait_cluster(&sh.slot_free[p][bb], zpar(sp), abort_flag, status, lim, PS_SLOT);
+                // dK storing dS: the store of step sp has read the buffer
+                if (got && OP == XOP_DK && a.store_ds)
+                    got = mbar_wait(&sh.stored[bb], zpar(sp), abort_flag, status, lim, PS_COPY);
                 if (!warp_ok(got)) {
                     ok = false;
                     break;
@@ -1075,7 +1098,7 @@ cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const PGeo& gm, i
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], a, gm);
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a, gm);
 }
 
 template <int OP>
@@ -1137,7 +1160,7 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const Src sdo = q_empty ? Src{a.k, pb.vk, true} : (a.dO ? Src{a.dO, pb.vdo, false} : sq);
     const Src sk = kv_empty ? Src{a.q, pb.vq, false} : Src{a.k, pb.vk, true};
     const Src sv = kv_empty ? Src{a.q, pb.vq, false} : Src{a.v, pb.vv, true};
-    CUtensorMap m[5];
+    CUtensorMap m[6];
     bool okm = true;
     auto row = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 128, 2, x.v); };
     auto col = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 64, 4, x.v); };
@@ -1151,6 +1174,7 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
               make_vt_map(&m[4], a.v8t, pb.B, pb.Hkv, pb.D, pb.Nkv, a.ldv, 128);
         m[1] = m[0];
         m[3] = m[2];
+        m[5] = m[0];
         if (!okm) return cudaErrorInvalidValue;
         const int n_rt8 = (pb.Nq + 255) / 256;
         const int bz8 = pb.B * pb.Hq;
@@ -1176,6 +1200,9 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
         n_rows = pb.Nkv; bz = pb.B * pb.Hkv;
         break;
     }
+    // dK storing dS: the dS^T buffer as stored tiles (64 queries x 128 key rows)
+    if (op == XOP_DK && a.store_ds) okm = okm && make_ds_map(&m[5], a.ds, pb, a.bf16, 128);
+    else m[5] = m[0];
     if (!okm) return cudaErrorInvalidValue;
     const int n_rt = (n_rows + 255) / 256;
     if (n_rt == 0 || bz == 0) return cudaSuccess;

@@ -249,7 +249,7 @@ ffpa_status run_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, 
         a.ds = static_cast<char*>(workspace) + need;
     if ((a.stages & 16u) && a.ds == nullptr)
         return fail(FFPA_ERR_INVALID_VALUE, "stage bit 4 (dQ from stored dS) needs the larger workspace of "
-                                            "ffpa_bwd_workspace_bytes_ds on a dense non-causal D = 256 / 512 problem");
+                                            "ffpa_bwd_workspace_bytes_ds on a dense D = 256 / 512 problem");
     return launch_result(ffpa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)), "backward launch");
 }
 

@@ -105,9 +105,11 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
     // idle (the first waits for the preprocess as usual; the later ones start
     // only once all of its CTAs have started, hence after the preprocess)
     // dQ from stored dS: the dK launch also writes dS^T into a.ds, then a plain
-    // GEMM forms dQ (dense non-causal, D = 256 / 512, with the buffer given);
+    // GEMM forms dQ (dense, D = 256 / 512, with the buffer given);
     // stage bit 4 runs that GEMM alone on a buffer an earlier dK launch filled
-    const bool use_ds = a.ds != nullptr && !q_empty && !kv_empty && dsq_supported(pb);
+    // (only the CTA-pair dK kernel stores dS)
+    const bool use_ds = a.ds != nullptr && !q_empty && !kv_empty && dsq_supported(pb) && xchg_uses_pair(pb);
+    if ((a.stages & 16u) && !use_ds) return cudaErrorInvalidConfiguration;  // no stored dS to read
     x.pdl = 0;
     if (!kv_empty && (a.stages & 2u)) {
         if ((e = launch_xchg(XOP_DV, x, st)) != cudaSuccess) return e;

@@ -1,5 +1,5 @@
 // dQ from the stored dS: dQ = scale * dS K, a plain GEMM per (batch, query
-// head), for dense non-causal problems whose dS the dK kernel wrote to the
+// head), for dense problems whose dS the dK kernel wrote to the
 // backward workspace (FFPA docs, "CuTe-DSL Backend" page, "Blackwell status":
 // the backward as a preprocess plus separate gradient launches; here the dQ
 // launch reuses the dS tiles of the dK launch instead of recomputing S and
@@ -8,7 +8,9 @@
 // The dK kernel stores dS^T, [B, Hq, Nkv, ldq] (keys x queries, queries
 // contiguous), tile by tile. A CTA pair owns 256 query rows (128 per CTA, in
 // its TMEM lanes) and the whole head dim (D <= 512 fp32 columns of TMEM), and
-// walks the keys in blocks of 64:
+// walks the keys in blocks of 64, up to the last key any of its rows may see
+// under the bottom-right causal mask (the dK kernel wrote every block below
+// that, masked entries as zeros; causal grids take the longest tiles first):
 //   A = dS for my 128 queries x 64 keys, read from dS^T as an MN-major
 //       operand (two 64-query boxes of 64 key rows x 128 bytes);
 //   B = K for 64 keys x my 128 columns of each 256-column half of D, also
@@ -38,7 +40,6 @@ static_assert(sizeof(QStatic) == 1024, "static shared block must be exactly 1 Ki
 struct QGeo {
     int nj;           // N = 256 pair MMAs across the head dim (D / 256)
     int stage_bytes;  // per CTA: A (16 KiB) + B (nj x 16 KiB)
-    int n_kb;         // key blocks of 64
 };
 
 template <bool BF16>
@@ -52,7 +53,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const bool leader = rh == 0;
     const int G = pb.Hq / pb.Hkv;
     const int b = blockIdx.z / pb.Hq, h = blockIdx.z % pb.Hq, hk = h / G;
-    const int qc = blockIdx.y * 256 + 128 * rh;  // my first query row
+    const int tile = pb.causal ? static_cast<int>(gridDim.y - 1 - blockIdx.y) : static_cast<int>(blockIdx.y);
+    const int q0 = tile * 256;
+    const int qc = q0 + 128 * rh;  // my first query row
+    const int key_end = pb.causal ? min(pb.Nkv, q0 + 255 + (pb.Nkv - pb.Nq) + 1) : pb.Nkv;
+    const int n_kb = key_end > 0 ? (key_end + 63) / 64 : 0;  // the same for both CTAs of the pair
     const int tcols = gm.nj * 256;
 
     __shared__ QStatic sh;
@@ -98,7 +103,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             }
             RingPos rp;
             int issued = 0;
-            for (int kb = 0; kb < gm.n_kb; ++kb) {
+            for (int kb = 0; kb < n_kb; ++kb) {
                 const bool got = mbar_wait(&sh.empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, QS_PROD);
                 if (!__all_sync(0x3u, got)) break;
                 uint8_t* st = smem + rp.slot * gm.stage_bytes;
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (leader && elect_one()) {
             const uint32_t idesc = idesc_f16(256, 256, BF16, true, true);
             RingPos rp;
-            for (int kb = 0; kb < gm.n_kb; ++kb) {
+            for (int kb = 0; kb < n_kb; ++kb) {
                 if (!mbar_wait_cluster(&sh.full[rp.slot], rp.phase, abort_flag, status, lim, QS_RING)) break;
                 mbar_arrive_expect_tx(&sh.full[rp.slot], 2 * gm.stage_bytes);  // arm the slot's next fill
                 tc_fence_after();
@@ -159,17 +164,24 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&sh.acc, 0, abort_flag, status, lim, QS_ACC));
         tc_fence_after();
         if (ok) {
+            // no key for any row of the pair: dQ = 0 (the accumulator was never written)
+            const float mul = n_kb > 0 ? pb.scale : 0.f;
             uint16_t* dst = reinterpret_cast<uint16_t*>(a.dq) + static_cast<size_t>(b) * pb.vdq.sb +
                             static_cast<size_t>(h) * pb.vdq.sh + static_cast<size_t>(q) * pb.vdq.sn;
             for (int cc = 0; cc < pb.D; cc += 32) {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_off + cc, v);
-                tmem_ld_wait(v);
+                if (n_kb > 0) {
+                    tmem_ld32(tmem + lane_off + cc, v);
+                    tmem_ld_wait(v);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
                 if (q < pb.Nq) {
                     uint32_t w[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * pb.scale, __uint_as_float(v[2 * e + 1]) * pb.scale);
+                        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
                     uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
@@ -193,7 +205,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 bool dsq_supported(const Problem& pb)
 {
-    return !pb.varlen && !pb.causal && (pb.D == 256 || pb.D == 512) && pb.Nq > 0 && pb.Nkv > 0;
+    return !pb.varlen && (pb.D == 256 || pb.D == 512) && pb.Nq > 0 && pb.Nkv > 0;
 }
 
 size_t dsq_ds_bytes(const Problem& pb)
@@ -228,7 +240,6 @@ cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s)
     QGeo gm{};
     gm.nj = pb.D / 256;
     gm.stage_bytes = 16384 * (1 + gm.nj);
-    gm.n_kb = (pb.Nkv + 63) / 64;
     const int smem = kQStages * gm.stage_bytes;
     const dim3 grid(2, (pb.Nq + 255) / 256, pb.B * pb.Hq);
     if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;

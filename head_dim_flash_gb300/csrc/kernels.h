@@ -87,8 +87,8 @@ struct XArgs {
     void* ds;
 };
 
-// dQ = scale * dS K from the dS^T the dK kernel stored (dense, non-causal,
-// D = 256 or 512); dsq_ds_bytes is the size of that dS^T buffer.
+// dQ = scale * dS K from the dS^T the dK kernel stored (dense, D = 256 or
+// 512); dsq_ds_bytes is the size of that dS^T buffer.
 struct DsqArgs {
     Problem pb;
     int bf16;
@@ -117,6 +117,7 @@ cudaError_t launch_fwd_fp8(const FwdArgs& a, void* workspace, cudaStream_t s, bo
 // one-CTA-per-slab form (clusters of C CTAs, every other head dim);
 // FFPA_KERNEL=pair|single in the environment forces one of them.
 cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s);
+bool xchg_uses_pair(const Problem& pb);  // the family launch_xchg picks for this problem
 cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s);
 cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s);
 

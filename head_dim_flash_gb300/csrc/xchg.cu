@@ -877,7 +877,7 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
     }
 }
 
-cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
+bool xchg_uses_pair(const Problem& pb)
 {
     // CTA pairs where the head dim splits into 256-column slabs without padding
     // waste and the cluster stays within 6 CTAs (measured faster there on
@@ -885,8 +885,12 @@ cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
     const char* e = std::getenv("FFPA_KERNEL");
     const int forced = e == nullptr ? 0 : std::strcmp(e, "single") == 0 ? 1 : (std::strcmp(e, "pair") == 0 ? 2 : 0);
     // (head dims that are not a multiple of 64 only run in the one-CTA form)
-    const bool pair = a.pb.D % 64 == 0 && (forced ? forced == 2 : (a.pb.D % 128 == 0 && a.pb.D <= 768));
-    return pair ? launch_pair(op, a, s) : launch_single(op, a, s);
+    return pb.D % 64 == 0 && (forced ? forced == 2 : (pb.D % 128 == 0 && pb.D <= 768));
+}
+
+cudaError_t launch_xchg(int op, const XArgs& a, cudaStream_t s)
+{
+    return xchg_uses_pair(a.pb) ? launch_pair(op, a, s) : launch_single(op, a, s);
 }
 
 }  // namespace ffpa

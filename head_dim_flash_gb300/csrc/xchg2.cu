@@ -172,7 +172,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             n_ct = kmax < 0 ? 0 : min(n_ct, kmax / 128 + 1);
         }
     } else {
-        if (pb.causal) m_start = max(0, R0 - off) / 128;
+        if (pb.causal) {
+            m_start = max(0, R0 - off) / 128;
+            // dK storing dS: start at an even query tile, so that every 256-query
+            // tile of the dQ GEMM finds all of its dS blocks written (the extra
+            // tile is fully masked: stored zeros)
+            if (OP == XOP_DK && a.store_ds) m_start &= ~1;
+        }
         n_mt = max(0, (lq + 127) / 128 - m_start);
         n_ct = G * n_mt;
     }

@@ -172,8 +172,8 @@ FFPA_API ffpa_status ffpa_fwd_fp8_quantized(ffpa_dtype dt, ffpa_view o, float* l
 /* Workspace bytes ffpa_bwd needs for this problem (fp32 row statistics). */
 FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 /*
- * Workspace bytes that also hold dS^T for the stored-dS backward: on a dense,
- * non-causal problem with D = 256 or 512, ffpa_bwd / ffpa_bwd_strided given a
+ * Workspace bytes that also hold dS^T for the stored-dS backward: on a dense
+ * problem with D = 256 or 512, ffpa_bwd / ffpa_bwd_strided given a
  * workspace at least this large have the dK launch also store every dS tile
  * (bf16/fp16, the same rounded values it multiplies) and form dQ = scale dS K
  * with one GEMM, instead of recomputing S and dP in a dQ launch (3 GEMM units
@@ -217,8 +217,8 @@ FFPA_API ffpa_status ffpa_bwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, f
  * workspace the preprocess stage wrote, so a caller that splits them issues
  * bit 0 first (the FFPA docs' CuTe-DSL page, "Blackwell status", describes the
  * same four launches). ffpa_bwd(...) == ffpa_bwd_stages(..., 15).
- * With the workspace of ffpa_bwd_workspace_bytes_ds (dense, non-causal, D =
- * 256 / 512), a dK stage also stores dS and a dQ stage in the same call is the
+ * With the workspace of ffpa_bwd_workspace_bytes_ds (dense, D = 256 / 512),
+ * a dK stage also stores dS and a dQ stage in the same call is the
  * dS K GEMM; bit 4 runs that GEMM alone on the dS an earlier dK stage stored
  * in this workspace for the same inputs (bit 2 alone recomputes S and dP).
  * Arguments otherwise as ffpa_bwd.

@@ -1,10 +1,10 @@
 """GPU parity of the stored-dS backward: the dK launch also writes dS^T to the
-workspace and dQ = scale dS K is one GEMM (dense, non-causal, D = 256 / 512).
+workspace and dQ = scale dS K is one GEMM (dense, D = 256 / 512, causal or not).
 
 Every case runs the backward twice on the same inputs, with the small
 workspace (dQ recomputes S and dP) and with the stored-dS workspace, and
-checks both against the fp64 oracle with the usual gradient tolerance; dK and
-dV must be bit-identical between the two (the same kernels compute them).
+checks both against the fp64 oracle with the usual gradient tolerance; dV (and
+dK when non-causal) must be bit-identical between the two.
 """
 import math
 
@@ -30,23 +30,27 @@ def _lib():
     oracle.build()
 
 
-def run_both(B, Hq, Hkv, Nq, Nkv, D, dtype=torch.bfloat16, seed=0):
+def run_both(B, Hq, Hkv, Nq, Nkv, D, dtype=torch.bfloat16, seed=0, causal=False):
     inp = workloads.random_dense(B, Hq, Hkv, Nq, Nkv, D, dtype, seed=seed)
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dO"))
     scale = 1.0 / math.sqrt(D)
-    o, lse = api.fwd(q, k, v, False, scale)
+    o, lse = api.fwd(q, k, v, causal, scale)
     small = torch.empty(api.bwd_workspace_bytes(q, k), dtype=torch.uint8, device="cuda")
-    big_n = api.bwd_workspace_bytes(q, k, False)
+    big_n = api.bwd_workspace_bytes(q, k, causal)
     assert big_n > small.numel(), "the stored-dS path applies to this problem"
     big = torch.empty(big_n, dtype=torch.uint8, device="cuda")
-    g_small = api.bwd(q, k, v, o, lse, do, False, scale, workspace=small)
-    g_big = api.bwd(q, k, v, o, lse, do, False, scale, workspace=big)
+    g_small = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=small)
+    g_big = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=big)
     api.get_status()
-    ref = oracle.attention_bwd(inp["q"], inp["k"], inp["v"], inp["dO"], False, scale)
+    ref = oracle.attention_bwd(inp["q"], inp["k"], inp["v"], inp["dO"], causal, scale)
     for gs in (g_small, g_big):
         for name, got, r in zip(("dQ", "dK", "dV"), gs, ref):
             check_grad(got, r, name)
-    assert torch.equal(g_small[1], g_big[1]) and torch.equal(g_small[2], g_big[2])
+    # dV is the same kernel either way; dK too, except that causal storing starts
+    # at an even query tile (an extra all-masked tile shifts its summation order)
+    assert torch.equal(g_small[2], g_big[2])
+    if not causal:
+        assert torch.equal(g_small[1], g_big[1])
     return inp, (q, k, v, do, o, lse, scale, big), g_big
 
 
@@ -71,8 +75,23 @@ def test_stage_bit_4_replays_the_gemm_on_the_stored_ds():
     assert torch.equal(dq, dq_full)
 
 
-def test_causal_problems_keep_the_recompute_path():
-    q = torch.zeros(1, 2, 64, 512, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(1, 2, 64, 512, dtype=torch.bfloat16, device="cuda")
+@pytest.mark.parametrize("Nq,Nkv", [(300, 300), (256, 700), (700, 256), (100, 1000), (513, 769)])
+def test_stored_ds_backward_causal(Nq, Nkv):
+    # bottom-right causal: the dQ GEMM stops at each tile's last legal key, and
+    # rows with no legal key (Nq > Nkv) get dQ = 0
+    run_both(1, 4, 2, Nq, Nkv, 512, seed=Nq + 2 * Nkv, causal=True)
+
+
+def test_varlen_and_other_head_dims_keep_the_recompute_path():
+    q = torch.zeros(1, 2, 64, 320, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 2, 64, 320, dtype=torch.bfloat16, device="cuda")
     assert api.bwd_workspace_bytes(q, k, True) == api.bwd_workspace_bytes(q, k)
-    assert api.bwd_workspace_bytes(q, k, False) > api.bwd_workspace_bytes(q, k)
+    q5 = torch.zeros(1, 2, 64, 512, dtype=torch.bfloat16, device="cuda")
+    assert api.bwd_workspace_bytes(q5, q5, True) > api.bwd_workspace_bytes(q5, q5)
+
+
+def test_one_cta_family_forced_keeps_the_recompute_path(monkeypatch):
+    # only the CTA-pair dK kernel stores dS: with the one-CTA family forced, the
+    # large workspace must still give the recompute path's (correct) dQ
+    monkeypatch.setenv("FFPA_KERNEL", "single")
+    run_both(1, 4, 2, 150, 333, 512, dtype=torch.float16, seed=552, causal=True)

@@ -574,9 +574,9 @@ def run_ours(args):
     else:
         lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
         ws = api.bwd_workspace(q, k, w.causal)
-        # the stored-dS backward (dQ as one GEMM over the dS the dK launch wrote) when the workspace holds it
+        # the stored-tile backward when the workspace holds it: dK also stores P^T
+        # and dS^T, and dV and dQ are one GEMM each over them
         ds_path = ws.numel() >= api.bwd_workspace_bytes(q, k, w.causal) > api.bwd_workspace_bytes(q, k)
-        dq_bit = 16 if ds_path else 4
         # the user's path: one forward call and one backward call per step (the
         # backward's dV, dK and dQ kernels overlap their neighbours' tails)
         names = ("fwd", "bwd")
@@ -593,13 +593,16 @@ def run_ours(args):
 
         # per-kernel durations (a second timed pass, one launch per call:
         # preprocess | dV | dK | dQ are ffpa_bwd_stages bits 0, 1, 3, then 2, or 4
-        # for the dQ GEMM over the dS that the dK launch just stored)
-        kernel_names = ("fwd", "preprocess", "dv", "dk", "dq")
+        # for the dQ GEMM over the dS that the dK launch just stored; with bit 5
+        # dK also stores P and runs first, and dV is the GEMM over that P, as in
+        # the full call)
+        kernel_names = ("fwd", "preprocess", "dk", "dv", "dq") if ds_path else ("fwd", "preprocess", "dv", "dk", "dq")
+        stage_bits = (1, 8 | 32, 2 | 32, 16) if ds_path else (1, 2, 8, 4)
 
         def kernel_step(ev):
             ev[0].record(stream)
             api.fwd(q, k, v, w.causal, w.scale, out=o, lse=lse)
-            for i, bit in enumerate((1, 2, 8, dq_bit)):
+            for i, bit in enumerate(stage_bits):
                 ev[i + 1].record(stream)
                 api.bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws, dq=dq, dk=dk, dv=dv, stages=bit)
             ev[5].record(stream)
@@ -651,13 +654,15 @@ def run_ours(args):
     clocks = clk.summary()
 
     # roofline of the dominant kernel (largest time share); algorithmic flops
-    # per launch = the GEMMs its outputs require: fwd 2 (S, PV), dV 2 (S, dV),
-    # dK 3 (S, dP, dK), dQ 3 (S, dP, dQ), each 2*B*Hq*Nq*Nkv*D (halved causal)
+    # per launch = the GEMMs it runs: fwd 2 (S, PV), dV 2 (S, dV) or 1 on the
+    # stored P, dK 3 (S, dP, dK), dQ 3 (S, dP, dQ) or 1 on the stored dS, each
+    # 2*B*Hq*Nq*Nkv*D (halved causal)
     gemm = f_fwd / 2.0
     if w.varlen:
         algo = {"fwd": 2 * gemm, "bwd": 8 * gemm}  # bwd: preprocess + dV (2) + dK (3) + dQ (3) units
     else:
-        algo = {"fwd": 2 * gemm, "dv": 2 * gemm, "dk": 3 * gemm, "dq": (1 if ds_path else 3) * gemm}
+        algo = {"fwd": 2 * gemm, "dv": (1 if ds_path else 2) * gemm, "dk": 3 * gemm,
+                "dq": (1 if ds_path else 3) * gemm}
     dom = max(algo, key=lambda n: per_ms[n])
     achieved = algo[dom] / (per_ms[dom] / 1e3) / 1e12
     peak = pk["bf16_tflops_sustained"]
@@ -690,6 +695,8 @@ def run_ours(args):
             "kernel_ms": per_ms,
             "dq_path": ("one GEMM over the dS stored by the dK launch" if not w.varlen and ds_path
                         else "S and dP recomputed"),
+            "dv_path": ("one GEMM over the P^T stored by the dK launch" if not w.varlen and ds_path
+                        else "S^T recomputed"),
             "kernel_ms_note": "each kernel launched alone (one call per stage), after the timed region"
             if not w.varlen else "fwd and bwd calls of the timed region",
             "pct_peak_burst": 100 * value / world / pk["bf16_tflops"],

@@ -222,7 +222,8 @@ def fwd_fp8_quantized(workspace, shape_q, shape_k, dtype, causal: bool = False, 
 
 def bwd_workspace_bytes(q, k, causal: bool | None = None) -> int:
     """Backward workspace bytes: the row statistics only (causal None), or with
-    room for the stored dS where that path applies (ffpa_bwd_workspace_bytes_ds)."""
+    room for the stored dS and P where that path applies
+    (ffpa_bwd_workspace_bytes_ds)."""
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape
     if causal is None:
@@ -230,12 +231,13 @@ def bwd_workspace_bytes(q, k, causal: bool | None = None) -> int:
     return int(_ffi.ffpa_bwd_workspace_bytes_ds(_dt(q), B, Hq, Hkv, Nq, Nkv, D, int(bool(causal))))
 
 
-DS_WORKSPACE_FRACTION = 0.25  # largest share of free device memory bwd() spends on the stored dS
+DS_WORKSPACE_FRACTION = 0.25  # largest share of free device memory bwd() spends on the stored dS and P
 
 
 def bwd_workspace(q, k, causal: bool):
-    """A backward workspace: with the stored-dS room when it applies and takes at
-    most DS_WORKSPACE_FRACTION of the free device memory, else the small one."""
+    """A backward workspace: with the stored-dS and -P room when it applies and
+    takes at most DS_WORKSPACE_FRACTION of the free device memory, else the
+    small one."""
     small = bwd_workspace_bytes(q, k)
     big = bwd_workspace_bytes(q, k, causal)
     n = small
@@ -250,9 +252,10 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
         dq=None, dk=None, dv=None, stages: int = 15):
     """Dense backward through ffpa_bwd_strided (views, no copy), or ffpa_bwd_stages
     for a subset of its launches (bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK,
-    bit 4 dQ from the dS a dK stage stored; contiguous tensors). Without a
-    workspace, one with room for the stored dS is allocated where that path
-    applies (bwd_workspace). Returns (dq, dk, dv)."""
+    bit 4 dQ from the dS a dK stage stored, bit 5 dV storing P / dK reading it;
+    contiguous tensors). Without a workspace, one with room for the stored dS
+    and P is allocated where that path applies (bwd_workspace). Returns
+    (dq, dk, dv)."""
     q, k, v, o, dout = _dense(q, k, v, o, dout)
     lse = lse.contiguous()
     B, Hq, Nq, D = q.shape

@@ -241,14 +241,22 @@ ffpa_status run_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, 
     a.dv = dv;
     a.delta = static_cast<float*>(workspace);
     a.lse_log2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + need / 2);
-    a.stages = stages & 31u;
+    a.stages = stages & 63u;
     // a workspace with room for dS^T after the row statistics selects the dQ
-    // GEMM from the dS that the dK launch stores (where that path applies)
+    // GEMM from the dS that the dK launch stores (where that path applies);
+    // room for P^T after it as well, the dK launch that reads the P of dV
     a.ds = nullptr;
-    if (ffpa::dsq_supported(pb) && workspace_bytes >= need + ffpa::dsq_ds_bytes(pb))
+    a.p = nullptr;
+    if (ffpa::dsq_supported(pb) && workspace_bytes >= need + ffpa::dsq_ds_bytes(pb)) {
         a.ds = static_cast<char*>(workspace) + need;
+        const size_t p_off = need + align256(ffpa::dsq_ds_bytes(pb));
+        if (workspace_bytes >= p_off + ffpa::dsq_ds_bytes(pb)) a.p = static_cast<char*>(workspace) + p_off;
+    }
     if ((a.stages & 16u) && a.ds == nullptr)
         return fail(FFPA_ERR_INVALID_VALUE, "stage bit 4 (dQ from stored dS) needs the larger workspace of "
+                                            "ffpa_bwd_workspace_bytes_ds on a dense D = 256 / 512 problem");
+    if ((a.stages & 32u) && a.p == nullptr)
+        return fail(FFPA_ERR_INVALID_VALUE, "stage bit 5 (stored P) needs the workspace of "
                                             "ffpa_bwd_workspace_bytes_ds on a dense D = 256 / 512 problem");
     return launch_result(ffpa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)), "backward launch");
 }
@@ -503,7 +511,8 @@ size_t ffpa_bwd_workspace_bytes_ds(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq
     const size_t small = ffpa_bwd_workspace_bytes(dt, B, Hq, Hkv, Nq, Nkv, D);
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nkv <= 0 || Hq % Hkv != 0) return small;
     const ffpa::Problem pb = dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, 1.f);
-    return ffpa::dsq_supported(pb) ? small + ffpa::dsq_ds_bytes(pb) : small;
+    // dS^T, then P^T at the next 256-byte boundary
+    return ffpa::dsq_supported(pb) ? small + align256(ffpa::dsq_ds_bytes(pb)) + ffpa::dsq_ds_bytes(pb) : small;
 }
 
 size_t ffpa_bwd_workspace_bytes(ffpa_dtype, int B, int Hq, int, int Nq, int, int)
@@ -561,7 +570,7 @@ ffpa_status ffpa_bwd_stages(ffpa_dtype dt, const void* q, const void* k, const v
 {
     FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
     FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
-    if (stages > 31u) return fail(FFPA_ERR_INVALID_VALUE, "stages mask %u: only bits 0..4", stages);
+    if (stages > 63u) return fail(FFPA_ERR_INVALID_VALUE, "stages mask %u: only bits 0..5", stages);
     const long q_rows = static_cast<long>(B) * Hq * Nq;
     const long k_rows = static_cast<long>(B) * Hkv * Nkv;
     return run_bwd(dt, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes,

@@ -11,7 +11,10 @@
 //   dK         : same tiles: dS^T = P^T (V dO^T - delta), dK += scale * dS^T Q
 //   dQ         : per query tile, over key tiles: dS = P (dO V^T - delta),
 //                dQ += scale * dS K
-// The three gradient launches run the cluster-exchange kernel (xchg.cu).
+// The three gradient launches run the cluster-exchange kernel (xchg.cu). With
+// room in the workspace (dense, D = 256 / 512), the dK launch also stores its
+// P^T and dS^T tiles, and dV = P^T dO and dQ = scale dS K become plain GEMMs
+// over them (dsq.cu): preprocess, dK, dV, dQ.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tile_common.cuh"
@@ -103,15 +106,33 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
     // disjoint outputs: each after the first is a programmatic dependent of the
     // one before, so it fills the SMs that the previous one's last wave leaves
     // idle (the first waits for the preprocess as usual; the later ones start
-    // only once all of its CTAs have started, hence after the preprocess)
-    // dQ from stored dS: the dK launch also writes dS^T into a.ds, then a plain
-    // GEMM forms dQ (dense, D = 256 / 512, with the buffer given);
-    // stage bit 4 runs that GEMM alone on a buffer an earlier dK launch filled
-    // (only the CTA-pair dK kernel stores dS)
+    // only once all of its CTAs have started, hence after the preprocess).
+    // Stored tiles (dense, D = 256 / 512, the buffers given; only the CTA-pair
+    // dK kernel stores them):
+    //  - dS: the dK launch also writes dS^T into a.ds and dQ is a plain GEMM
+    //    over it; stage bit 4 runs that GEMM alone on a buffer an earlier dK
+    //    launch filled;
+    //  - P: with dV and dK in one call, or stage bit 5, the dK launch also
+    //    writes P^T into a.p and dV is a plain GEMM over it, after dK.
     const bool use_ds = a.ds != nullptr && !q_empty && !kv_empty && dsq_supported(pb) && xchg_uses_pair(pb);
     if ((a.stages & 16u) && !use_ds) return cudaErrorInvalidConfiguration;  // no stored dS to read
+    const bool use_p = use_ds && a.p != nullptr;
+    if ((a.stages & 32u) && !use_p) return cudaErrorInvalidConfiguration;  // no P buffer
+    const bool p_mode = use_p && ((a.stages & 32u) || ((a.stages & 2u) && (a.stages & 8u)));
+    auto tile_gemm = [&](bool dv) {
+        DsqArgs d{};
+        d.pb = pb;
+        d.bf16 = BF16;
+        d.dv = dv ? 1 : 0;
+        d.tiles = dv ? a.p : a.ds;
+        d.rhs = dv ? a.dO : a.k;
+        d.out = dv ? a.dv : a.dq;
+        d.ctl = a.ctl;
+        // a plain launch: the GEMM reads what the dK launch wrote
+        return launch_dsq(d, st);
+    };
     x.pdl = 0;
-    if (!kv_empty && (a.stages & 2u)) {
+    if (!kv_empty && (a.stages & 2u) && !p_mode) {
         if ((e = launch_xchg(XOP_DV, x, st)) != cudaSuccess) return e;
         x.pdl = 1;
     }
@@ -119,20 +140,15 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
         XArgs xk = x;
         xk.store_ds = use_ds ? 1 : 0;
         xk.ds = a.ds;
+        xk.store_p = p_mode ? 1 : 0;
+        xk.p = a.p;
         if ((e = launch_xchg(XOP_DK, xk, st)) != cudaSuccess) return e;
         x.pdl = 1;
     }
+    if (!kv_empty && (a.stages & 2u) && p_mode && (e = tile_gemm(true)) != cudaSuccess) return e;
     const bool dq_from_ds = use_ds && ((a.stages & 16u) || ((a.stages & 4u) && (a.stages & 8u)));
     if (!q_empty && dq_from_ds) {
-        DsqArgs d{};
-        d.pb = pb;
-        d.bf16 = BF16;
-        d.ds = a.ds;
-        d.k = a.k;
-        d.dq = a.dq;
-        d.ctl = a.ctl;
-        // a plain launch: the GEMM reads what the dK launch wrote
-        if ((e = launch_dsq(d, st)) != cudaSuccess) return e;
+        if ((e = tile_gemm(false)) != cudaSuccess) return e;
     } else if (!q_empty && (a.stages & 4u) && (e = launch_xchg(XOP_DQ, x, st)) != cudaSuccess) {
         return e;
     }

@@ -1,23 +1,31 @@
-// dQ from the stored dS: dQ = scale * dS K, a plain GEMM per (batch, query
-// head), for dense problems whose dS the dK kernel wrote to the
-// backward workspace (FFPA docs, "CuTe-DSL Backend" page, "Blackwell status":
-// the backward as a preprocess plus separate gradient launches; here the dQ
-// launch reuses the dS tiles of the dK launch instead of recomputing S and
-// dP, which turns 3 GEMM units into 1).
+// dQ and dV from the tiles the dK kernel stored: plain GEMMs for dense
+// problems whose dS^T and P^T the dK kernel wrote to the backward workspace
+// (FFPA docs, "CuTe-DSL Backend" page, "Blackwell status": the backward as a
+// preprocess plus separate gradient launches; here the dQ and dV launches
+// reuse the dK launch's tiles instead of recomputing S (and dP), which turns
+// 3 + 2 GEMM units into 1 + 1).
 //
-// The dK kernel stores dS^T, [B, Hq, Nkv, ldq] (keys x queries, queries
-// contiguous), tile by tile. A CTA pair owns 256 query rows (128 per CTA, in
-// its TMEM lanes) and the whole head dim (D <= 512 fp32 columns of TMEM), and
-// walks the keys in blocks of 64, up to the last key any of its rows may see
-// under the bottom-right causal mask (the dK kernel wrote every block below
-// that, masked entries as zeros; causal grids take the longest tiles first):
-//   A = dS for my 128 queries x 64 keys, read from dS^T as an MN-major
+// The dK kernel stores dS^T and P^T, each [B, Hq, Nkv, ldq] (keys x queries,
+// queries contiguous), tile by tile; masked entries are stored zeros, and
+// under the bottom-right causal mask every tile that holds a legal entry is
+// stored. A CTA pair owns 256 output rows (128 per CTA, in its TMEM lanes)
+// and the whole head dim (D <= 512 fp32 columns of TMEM); a ring of 4 stages
+// feeds M=256, N=256 pair MMAs, acc[:, 256 j ..] += A B_j:
+//   dQ = scale dS K (rows = queries of one head; causal grids take the
+//       longest tiles, the last ones, first). K runs over keys in blocks of
+//       64, up to the last key any row of the pair may see.
+//       A = dS for my 128 queries x 64 keys, read from dS^T as an MN-major
 //       operand (two 64-query boxes of 64 key rows x 128 bytes);
-//   B = K for 64 keys x my 128 columns of each 256-column half of D, also
-//       MN-major (the forward's value-operand form);
-//   acc[:, 256 j .. 256 j + 255] += A B_j as M=256, N=256 pair MMAs.
-// Warp 0 lanes 0 / 1 load A / B with TMA into a 4-stage ring, warp 1 of the
-// even rank issues the MMAs, warps 2..5 scale and store dQ rows.
+//       B = K for 64 keys x my 128 columns of each 256-column half of D,
+//       also MN-major (the forward's value-operand form).
+//   dV = P^T dO (rows = keys of one KV head; the first tiles are the
+//       longest). K runs over the query heads of the group and, per head,
+//       over queries in blocks of 64 from the first that any row of the pair
+//       may see.
+//       A = P^T for my 128 keys x 64 queries, K-major (one box);
+//       B = dO for 64 queries x my 128 columns of each half, MN-major.
+// Warp 0 lanes 0 / 1 load A / B with TMA, warp 1 of the even rank issues the
+// MMAs, warps 2..5 scale and store the output rows.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tile_common.cuh"
@@ -42,7 +50,7 @@ struct QGeo {
     int stage_bytes;  // per CTA: A (16 KiB) + B (nj x 16 KiB)
 };
 
-template <bool BF16>
+template <bool BF16, bool DV>
 __global__ void __launch_bounds__(kQThreads, 1)
     dsq_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB, const DsqArgs a,
                const QGeo gm)
@@ -52,12 +60,27 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int rh = rank & 1;
     const bool leader = rh == 0;
     const int G = pb.Hq / pb.Hkv;
-    const int b = blockIdx.z / pb.Hq, h = blockIdx.z % pb.Hq, hk = h / G;
-    const int tile = pb.causal ? static_cast<int>(gridDim.y - 1 - blockIdx.y) : static_cast<int>(blockIdx.y);
-    const int q0 = tile * 256;
-    const int qc = q0 + 128 * rh;  // my first query row
-    const int key_end = pb.causal ? min(pb.Nkv, q0 + 255 + (pb.Nkv - pb.Nq) + 1) : pb.Nkv;
-    const int n_kb = key_end > 0 ? (key_end + 63) / 64 : 0;  // the same for both CTAs of the pair
+    const int off = pb.Nkv - pb.Nq;  // causal: key j legal for query i iff j <= i + off
+    // dQ: (b, query head h); dV: (b, KV head hk), the group's query heads hk*G ..
+    const int hb = DV ? pb.Hkv : pb.Hq;
+    const int b = blockIdx.z / hb, h = blockIdx.z % hb, hk = DV ? h : h / G;
+    // causal: the longest tiles first (dQ: the last query tiles, dV: the first key tiles)
+    const int tile = (pb.causal && !DV) ? static_cast<int>(gridDim.y - 1 - blockIdx.y) : static_cast<int>(blockIdx.y);
+    const int row0 = tile * 256;
+    const int rc = row0 + 128 * rh;  // my first row (query for dQ, key for dV)
+    const int n_rows = DV ? pb.Nkv : pb.Nq;
+    // K blocks of 64 (both CTAs of the pair alike): dQ keys [0, key_end);
+    // dV per query head: queries [64 qb_lo, Nq)
+    int kb_lo = 0, n_kb;
+    if constexpr (DV) {
+        const int i_lo = pb.causal ? max(0, row0 - off) : 0;
+        kb_lo = i_lo / 64;
+        n_kb = i_lo < pb.Nq ? (pb.Nq + 63) / 64 - kb_lo : 0;
+    } else {
+        const int key_end = pb.causal ? min(pb.Nkv, row0 + 255 + off + 1) : pb.Nkv;
+        n_kb = key_end > 0 ? (key_end + 63) / 64 : 0;
+    }
+    const int n_it = DV ? G * n_kb : n_kb;  // K iterations
     const int tcols = gm.nj * 256;
 
     __shared__ QStatic sh;
@@ -103,19 +126,34 @@ __global__ void __launch_bounds__(kQThreads, 1)
             }
             RingPos rp;
             int issued = 0;
-            for (int kb = 0; kb < n_kb; ++kb) {
+            for (int it = 0; it < n_it; ++it) {
                 const bool got = mbar_wait(&sh.empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, QS_PROD);
                 if (!__all_sync(0x3u, got)) break;
                 uint8_t* st = smem + rp.slot * gm.stage_bytes;
                 const uint32_t fb = mapa_shared(smem_u32(&sh.full[rp.slot]), lead_rank);
-                if (lane == 0) {
-                    // A: dS^T rows = keys [64 kb, +64), my 128 queries as two 64-query boxes
-                    tma_load_4d_pair(st, &tA, fb, qc, kb * 64, h, b);
-                    tma_load_4d_pair(st + 8192, &tA, fb, qc + 64, kb * 64, h, b);
+                if constexpr (DV) {
+                    const int hq = hk * G + it / n_kb;    // query head of the group
+                    const int i0 = (kb_lo + it % n_kb) * 64;  // first query of the block
+                    if (lane == 0) {
+                        // A: P^T rows = my 128 keys, queries [i0, +64)
+                        tma_load_4d_pair(st, &tA, fb, i0, rc, hq, b);
+                    } else {
+                        // B: dO rows = queries [i0, +64), my 128 columns of each 256-column half
+                        for (int j = 0; j < gm.nj; ++j)
+                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, i0, (j * 256 + rh * 128) / 64, hq, b);
+                    }
                 } else {
-                    // B: K rows = keys [64 kb, +64), my 128 columns of each 256-column half
-                    for (int j = 0; j < gm.nj; ++j)
-                        tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, kb * 64, (j * 256 + rh * 128) / 64, hk, b);
+                    const int kb = it;
+                    if (lane == 0) {
+                        // A: dS^T rows = keys [64 kb, +64), my 128 queries as two 64-query boxes
+                        tma_load_4d_pair(st, &tA, fb, rc, kb * 64, h, b);
+                        tma_load_4d_pair(st + 8192, &tA, fb, rc + 64, kb * 64, h, b);
+                    } else {
+                        // B: K rows = keys [64 kb, +64), my 128 columns of each 256-column half
+                        for (int j = 0; j < gm.nj; ++j)
+                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, kb * 64, (j * 256 + rh * 128) / 64, hk,
+                                             b);
+                    }
                 }
                 rp.advance(kQStages);
                 ++issued;
@@ -133,21 +171,24 @@ __global__ void __launch_bounds__(kQThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer (pair)
         if (leader && elect_one()) {
-            const uint32_t idesc = idesc_f16(256, 256, BF16, true, true);
+            // A: MN-major dS (dQ) or K-major P^T (dV); B: MN-major
+            const uint32_t idesc = idesc_f16(256, 256, BF16, !DV, true);
             RingPos rp;
-            for (int kb = 0; kb < n_kb; ++kb) {
+            for (int it = 0; it < n_it; ++it) {
                 if (!mbar_wait_cluster(&sh.full[rp.slot], rp.phase, abort_flag, status, lim, QS_RING)) break;
                 mbar_arrive_expect_tx(&sh.full[rp.slot], 2 * gm.stage_bytes);  // arm the slot's next fill
                 tc_fence_after();
                 const uint8_t* st = smem + rp.slot * gm.stage_bytes;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    // 16 keys per MMA: 16 rows x 128 bytes into both operands; 64-element
-                    // chunks along M (A) and N (B) are 64 key rows x 128 bytes apart
-                    const uint64_t ad = sdesc_sw128(smem_u32(st + kk * 2048), 8192, 1024);
+                    // 16 K values per MMA. MN-major operands: 16 rows x 128 bytes, with
+                    // 64-element chunks along M (A) and N (B) 64 rows x 128 bytes apart;
+                    // K-major A (dV): 32 bytes into each of the 128 rows of the box
+                    const uint64_t ad = DV ? sdesc_sw128(smem_u32(st + kk * 32), 16, 1024)
+                                           : sdesc_sw128(smem_u32(st + kk * 2048), 8192, 1024);
                     for (int j = 0; j < gm.nj; ++j) {
                         const uint64_t bd = sdesc_sw128(smem_u32(st + 16384 * (1 + j) + kk * 2048), 8192, 1024);
-                        umma_f16_pair(tmem + j * 256, ad, bd, idesc, (kb | kk) != 0);
+                        umma_f16_pair(tmem + j * 256, ad, bd, idesc, (it | kk) != 0);
                     }
                 }
                 umma_commit_pair_multicast(&sh.empty[rp.slot], pair_mask);
@@ -159,25 +200,26 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // ------------------------------------------------------ epilogue (warps 2..5)
         const int quarter = warp & 3;
         const int r = quarter * 32 + static_cast<int>(lane_id());
-        const int q = qc + r;
+        const int q = rc + r;  // my output row
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&sh.acc, 0, abort_flag, status, lim, QS_ACC));
         tc_fence_after();
         if (ok) {
-            // no key for any row of the pair: dQ = 0 (the accumulator was never written)
-            const float mul = n_kb > 0 ? pb.scale : 0.f;
-            uint16_t* dst = reinterpret_cast<uint16_t*>(a.dq) + static_cast<size_t>(b) * pb.vdq.sb +
-                            static_cast<size_t>(h) * pb.vdq.sh + static_cast<size_t>(q) * pb.vdq.sn;
+            // no K block for any row of the pair: zero rows (the accumulator was never written)
+            const float mul = n_it > 0 ? (DV ? 1.f : pb.scale) : 0.f;
+            const View& vo = DV ? pb.vdv : pb.vdq;
+            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + static_cast<size_t>(b) * vo.sb +
+                            static_cast<size_t>(h) * vo.sh + static_cast<size_t>(q) * vo.sn;
             for (int cc = 0; cc < pb.D; cc += 32) {
                 uint32_t v[32];
-                if (n_kb > 0) {
+                if (n_it > 0) {
                     tmem_ld32(tmem + lane_off + cc, v);
                     tmem_ld_wait(v);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0u;
                 }
-                if (q < pb.Nq) {
+                if (q < n_rows) {
                     uint32_t w[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
@@ -235,15 +277,21 @@ cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s)
     const Problem& pb = a.pb;
     if (!dsq_supported(pb)) return cudaErrorInvalidConfiguration;
     CUtensorMap tA, tB;
-    if (!make_ds_map(&tA, a.ds, pb, a.bf16, 64) || !make_slab_map(&tB, a.k, pb, true, a.bf16, 64, 2, pb.vk))
-        return cudaErrorInvalidValue;
+    // dQ: dS^T as 64 queries x 64 key rows boxes, K rows; dV: P^T as 64 queries x
+    // 128 key rows boxes, dO rows (the query side)
+    const bool okm = a.dv ? make_ds_map(&tA, a.tiles, pb, a.bf16, 128) &&
+                                make_slab_map(&tB, a.rhs, pb, false, a.bf16, 64, 2, pb.vdo)
+                          : make_ds_map(&tA, a.tiles, pb, a.bf16, 64) &&
+                                make_slab_map(&tB, a.rhs, pb, true, a.bf16, 64, 2, pb.vk);
+    if (!okm) return cudaErrorInvalidValue;
     QGeo gm{};
     gm.nj = pb.D / 256;
     gm.stage_bytes = 16384 * (1 + gm.nj);
     const int smem = kQStages * gm.stage_bytes;
-    const dim3 grid(2, (pb.Nq + 255) / 256, pb.B * pb.Hq);
+    const dim3 grid = a.dv ? dim3(2, (pb.Nkv + 255) / 256, pb.B * pb.Hkv) : dim3(2, (pb.Nq + 255) / 256, pb.B * pb.Hq);
     if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
-    auto kern = a.bf16 ? dsq_kernel<true> : dsq_kernel<false>;
+    auto kern = a.dv ? (a.bf16 ? dsq_kernel<true, true> : dsq_kernel<false, true>)
+                     : (a.bf16 ? dsq_kernel<true, false> : dsq_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -55,8 +55,10 @@ struct BwdArgs {
     void *dq, *dk, *dv;
     float* delta;      // workspace [rows] fp32: rowsum(dO * O)
     float* lse_log2;   // workspace [rows] fp32: LSE * log2(e), +inf for empty rows
-    unsigned stages;   // bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK, bit 4 dQ from the stored dS
+    unsigned stages;   // bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK, bit 4 dQ from the stored dS,
+                       // bit 5 stored P (dK stores it, dV is the GEMM over it)
     void* ds;          // dS^T buffer of dsq_ds_bytes() bytes, or null (dQ recomputes S and dP)
+    void* p;           // P^T buffer of the same size, or null (dV recomputes S)
     DeviceCtl ctl;
 };
 
@@ -85,16 +87,22 @@ struct XArgs {
     // dK: also store every dS^T tile to ds ([B, Hq, Nkv, ldq], ldq = Nq rounded up to 8)
     int store_ds;
     void* ds;
+    // dK: also store every P^T tile (input dtype) to p, the same layout
+    int store_p;
+    void* p;
 };
 
-// dQ = scale * dS K from the dS^T the dK kernel stored (dense, D = 256 or
-// 512); dsq_ds_bytes is the size of that dS^T buffer.
+// The GEMMs over the tiles the dK kernel stored (dense, D = 256 or 512;
+// dsq_ds_bytes is the size of one [B, Hq, Nkv, ldq] tile buffer):
+//   dv = 0: dQ = scale * dS K from the stored dS^T;
+//   dv = 1: dV = P^T dO from the stored P^T, over the query heads of the group.
 struct DsqArgs {
     Problem pb;
     int bf16;
-    const void* ds;
-    const void* k;
-    void* dq;
+    int dv;
+    const void* tiles;  // dS^T (dv = 0) or P^T (dv = 1)
+    const void* rhs;    // K (dv = 0) or dO (dv = 1)
+    void* out;          // dQ (dv = 0) or dV (dv = 1), in its view
     DeviceCtl ctl;
 };
 bool dsq_supported(const Problem& pb);

@@ -87,6 +87,8 @@ struct __align__(1024) StaticSmem {
     int abort_flag;
     uint32_t relay_sink[4];  // (even rank) target of the odd rank's 4-byte relay stores
     uint64_t stored[2];      // (dK storing dS) the store of the own Z buffer has read it
+    uint64_t p_full[2];      // (dK storing P) the own Z buffer holds the step's P^T
+    uint64_t p_read[2];      // (dK storing P) the store of that P^T has read the buffer
 };
 static_assert(sizeof(StaticSmem) == 1024, "static shared block must be exactly 1 KiB");
 
@@ -110,8 +112,8 @@ template <int OP, bool BF16, bool VARLEN, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     pair_kernel(const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tA2,
                 const __grid_constant__ CUtensorMap tB1, const __grid_constant__ CUtensorMap tB2,
-                const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tS, const XArgs a,
-                const PGeo gm)
+                const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tS,
+                const __grid_constant__ CUtensorMap tP, const XArgs a, const PGeo gm)
 {
     // the next GEMM kernel of a backward may take SMs as this grid's last CTAs start
     pdl_trigger();
@@ -233,8 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         mbar_init(&sh.half, 256);
-        mbar_init(&sh.stored[0], 1);
-        mbar_init(&sh.stored[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh.stored[i], 1);
+            mbar_init(&sh.p_full[i], 256);
+            mbar_init(&sh.p_read[i], 1);
+        }
         mbar_init(&sh.lsum, 1);
         mbar_init(&sh.drain, 1);
         sh.abort_flag = 0;
@@ -640,37 +645,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Ships the own Z tile of every step, once all 256 elementwise threads
         // wrote it, into the CTA of every other pair that holds my rows, as one
         // bulk copy each, once that pair's value products consumed the previous
-        // copy in the target buffer. The dK kernel that stores dS also writes the
-        // tile (dS^T: my 128 key rows x the tile's 128 queries) to the dS buffer
-        // with two TMA stores and reports when they have read it.
-        const bool store = OP == XOP_DK && a.store_ds != 0;
-        if ((C > 1 || store) && elect_one()) {
-            if (store) prefetch_tmap(&tS);
+        // copy in the target buffer. The dK kernel that stores dS then also writes
+        // the tile (dS^T: my 128 key rows x the tile's 128 queries) to that buffer
+        // with two TMA stores and reports when they have read it; the dK kernel
+        // that stores P does the same, earlier in the step, with the P^T tile the
+        // elementwise threads put in the buffer before dS.
+        const bool store_ds = OP == XOP_DK && a.store_ds != 0;
+        const bool store_p = OP == XOP_DK && a.store_p != 0;
+        if ((C > 1 || store_ds || store_p) && elect_one()) {
+            if (store_ds) prefetch_tmap(&tS);
+            if (store_p) prefetch_tmap(&tP);
+            // the stored tiles are read by later launches, after many more were
+            // written: they leave L2 before the operand tiles this kernel reuses
+            const uint64_t pol = l2_policy_evict_first();
             for (int s = 0; s < n_steps; ++s) {
                 const int bb = zbuf(s);
-                bool ok = mbar_wait(&sh.z_full[bb], zpar(s), abort_flag, status, lim, PS_COPY);
-                if (ok && store) {
-                    const int t = s * C + c;
-                    if (t < n_ct) {
-                        const uint8_t* zown = zslot(C - 1, bb);
-                        tma_store_4d(&tS, zown, col_row0(t), row_co(r0), col_head(t), bco);
-                        tma_store_4d(&tS, zown + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco);
-                        bulk_commit_group();
-                        bulk_wait_read_all();
+                const int t = s * C + c;
+                const uint8_t* zown_base = zslot(C - 1, bb);
+                bool ok = true;
+                if (store_p) {
+                    ok = mbar_wait(&sh.p_full[bb], zpar(s), abort_flag, status, lim, PS_COPY);
+                    if (ok) {
+                        if (t < n_ct) {
+                            tma_store_4d_hint(&tP, zown_base, col_row0(t), row_co(r0), col_head(t), bco, pol);
+                            tma_store_4d_hint(&tP, zown_base + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco,
+                                              pol);
+                            bulk_commit_group();
+                            bulk_wait_read_all();
+                        }
+                        mbar_arrive(&sh.p_read[bb]);
                     }
-                    mbar_arrive(&sh.stored[bb]);
                 }
+                if (ok) ok = mbar_wait(&sh.z_full[bb], zpar(s), abort_flag, status, lim, PS_COPY);
+                // the exchange first (the other pairs' value products wait for it)
                 for (int k = 1; k < C && ok; ++k) {
                     const int p = (c + k) % C;
                     if (s >= nbuf)
                         ok = mbar_wait_cluster(&sh.slot_free[p][bb], zpar(s) ^ 1u, abort_flag, status, lim, PS_SLOT);
                     if (ok)
-                        bulk_copy_s2cluster(mapa_shared(smem_u32(zslot(slot_of(c, p), bb)), xrank(p)), zslot(C - 1, bb),
+                        bulk_copy_s2cluster(mapa_shared(smem_u32(zslot(slot_of(c, p), bb)), xrank(p)), zown_base,
                                             kZ, mapa_shared(smem_u32(&sh.zpeer[slot_of(c, p)][bb]), xrank(p)));
+                }
+                if (ok && store_ds) {
+                    if (t < n_ct) {
+                        tma_store_4d_hint(&tS, zown_base, col_row0(t), row_co(r0), col_head(t), bco, pol);
+                        tma_store_4d_hint(&tS, zown_base + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco, pol);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                    }
+                    mbar_arrive(&sh.stored[bb]);
                 }
                 if (!ok) break;
             }
-            if (store) bulk_wait_all();  // the dS stores are complete before the CTA leaves
+            if (store_ds || store_p) bulk_wait_all();  // the stores are complete before the CTA leaves
         }
     } else {
         // ------------------------------------------------------ elementwise
@@ -715,6 +742,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             return half == 0 ? INFINITY : 0.f;
         };
         float stat_next = (!T::kRowsQ && n_steps > 0) ? fetch_stat(c) : 0.f;
+        // Own buffer zbuf(s) was last used at step s - nbuf: it may be rewritten once
+        // the value MMAs of that step (acc, observed here at every step, in order)
+        // and the copies of it (slot_free of every other pair: it consumed the copy,
+        // so the copy has read the buffer) are done, and (dK storing dS) the store
+        // of that step's dS has read it.
+        auto own_free = [&](int s) -> bool {
+            if (s < nbuf) return true;
+            const int sp = s - nbuf, bb = zbuf(s);
+            bool got = mbar_wait(&sh.acc[sp & 1], accpar(sp), abort_flag, status, lim, PS_ACC);
+            for (int p = 0; p < C && got; ++p)
+                if (p != c) got = mbar_wait_cluster(&sh.slot_free[p][bb], zpar(sp), abort_flag, status, lim, PS_SLOT);
+            if (got && OP == XOP_DK && a.store_ds) got = mbar_wait(&sh.stored[bb], zpar(sp), abort_flag, status, lim, PS_COPY);
+            return warp_ok(got);
+        };
         for (int s = 0; s < n_steps; ++s) {
             const int t = s * C + c;
             const int sb = T::kXdb ? (s & 1) : 0;
@@ -919,6 +960,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh.x_free[0]);
+                    if (OP == XOP_DK && a.store_p) {
+                        // dK storing P: P^T (input dtype) goes through the own buffer first;
+                        // the copier stores it while dP^T is computed, then dS^T replaces it
+                        if (!own_free(s)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* zp = zslot(C - 1, zbuf(s)) + half * 16384;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 pv = unpack2<false>(pp[4 * u + e]);
+                                w[e] = pack2<BF16>(pv.x, pv.y);
+                            }
+                            *reinterpret_cast<uint4*>(zp + sw128_offset(r, u)) = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(&sh.p_full[zbuf(s)]);
+                    }
                     if (!warp_ok(mbar_wait(&sh.x_full[1], s & 1, abort_flag, status, lim, PS_XFULL))) {
                         ok = false;
                         break;
@@ -949,25 +1011,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.x_free[(T::kTwo || sb) ? 1 : 0]);
-            // Own buffer bb was last used at step s - nbuf: it may be rewritten once the
-            // value MMAs of that step (acc, observed here at every step, in order)
-            // and the copies of it (slot_free of every other pair: it consumed the
-            // copy, so the copy has read the buffer) are done.
             const int bb = zbuf(s);
-            if (s >= nbuf) {
-                const int sp = s - nbuf;
-                bool got = mbar_wait(&sh.acc[sp & 1], accpar(sp), abort_flag, status, lim, PS_ACC);
-                for (int p = 0; p < C && got; ++p)
-                    if (p != c) got = mbar_wait_cluster(&sh.slot_free[p][bb], zpar(sp), abort_flag, status, lim, PS_SLOT);
-                // dK storing dS: the store of step sp has read the buffer
-                if (got && OP == XOP_DK && a.store_ds)
-                    got = mbar_wait(&sh.stored[bb], zpar(sp), abort_flag, status, lim, PS_COPY);
-                if (!warp_ok(got)) {
+            uint8_t* zown = zslot(C - 1, bb);
+            if (OP == XOP_DK && a.store_p) {
+                // the P^T of this step, written to the buffer earlier, has been read by its store
+                if (!warp_ok(mbar_wait(&sh.p_read[bb], zpar(s), abort_flag, status, lim, PS_COPY))) {
                     ok = false;
                     break;
                 }
+            } else if (!own_free(s)) {
+                ok = false;
+                break;
             }
-            uint8_t* zown = zslot(C - 1, bb);
             if constexpr (F8) {
                 // one 128-byte row of 128 e4m3 values: my 64 columns are 16-byte units 4 half .. 4 half + 3
 #pragma unroll
@@ -1104,7 +1159,7 @@ cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const PGeo& gm, i
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a, gm);
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], a, gm);
 }
 
 template <int OP>
@@ -1166,7 +1221,7 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const Src sdo = q_empty ? Src{a.k, pb.vk, true} : (a.dO ? Src{a.dO, pb.vdo, false} : sq);
     const Src sk = kv_empty ? Src{a.q, pb.vq, false} : Src{a.k, pb.vk, true};
     const Src sv = kv_empty ? Src{a.q, pb.vq, false} : Src{a.v, pb.vv, true};
-    CUtensorMap m[6];
+    CUtensorMap m[7];
     bool okm = true;
     auto row = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 128, 2, x.v); };
     auto col = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 64, 4, x.v); };
@@ -1181,6 +1236,7 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
         m[1] = m[0];
         m[3] = m[2];
         m[5] = m[0];
+        m[6] = m[0];
         if (!okm) return cudaErrorInvalidValue;
         const int n_rt8 = (pb.Nq + 255) / 256;
         const int bz8 = pb.B * pb.Hq;
@@ -1209,6 +1265,9 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     // dK storing dS: the dS^T buffer as stored tiles (64 queries x 128 key rows)
     if (op == XOP_DK && a.store_ds) okm = okm && make_ds_map(&m[5], a.ds, pb, a.bf16, 128);
     else m[5] = m[0];
+    // dK storing P: the P^T buffer, the same layout
+    if (op == XOP_DK && a.store_p) okm = okm && make_ds_map(&m[6], a.p, pb, a.bf16, 128);
+    else m[6] = m[0];
     if (!okm) return cudaErrorInvalidValue;
     const int n_rt = (n_rows + 255) / 256;
     if (n_rt == 0 || bz == 0) return cudaSuccess;

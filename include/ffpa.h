@@ -172,12 +172,18 @@ FFPA_API ffpa_status ffpa_fwd_fp8_quantized(ffpa_dtype dt, ffpa_view o, float* l
 /* Workspace bytes ffpa_bwd needs for this problem (fp32 row statistics). */
 FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 /*
- * Workspace bytes that also hold dS^T for the stored-dS backward: on a dense
- * problem with D = 256 or 512, ffpa_bwd / ffpa_bwd_strided given a
- * workspace at least this large have the dK launch also store every dS tile
- * (bf16/fp16, the same rounded values it multiplies) and form dQ = scale dS K
- * with one GEMM, instead of recomputing S and dP in a dQ launch (3 GEMM units
- * become 1). Costs B * Hq * Nkv * round_up(Nq, 8) * 2 extra bytes. Returns
+ * Workspace bytes that also hold dS^T and P^T for the stored-tile backward:
+ * on a dense problem with D = 256 or 512, ffpa_bwd / ffpa_bwd_strided given a
+ * workspace at least this large
+ *   - have the dK launch also store every P^T tile (in the input dtype) and
+ *     form dV = P^T dO with one GEMM after it, instead of a dV launch that
+ *     computes S^T = K Q^T again (2 GEMM units become 1);
+ *   - have the dK launch also store every dS tile (bf16/fp16, the same
+ *     rounded values it multiplies) and form dQ = scale dS K with one GEMM,
+ *     instead of recomputing S and dP in a dQ launch (3 GEMM units become 1).
+ * Each buffer is B * Hq * Nkv * round_up(Nq, 8) * 2 bytes. A workspace with
+ * room for the dS buffer only (ffpa_bwd_workspace_bytes() plus one buffer)
+ * keeps the stored dS and the dV launch that recomputes S^T. Returns
  * ffpa_bwd_workspace_bytes() where the path does not apply.
  */
 FFPA_API size_t ffpa_bwd_workspace_bytes_ds(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
@@ -221,7 +227,12 @@ FFPA_API ffpa_status ffpa_bwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, f
  * a dK stage also stores dS and a dQ stage in the same call is the
  * dS K GEMM; bit 4 runs that GEMM alone on the dS an earlier dK stage stored
  * in this workspace for the same inputs (bit 2 alone recomputes S and dP).
- * Arguments otherwise as ffpa_bwd.
+ * With dV and dK in one call, the dK stage also stores P^T and the dV stage
+ * is the P^T dO GEMM, run after dK; bit 5 selects that mode for a dK or dV
+ * stage on its own (a dV stage with bit 5 reads the P an earlier dK stage
+ * with bit 5 stored in this workspace for the same inputs). Bits 4 and 5
+ * without the workspace room they use are FFPA_ERR_INVALID_VALUE. Arguments
+ * otherwise as ffpa_bwd.
  */
 FFPA_API ffpa_status ffpa_bwd_stages(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
                                      const float* lse, const void* dO, void* dq, void* dk, void* dv,

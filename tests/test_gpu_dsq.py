@@ -1,10 +1,15 @@
-"""GPU parity of the stored-dS backward: the dK launch also writes dS^T to the
-workspace and dQ = scale dS K is one GEMM (dense, D = 256 / 512, causal or not).
+"""GPU parity of the stored-tile backward (dense, D = 256 / 512, causal or not):
+the dK launch also writes dS^T to the workspace and dQ = scale dS K is one
+GEMM; with room for P^T as well, the dK launch also writes P^T and
+dV = P^T dO is one GEMM instead of a launch that recomputes S^T.
 
-Every case runs the backward twice on the same inputs, with the small
-workspace (dQ recomputes S and dP) and with the stored-dS workspace, and
-checks both against the fp64 oracle with the usual gradient tolerance; dV (and
-dK when non-causal) must be bit-identical between the two.
+Every case runs the backward three times on the same inputs: with the small
+workspace (dQ recomputes S and dP), with room for dS only, and with room for
+dS and P. All three are checked against the fp64 oracle with the usual
+gradient tolerance. dV must be bit-identical between the first two (the same
+kernel); dK between the last two (storing P does not change it) and, when
+non-causal, between the first two (causal storing starts at an even query
+tile: an extra all-masked tile shifts the summation order).
 """
 import math
 
@@ -30,28 +35,38 @@ def _lib():
     oracle.build()
 
 
+def tile_buffer_bytes(q, k):
+    """Bytes of one stored-tile buffer: [B, Hq, Nkv, round_up(Nq, 8)] 16-bit values."""
+    B, Hq, Nq, _ = q.shape
+    Nkv = k.shape[2]
+    return B * Hq * Nkv * ((Nq + 7) // 8 * 8) * 2
+
+
 def run_both(B, Hq, Hkv, Nq, Nkv, D, dtype=torch.bfloat16, seed=0, causal=False):
     inp = workloads.random_dense(B, Hq, Hkv, Nq, Nkv, D, dtype, seed=seed)
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dO"))
     scale = 1.0 / math.sqrt(D)
     o, lse = api.fwd(q, k, v, causal, scale)
-    small = torch.empty(api.bwd_workspace_bytes(q, k), dtype=torch.uint8, device="cuda")
+    small_n = api.bwd_workspace_bytes(q, k)
     big_n = api.bwd_workspace_bytes(q, k, causal)
-    assert big_n > small.numel(), "the stored-dS path applies to this problem"
+    one = tile_buffer_bytes(q, k)
+    assert big_n >= small_n + 2 * one, "the stored-tile path applies to this problem"
+    small = torch.empty(small_n, dtype=torch.uint8, device="cuda")
+    ds_only = torch.empty(small_n + one, dtype=torch.uint8, device="cuda")
     big = torch.empty(big_n, dtype=torch.uint8, device="cuda")
     g_small = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=small)
+    g_ds = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=ds_only)
     g_big = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=big)
     api.get_status()
     ref = oracle.attention_bwd(inp["q"], inp["k"], inp["v"], inp["dO"], causal, scale)
-    for gs in (g_small, g_big):
+    for gs in (g_small, g_ds, g_big):
         for name, got, r in zip(("dQ", "dK", "dV"), gs, ref):
             check_grad(got, r, name)
-    # dV is the same kernel either way; dK too, except that causal storing starts
-    # at an even query tile (an extra all-masked tile shifts its summation order)
-    assert torch.equal(g_small[2], g_big[2])
+    assert torch.equal(g_small[2], g_ds[2])
+    assert torch.equal(g_ds[1], g_big[1])
     if not causal:
-        assert torch.equal(g_small[1], g_big[1])
-    return inp, (q, k, v, do, o, lse, scale, big), g_big
+        assert torch.equal(g_small[1], g_ds[1])
+    return inp, (q, k, v, do, o, lse, scale, big, ds_only), g_big, g_ds
 
 
 @pytest.mark.parametrize("D", [256, 512])
@@ -66,13 +81,37 @@ def test_stored_ds_backward_gqa_fp16():
 
 def test_stage_bit_4_replays_the_gemm_on_the_stored_ds():
     # preprocess, dK (stores dS), then bit 4 alone: the same dQ as the full call
-    inp, (q, k, v, do, o, lse, scale, big), (dq_full, _, _) = run_both(1, 4, 2, 512, 512, 512, seed=5)
+    # with room for dS only (dK computes S^T, as it does without bit 5)
+    inp, (q, k, v, do, o, lse, scale, big, ds_only), _, (dq_full, _, _) = run_both(1, 4, 2, 512, 512, 512, seed=5)
     dq = torch.empty_like(q)
     dk, dv = torch.empty_like(k), torch.empty_like(v)
     for bit in (1, 8, 16):
-        api.bwd(q, k, v, o, lse, do, False, scale, workspace=big, dq=dq, dk=dk, dv=dv, stages=bit)
+        api.bwd(q, k, v, o, lse, do, False, scale, workspace=ds_only, dq=dq, dk=dk, dv=dv, stages=bit)
     api.get_status()
     assert torch.equal(dq, dq_full)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_stage_bit_5_splits_the_stored_p_launches(causal):
+    # preprocess, dK storing P and dS, then the dV and dQ GEMMs: the same
+    # gradients as the full call, launch by launch
+    inp, (q, k, v, do, o, lse, scale, big, _), g_full, _ = run_both(1, 4, 2, 640, 384, 512, seed=7, causal=causal)
+    dq = torch.empty_like(q)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    for bits in (1, 8 | 32, 2 | 32, 16):
+        api.bwd(q, k, v, o, lse, do, causal, scale, workspace=big, dq=dq, dk=dk, dv=dv, stages=bits)
+    api.get_status()
+    for got, want in zip((dq, dk, dv), g_full):
+        assert torch.equal(got, want)
+
+
+def test_stage_bit_5_needs_the_p_buffer():
+    q = torch.zeros(1, 2, 256, 512, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros_like(q)
+    lse = torch.zeros(1, 2, 256, dtype=torch.float32, device="cuda")
+    ds_only = torch.empty(api.bwd_workspace_bytes(q, q) + tile_buffer_bytes(q, q), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError, match="stage bit 5"):
+        api.bwd(q, q, q, o, lse, o, False, 0.05, workspace=ds_only, stages=1 | 8 | 32)
 
 
 @pytest.mark.parametrize("Nq,Nkv", [(300, 300), (256, 700), (700, 256), (100, 1000), (513, 769)])

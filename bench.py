@@ -206,15 +206,16 @@ PAIR_SOURCES = ("xchg.cu", "xchg2.cu", "ptx.cuh", "tile_common.cuh", "kernels.h"
 DECODE_SOURCES = ("decode.cu", "ptx.cuh", "tile_common.cuh", "kernels.h")
 FP8_SOURCES = ("xchg2.cu", "fp8.cu", "ptx.cuh", "tile_common.cuh", "kernels.h", "host.cu")
 TRAFFIC = {
-    # dK (also storing dS) at 16 heads (755,625,472 + 2,224,594,944 bytes) scaled to 32
-    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 5960440832, "files": PAIR_SOURCES, "sources": "941e97ce961b0808"},
+    # dK (also storing P^T and dS^T) at 16 heads (764,000,768 + 4,367,750,144 bytes) scaled to 32
+    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 10263501824, "files": PAIR_SOURCES,
+                                             "sources": "2e8a8fae1772c025"},
     # one ffpa_decode_fwd call: split kernel + combine (means over six calls)
-    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2156691499, "files": DECODE_SOURCES,
-                                                                "sources": "a0c6fdf25a78af69"},
+    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2156703957, "files": DECODE_SOURCES,
+                                                                "sources": "452646d840e0c29f"},
     # the e4m3 attention kernel (reads q8, k8, V^T codes; writes O, LSE)
-    ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 638806886,
+    ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 638421043,
                                                                              "files": FP8_SOURCES,
-                                                                             "sources": "3b44daad1b48656f"},
+                                                                             "sources": "32d8ddba290d320a"},
 }
 
 

@@ -711,40 +711,75 @@ def run_ours(args):
 
 def measure_e2e(w, args, dev, stream, inp, step_flops, world):
     """Same metric through the public API with pinned host buffers: every step
-    copies q, k, v, dO host->device and reads dq, dk, dv back."""
+    copies q, k, v, dO host->device and reads dq, dk, dv back.
+
+    The copies run as a training loop runs them: on two copy streams, into
+    two device input buffers, so that step i+1's inputs move in and step i's
+    gradients move out while the GPU computes (the C2C link is full duplex).
+    The timed region starts before the first input copy and ends after the
+    last gradient copy."""
     import torch
 
     from head_dim_flash_gb300 import api
 
     host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "dO")}
-    dev_t = {n: torch.empty_like(host[n], device=dev) for n in host}
+    bufs = [{n: torch.empty_like(host[n], device=dev) for n in host} for _ in range(2)]
     out_h = {n: torch.empty(inp[src].shape, dtype=inp[src].dtype).pin_memory()
              for n, src in (("dq", "q"), ("dk", "k"), ("dv", "v"))}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]  # inputs of buffer b landed
+    buf_free = [None, None]                            # last step that read buffer b is done
 
-    def step():
-        for n in host:
-            dev_t[n].copy_(host[n], non_blocking=True)
-        o, lse = api.fwd(dev_t["q"], dev_t["k"], dev_t["v"], w.causal, w.scale)
-        dq, dk, dv = api.bwd(dev_t["q"], dev_t["k"], dev_t["v"], o, lse, dev_t["dO"], w.causal, w.scale)
-        out_h["dq"].copy_(dq, non_blocking=True)
-        out_h["dk"].copy_(dk, non_blocking=True)
-        out_h["dv"].copy_(dv, non_blocking=True)
+    def copy_in(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if buf_free[b] is not None:
+                s_in.wait_event(buf_free[b])
+            for n in host:
+                bufs[b][n].copy_(host[n], non_blocking=True)
+            in_ready[b].record(s_in)
 
-    for _ in range(2):
-        step()
+    def compute(i):
+        b = i % 2
+        x = bufs[b]
+        stream.wait_event(in_ready[b])
+        o, lse = api.fwd(x["q"], x["k"], x["v"], w.causal, w.scale)
+        grads = api.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], w.causal, w.scale)
+        done = torch.cuda.Event()
+        done.record(stream)
+        buf_free[b] = done
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            for n, g in zip(("dq", "dk", "dv"), grads):
+                g.record_stream(s_out)  # not reused before the copy has read it
+                out_h[n].copy_(g, non_blocking=True)
+
+    def run(n, start=None):
+        if start is not None:
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            compute(i)
+        stream.wait_stream(s_out)
+
+    run(2)
     torch.cuda.synchronize()
-    n = max(1, min(args.steps, 5))
+    n = max(1, min(args.steps, 10))
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
-    for _ in range(n):
-        step()
+    run(n, start=s)
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / n
     return {"value": world * step_flops / (ms / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": "double-buffered inputs; copies on two side streams overlap the compute of the "
+                       "neighbouring steps; first copy-in and last copy-out inside the timed region"}
 
 
 def main():

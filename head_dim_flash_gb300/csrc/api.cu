@@ -228,23 +228,10 @@ ffpa_status run_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, 
     if (!any) return ok();
     ffpa::BwdArgs a{};
     a.pb = pb;
-    FFPA_TRY(device_ctl(&a.ctl));
-    a.bf16 = dt == FFPA_BF16;
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.o = o;
-    a.dO = dO;
-    a.lse = lse;
-    a.dq = dq;
-    a.dk = dk;
-    a.dv = dv;
-    a.delta = static_cast<float*>(workspace);
-    a.lse_log2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + need / 2);
     a.stages = stages & 63u;
-    // a workspace with room for dS^T after the row statistics selects the dQ
-    // GEMM from the dS that the dK launch stores (where that path applies);
-    // room for P^T after it as well, the dK launch that reads the P of dV
+    // a workspace with room for dS^T after the row statistics has the dK launch
+    // store dS and dQ formed by a GEMM over it (where that path applies); room
+    // for P^T after that as well has it store P^T and dV formed the same way
     a.ds = nullptr;
     a.p = nullptr;
     if (ffpa::dsq_supported(pb) && workspace_bytes >= need + ffpa::dsq_ds_bytes(pb)) {
@@ -258,6 +245,19 @@ ffpa_status run_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, 
     if ((a.stages & 32u) && a.p == nullptr)
         return fail(FFPA_ERR_INVALID_VALUE, "stage bit 5 (stored P) needs the workspace of "
                                             "ffpa_bwd_workspace_bytes_ds on a dense D = 256 / 512 problem");
+    FFPA_TRY(device_ctl(&a.ctl));
+    a.bf16 = dt == FFPA_BF16;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.dO = dO;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.delta = static_cast<float*>(workspace);
+    a.lse_log2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + need / 2);
     return launch_result(ffpa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)), "backward launch");
 }
 

@@ -104,6 +104,27 @@ def test_workspace_size_and_checks(lib):
     assert lib.ffpa_varlen_bwd_workspace_bytes(0, 2, 100, 100, 60, 60, 4, 2, 512) >= 2 * 4 * 100 * 4
 
 
+def test_stored_tile_workspace_and_stage_bits(lib):
+    # dense D = 512: row statistics, then dS^T, then P^T at the next 256-byte boundary
+    B, Hq, Hkv, Nq, Nkv, D = 1, 4, 2, 300, 200, 512
+    small = lib.ffpa_bwd_workspace_bytes(0, B, Hq, Hkv, Nq, Nkv, D)
+    tile = B * Hq * Nkv * ((Nq + 7) // 8 * 8) * 2
+    big = lib.ffpa_bwd_workspace_bytes_ds(0, B, Hq, Hkv, Nq, Nkv, D, 1)
+    assert big == small + (tile + 255) // 256 * 256 + tile
+    # head dims outside the path keep the small workspace
+    assert lib.ffpa_bwd_workspace_bytes_ds(0, B, Hq, Hkv, Nq, Nkv, 320, 0) == lib.ffpa_bwd_workspace_bytes(
+        0, B, Hq, Hkv, Nq, Nkv, 320)
+    ptrs = [FAKE] * 9  # q, k, v, o, lse, dO, dq, dk, dv
+
+    def stages(ws_bytes, bits):
+        return lib.ffpa_bwd_stages(0, *ptrs, FAKE, ws_bytes, B, Hq, Hkv, Nq, Nkv, D, 0, 0.05, bits, None)
+
+    assert stages(big, 64) == 1 and "bits 0..5" in lib.ffpa_last_error().decode()
+    assert stages(small, 16) == 1 and "stage bit 4" in lib.ffpa_last_error().decode()
+    assert stages(small + tile, 1 | 8 | 32) == 1 and "stage bit 5" in lib.ffpa_last_error().decode()
+    assert stages(small, 2 | 32) == 1 and "stage bit 5" in lib.ffpa_last_error().decode()
+
+
 def test_varlen_requires_both_cu_seqlens(lib):
     st = lib.ffpa_varlen_fwd(0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 10, 10, 5, 5, 4, 2, 512, 0, 0.05, None)
     assert st == 1

@@ -12,9 +12,9 @@
 //   dQ         : per query tile, over key tiles: dS = P (dO V^T - delta),
 //                dQ += scale * dS K
 // The three gradient launches run the cluster-exchange kernel (xchg.cu). With
-// room in the workspace (dense, D = 256 / 512), the dK launch also stores its
-// P^T and dS^T tiles, and dV = P^T dO and dQ = scale dS K become plain GEMMs
-// over them (dsq.cu): preprocess, dK, dV, dQ.
+// room in the workspace (dense, D a multiple of 128 up to 768), the dK launch
+// also stores its P^T and dS^T tiles, and dV = P^T dO and dQ = scale dS K
+// become plain GEMMs over them (dsq.cu): preprocess, dK, dV, dQ.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tile_common.cuh"
@@ -107,7 +107,7 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
     // one before, so it fills the SMs that the previous one's last wave leaves
     // idle (the first waits for the preprocess as usual; the later ones start
     // only once all of its CTAs have started, hence after the preprocess).
-    // Stored tiles (dense, D = 256 / 512, the buffers given; only the CTA-pair
+    // Stored tiles (dense, D % 128 == 0 up to 768, the buffers given; only the CTA-pair
     // dK kernel stores them):
     //  - dS: the dK launch also writes dS^T into a.ds and dQ is a plain GEMM
     //    over it; stage bit 4 runs that GEMM alone on a buffer an earlier dK

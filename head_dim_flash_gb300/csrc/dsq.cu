@@ -9,8 +9,10 @@
 // queries contiguous), tile by tile; masked entries are stored zeros, and
 // under the bottom-right causal mask every tile that holds a legal entry is
 // stored. A CTA pair owns 256 output rows (128 per CTA, in its TMEM lanes)
-// and the whole head dim (D <= 512 fp32 columns of TMEM); a ring of 4 stages
-// feeds M=256, N=256 pair MMAs, acc[:, 256 j ..] += A B_j:
+// and one slab of at most 512 head-dim columns (fp32 in TMEM; D > 512 takes
+// two pairs, each reading the stored tiles); a ring of 4 stages feeds M=256,
+// N=256 pair MMAs (the last one N=128 for a slab of 128, 384 or 640 columns),
+// acc[:, 256 j ..] += A B_j:
 //   dQ = scale dS K (rows = queries of one head; causal grids take the
 //       longest tiles, the last ones, first). K runs over keys in blocks of
 //       64, up to the last key any row of the pair may see.
@@ -46,8 +48,8 @@ struct __align__(1024) QStatic {
 static_assert(sizeof(QStatic) == 1024, "static shared block must be exactly 1 KiB");
 
 struct QGeo {
-    int nj;           // N = 256 pair MMAs across the head dim (D / 256)
-    int stage_bytes;  // per CTA: A (16 KiB) + B (nj x 16 KiB)
+    int nj_max;       // pair MMAs (N = 256, the last one of a slab N = 128 if it is narrower) of the widest slab
+    int stage_bytes;  // ring slot per CTA: A (16 KiB) + B (nj_max x 16 KiB)
 };
 
 template <bool BF16, bool DV>
@@ -81,7 +83,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
         n_kb = key_end > 0 ? (key_end + 63) / 64 : 0;
     }
     const int n_it = DV ? G * n_kb : n_kb;  // K iterations
-    const int tcols = gm.nj * 256;
+    // the pair's head-dim slab: columns [c0, c0 + w), w <= 512, as nj MMAs of N = 256
+    // (the last N = last_n = 128 when w is an odd multiple of 128)
+    const int c0 = static_cast<int>(blockIdx.x >> 1) * 512;
+    const int w = min(512, pb.D - c0);
+    const int nj = (w + 255) / 256;
+    const int last_n = w - (nj - 1) * 256;
+    const int tx_bytes = 16384 * (1 + nj);  // bytes one CTA loads per K block
+    auto n_of = [&](int j) { return j == nj - 1 ? last_n : 256; };
+    const int tcols = gm.nj_max * 256;
 
     __shared__ QStatic sh;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -99,7 +109,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         sh.abort_flag = 0;
         // the even rank's full barriers count both CTAs' bytes
         if (leader)
-            for (int i = 0; i < kQStages; ++i) mbar_arrive_expect_tx(&sh.full[i], 2 * gm.stage_bytes);
+            for (int i = 0; i < kQStages; ++i) mbar_arrive_expect_tx(&sh.full[i], 2 * tx_bytes);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -138,9 +148,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
                         // A: P^T rows = my 128 keys, queries [i0, +64)
                         tma_load_4d_pair(st, &tA, fb, i0, rc, hq, b);
                     } else {
-                        // B: dO rows = queries [i0, +64), my 128 columns of each 256-column half
-                        for (int j = 0; j < gm.nj; ++j)
-                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, i0, (j * 256 + rh * 128) / 64, hq, b);
+                        // B: dO rows = queries [i0, +64), my half of each MMA's N columns
+                        // (a 128-column box; an N = 128 MMA reads its first 64)
+                        for (int j = 0; j < nj; ++j)
+                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, i0, (c0 + j * 256 + rh * n_of(j) / 2) / 64,
+                                             hq, b);
                     }
                 } else {
                     const int kb = it;
@@ -149,10 +161,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
                         tma_load_4d_pair(st, &tA, fb, rc, kb * 64, h, b);
                         tma_load_4d_pair(st + 8192, &tA, fb, rc + 64, kb * 64, h, b);
                     } else {
-                        // B: K rows = keys [64 kb, +64), my 128 columns of each 256-column half
-                        for (int j = 0; j < gm.nj; ++j)
-                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, kb * 64, (j * 256 + rh * 128) / 64, hk,
-                                             b);
+                        // B: K rows = keys [64 kb, +64), my half of each MMA's N columns
+                        for (int j = 0; j < nj; ++j)
+                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, kb * 64,
+                                             (c0 + j * 256 + rh * n_of(j) / 2) / 64, hk, b);
                     }
                 }
                 rp.advance(kQStages);
@@ -173,10 +185,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (leader && elect_one()) {
             // A: MN-major dS (dQ) or K-major P^T (dV); B: MN-major
             const uint32_t idesc = idesc_f16(256, 256, BF16, !DV, true);
+            const uint32_t idesc_n128 = idesc_f16(256, 128, BF16, !DV, true);
             RingPos rp;
             for (int it = 0; it < n_it; ++it) {
                 if (!mbar_wait_cluster(&sh.full[rp.slot], rp.phase, abort_flag, status, lim, QS_RING)) break;
-                mbar_arrive_expect_tx(&sh.full[rp.slot], 2 * gm.stage_bytes);  // arm the slot's next fill
+                mbar_arrive_expect_tx(&sh.full[rp.slot], 2 * tx_bytes);  // arm the slot's next fill
                 tc_fence_after();
                 const uint8_t* st = smem + rp.slot * gm.stage_bytes;
 #pragma unroll
@@ -186,9 +199,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
                     // K-major A (dV): 32 bytes into each of the 128 rows of the box
                     const uint64_t ad = DV ? sdesc_sw128(smem_u32(st + kk * 32), 16, 1024)
                                            : sdesc_sw128(smem_u32(st + kk * 2048), 8192, 1024);
-                    for (int j = 0; j < gm.nj; ++j) {
+                    for (int j = 0; j < nj; ++j) {
                         const uint64_t bd = sdesc_sw128(smem_u32(st + 16384 * (1 + j) + kk * 2048), 8192, 1024);
-                        umma_f16_pair(tmem + j * 256, ad, bd, idesc, (it | kk) != 0);
+                        umma_f16_pair(tmem + j * 256, ad, bd, n_of(j) == 256 ? idesc : idesc_n128, (it | kk) != 0);
                     }
                 }
                 umma_commit_pair_multicast(&sh.empty[rp.slot], pair_mask);
@@ -209,8 +222,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const float mul = n_it > 0 ? (DV ? 1.f : pb.scale) : 0.f;
             const View& vo = DV ? pb.vdv : pb.vdq;
             uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + static_cast<size_t>(b) * vo.sb +
-                            static_cast<size_t>(h) * vo.sh + static_cast<size_t>(q) * vo.sn;
-            for (int cc = 0; cc < pb.D; cc += 32) {
+                            static_cast<size_t>(h) * vo.sh + static_cast<size_t>(q) * vo.sn + c0;
+            for (int cc = 0; cc < w; cc += 32) {
                 uint32_t v[32];
                 if (n_it > 0) {
                     tmem_ld32(tmem + lane_off + cc, v);
@@ -247,7 +260,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 bool dsq_supported(const Problem& pb)
 {
-    return !pb.varlen && (pb.D == 256 || pb.D == 512) && pb.Nq > 0 && pb.Nkv > 0;
+    // the head dims of the CTA-pair kernels, which store the tiles
+    return !pb.varlen && pb.D % 128 == 0 && pb.D <= 768 && pb.Nq > 0 && pb.Nkv > 0;
 }
 
 size_t dsq_ds_bytes(const Problem& pb)
@@ -285,10 +299,12 @@ cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s)
                                 make_slab_map(&tB, a.rhs, pb, true, a.bf16, 64, 2, pb.vk);
     if (!okm) return cudaErrorInvalidValue;
     QGeo gm{};
-    gm.nj = pb.D / 256;
-    gm.stage_bytes = 16384 * (1 + gm.nj);
+    gm.nj_max = (min(pb.D, 512) + 255) / 256;
+    gm.stage_bytes = 16384 * (1 + gm.nj_max);
+    const int n_slab = (pb.D + 511) / 512;
     const int smem = kQStages * gm.stage_bytes;
-    const dim3 grid = a.dv ? dim3(2, (pb.Nkv + 255) / 256, pb.B * pb.Hkv) : dim3(2, (pb.Nq + 255) / 256, pb.B * pb.Hq);
+    const dim3 grid = a.dv ? dim3(2 * n_slab, (pb.Nkv + 255) / 256, pb.B * pb.Hkv)
+                           : dim3(2 * n_slab, (pb.Nq + 255) / 256, pb.B * pb.Hq);
     if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
     auto kern = a.dv ? (a.bf16 ? dsq_kernel<true, true> : dsq_kernel<false, true>)
                      : (a.bf16 ? dsq_kernel<true, false> : dsq_kernel<false, false>);

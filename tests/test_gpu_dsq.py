@@ -1,4 +1,5 @@
-"""GPU parity of the stored-tile backward (dense, D = 256 / 512, causal or not):
+"""GPU parity of the stored-tile backward (dense, D a multiple of 128 up to 768,
+causal or not):
 the dK launch also writes dS^T to the workspace and dQ = scale dS K is one
 GEMM; with room for P^T as well, the dK launch also writes P^T and
 dV = P^T dO is one GEMM instead of a launch that recomputes S^T.
@@ -75,6 +76,17 @@ def test_stored_ds_backward(D, Nq, Nkv):
     run_both(1, 2, 2, Nq, Nkv, D, seed=Nq + D)
 
 
+@pytest.mark.parametrize("D", [128, 384, 640, 768])
+def test_stored_tile_backward_other_head_dims(D):
+    # slabs of 128 / 384 / 640 columns end in an N = 128 MMA; D > 512 takes two
+    # slabs per row tile
+    run_both(1, 2, 1, 300, 333, D, dtype=torch.float16, seed=D)
+
+
+def test_stored_tile_backward_other_head_dims_causal():
+    run_both(1, 2, 2, 400, 300, 640, seed=11, causal=True)
+
+
 def test_stored_ds_backward_gqa_fp16():
     run_both(2, 8, 2, 300, 520, 512, dtype=torch.float16, seed=3)
 
@@ -122,11 +134,12 @@ def test_stored_ds_backward_causal(Nq, Nkv):
 
 
 def test_varlen_and_other_head_dims_keep_the_recompute_path():
-    q = torch.zeros(1, 2, 64, 320, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(1, 2, 64, 320, dtype=torch.bfloat16, device="cuda")
-    assert api.bwd_workspace_bytes(q, k, True) == api.bwd_workspace_bytes(q, k)
-    q5 = torch.zeros(1, 2, 64, 512, dtype=torch.bfloat16, device="cuda")
-    assert api.bwd_workspace_bytes(q5, q5, True) > api.bwd_workspace_bytes(q5, q5)
+    for D in (320, 896, 1024):
+        q = torch.zeros(1, 2, 64, D, dtype=torch.bfloat16, device="cuda")
+        assert api.bwd_workspace_bytes(q, q, True) == api.bwd_workspace_bytes(q, q)
+    for D in (128, 512, 768):
+        q5 = torch.zeros(1, 2, 64, D, dtype=torch.bfloat16, device="cuda")
+        assert api.bwd_workspace_bytes(q5, q5, True) > api.bwd_workspace_bytes(q5, q5)
 
 
 def test_one_cta_family_forced_keeps_the_recompute_path(monkeypatch):

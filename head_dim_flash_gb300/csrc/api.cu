@@ -241,10 +241,10 @@ ffpa_status run_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, 
     }
     if ((a.stages & 16u) && a.ds == nullptr)
         return fail(FFPA_ERR_INVALID_VALUE, "stage bit 4 (dQ from stored dS) needs the larger workspace of "
-                                            "ffpa_bwd_workspace_bytes_ds on a dense problem with D % 128 == 0, D <= 768");
+                                            "ffpa_bwd_workspace_bytes_ds on a dense problem with D % 64 == 0, D <= 1024");
     if ((a.stages & 32u) && a.p == nullptr)
         return fail(FFPA_ERR_INVALID_VALUE, "stage bit 5 (stored P) needs the workspace of "
-                                            "ffpa_bwd_workspace_bytes_ds on a dense problem with D % 128 == 0, D <= 768");
+                                            "ffpa_bwd_workspace_bytes_ds on a dense problem with D % 64 == 0, D <= 1024");
     FFPA_TRY(device_ctl(&a.ctl));
     a.bf16 = dt == FFPA_BF16;
     a.q = q;

@@ -12,7 +12,7 @@
 //   dQ         : per query tile, over key tiles: dS = P (dO V^T - delta),
 //                dQ += scale * dS K
 // The three gradient launches run the cluster-exchange kernel (xchg.cu). With
-// room in the workspace (dense, D a multiple of 128 up to 768), the dK launch
+// room in the workspace (dense, D a multiple of 64 up to 1024), the dK launch
 // also stores its P^T and dS^T tiles, and dV = P^T dO and dQ = scale dS K
 // become plain GEMMs over them (dsq.cu): preprocess, dK, dV, dQ.
 #include "kernels.h"
@@ -107,14 +107,14 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
     // one before, so it fills the SMs that the previous one's last wave leaves
     // idle (the first waits for the preprocess as usual; the later ones start
     // only once all of its CTAs have started, hence after the preprocess).
-    // Stored tiles (dense, D % 128 == 0 up to 768, the buffers given; only the CTA-pair
-    // dK kernel stores them):
+    // Stored tiles (dense, D % 64 == 0 up to 1024, the buffers given; the dK
+    // kernels of both families store them):
     //  - dS: the dK launch also writes dS^T into a.ds and dQ is a plain GEMM
     //    over it; stage bit 4 runs that GEMM alone on a buffer an earlier dK
     //    launch filled;
     //  - P: with dV and dK in one call, or stage bit 5, the dK launch also
     //    writes P^T into a.p and dV is a plain GEMM over it, after dK.
-    const bool use_ds = a.ds != nullptr && !q_empty && !kv_empty && dsq_supported(pb) && xchg_uses_pair(pb);
+    const bool use_ds = a.ds != nullptr && !q_empty && !kv_empty && dsq_supported(pb);
     if ((a.stages & 16u) && !use_ds) return cudaErrorInvalidConfiguration;  // no stored dS to read
     const bool use_p = use_ds && a.p != nullptr;
     if ((a.stages & 32u) && !use_p) return cudaErrorInvalidConfiguration;  // no P buffer

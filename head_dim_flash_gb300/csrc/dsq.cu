@@ -11,8 +11,8 @@
 // stored. A CTA pair owns 256 output rows (128 per CTA, in its TMEM lanes)
 // and one slab of at most 512 head-dim columns (fp32 in TMEM; D > 512 takes
 // two pairs, each reading the stored tiles); a ring of 4 stages feeds M=256,
-// N=256 pair MMAs (the last one N=128 for a slab of 128, 384 or 640 columns),
-// acc[:, 256 j ..] += A B_j:
+// N=256 pair MMAs (the last one N=128 when the slab ends 64 or 128 columns
+// past a multiple of 256), acc[:, 256 j ..] += A B_j:
 //   dQ = scale dS K (rows = queries of one head; causal grids take the
 //       longest tiles, the last ones, first). K runs over keys in blocks of
 //       64, up to the last key any row of the pair may see.
@@ -83,12 +83,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
         n_kb = key_end > 0 ? (key_end + 63) / 64 : 0;
     }
     const int n_it = DV ? G * n_kb : n_kb;  // K iterations
-    // the pair's head-dim slab: columns [c0, c0 + w), w <= 512, as nj MMAs of N = 256
-    // (the last N = last_n = 128 when w is an odd multiple of 128)
+    // the pair's head-dim slab: columns [c0, c0 + w), w <= 512, as nj MMAs of N = 256;
+    // the last one N = last_n, the rest of the slab rounded up to 128 (columns past
+    // D are loaded as zeros and not stored)
     const int c0 = static_cast<int>(blockIdx.x >> 1) * 512;
     const int w = min(512, pb.D - c0);
     const int nj = (w + 255) / 256;
-    const int last_n = w - (nj - 1) * 256;
+    const int last_n = (w - (nj - 1) * 256 + 127) / 128 * 128;
     const int tx_bytes = 16384 * (1 + nj);  // bytes one CTA loads per K block
     auto n_of = [&](int j) { return j == nj - 1 ? last_n : 256; };
     const int tcols = gm.nj_max * 256;
@@ -260,8 +261,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 bool dsq_supported(const Problem& pb)
 {
-    // the head dims of the CTA-pair kernels, which store the tiles
-    return !pb.varlen && pb.D % 128 == 0 && pb.D <= 768 && pb.Nq > 0 && pb.Nkv > 0;
+    // whole 64-column chunks (the 5-D operand maps), at most two 512-column slabs
+    return !pb.varlen && pb.D % 64 == 0 && pb.D <= 1024 && pb.Nq > 0 && pb.Nkv > 0;
 }
 
 size_t dsq_ds_bytes(const Problem& pb)

@@ -92,7 +92,7 @@ struct XArgs {
     void* p;
 };
 
-// The GEMMs over the tiles the dK kernel stored (dense, D a multiple of 128 up to 768;
+// The GEMMs over the tiles the dK kernel stored (dense, D a multiple of 64 up to 1024;
 // dsq_ds_bytes is the size of one [B, Hq, Nkv, ldq] tile buffer):
 //   dv = 0: dQ = scale * dS K from the stored dS^T;
 //   dv = 1: dV = P^T dO from the stored P^T, over the query heads of the group.

@@ -72,6 +72,8 @@ struct __align__(1024) StaticSmem {
     uint64_t zpeer[kMaxC], slot_free[kMaxC], stat[2], rmax[2], lsum, drain, half;
     uint32_t tmem_base;
     int abort_flag;
+    // dK storing tiles: the own slot holds P^T / its store read it; the dS store read it
+    uint64_t p_full, p_read, stored;
 };
 static_assert(sizeof(StaticSmem) == 1024, "static shared block must be exactly 1 KiB");
 
@@ -90,7 +92,8 @@ template <int OP, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     xchg_kernel(const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tA2,
                 const __grid_constant__ CUtensorMap tB1, const __grid_constant__ CUtensorMap tB2,
-                const __grid_constant__ CUtensorMap tW, const XArgs a, const Geo gm)
+                const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tS,
+                const __grid_constant__ CUtensorMap tP, const XArgs a, const Geo gm)
 {
     // the next GEMM kernel of a backward may take SMs as this grid's last CTAs start
     pdl_trigger();
@@ -146,7 +149,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             n_ct = kmax < 0 ? 0 : min(n_ct, kmax / 128 + 1);
         }
     } else {
-        if (pb.causal) m_start = max(0, r0 - off) / 128;
+        if (pb.causal) {
+            // dK storing tiles starts where the 256-key tile that holds my rows
+            // starts, at an even query tile: every tile a GEMM tile of the stored-tile
+            // GEMMs reads is then written (the extra tiles are fully masked: zeros)
+            const bool st = OP == XOP_DK && (a.store_ds || a.store_p);
+            m_start = max(0, (st ? (r0 & ~255) : r0) - off) / 128;
+            if (st) m_start &= ~1;
+        }
         n_mt = max(0, (lq + 127) / 128 - m_start);
         n_ct = G * n_mt;
     }
@@ -207,6 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bar_lsum, 1);
         mbar_init(&bar_drain, 1);
+        mbar_init(&sh.p_full, 256);
+        mbar_init(&sh.p_read, 1);
+        mbar_init(&sh.stored, 1);
         sh.abort_flag = 0;
         // Peers deliver with st.async, completing bytes on these barriers; each is
         // armed (one arrival + expected bytes) by its receiver before any peer can
@@ -457,6 +470,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l_part = 0.f;  // forward softmax state (l over my columns of own tiles)
         bool ok = true;
         auto warp_ok = [&](bool v) { return __all_sync(0xffffffffu, v); };
+        // dK storing dS^T / P^T tiles ([B, Hq, Nkv, ldq]): thread ew == 0 stores the
+        // own slot with two TMA stores (evict-first: later launches read them)
+        const bool st_ds = OP == XOP_DK && a.store_ds != 0;
+        const bool st_p = OP == XOP_DK && a.store_p != 0;
+        const uint64_t pol = (ew == 0 && (st_ds || st_p)) ? l2_policy_evict_first() : 0;
         for (int s = 0; s < n_steps; ++s) {
             const int t = s * C + c;
             const int sb = T::kXdb ? (s & 1) : 0;
@@ -491,12 +509,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            // Peers' slots for this step are free once their previous value MMAs ran.
-            auto wait_slots = [&]() -> bool {
-                if (C == 1 || s == 0) return true;
-                bool got = true;
+            // The own slot may be rewritten once the previous step's value MMAs here
+            // (acc) and every peer (slot_free: it consumed our copy, so the copy has
+            // read the slot) are done with it, and (dK storing dS) the store of the
+            // previous step's dS^T has read it.
+            auto own_free = [&]() -> bool {
+                if (s == 0) return true;
+                bool got = mbar_wait(&bar_acc, (s - 1) & 1, abort_flag, status, lim, XS_ACC);
                 for (int p = 0; p < C && got; ++p)
                     if (p != c) got = mbar_wait_cluster(&bar_slot_free[p], (s - 1) & 1, abort_flag, status, lim, XS_SLOT);
+                if (got && st_ds) got = mbar_wait(&sh.stored, (s - 1) & 1, abort_flag, status, lim, XS_ZFULL);
                 return warp_ok(got);
             };
             uint32_t z[32];  // my 64 columns of Z as packed pairs
@@ -609,6 +631,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool full = j_lo <= col0 && j_hi >= col0 + 64;
                 const float* s_l2 = stats + sbuf * 128;
                 const float* s_dl = stats + 256 + sbuf * 128;
+                if (OP == XOP_DK && st_p) {
+                    // dK storing P: P^T (input dtype) goes through the own slot first;
+                    // its store runs while dS^T is formed, then dS^T replaces it
+                    uint32_t pp[32];  // P of my 64 columns as fp16 pairs
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t x[32];
+                        tmem_ld32(tx + col0 + q2 * 32, x);
+                        tmem_ld_wait(x);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            float pv[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int j = col0 + q2 * 32 + 2 * e + u;
+                                const bool legal = full || (j >= j_lo && j < j_hi);
+                                pv[u] = legal ? ex2_approx(fmaf(__uint_as_float(x[2 * e + u]), c2, -s_l2[j])) : 0.f;
+                            }
+                            pp[q2 * 16 + e] = pack2<false>(pv[0], pv[1]);
+                        }
+                    }
+                    if (!own_free()) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 pv = unpack2<false>(pp[4 * u + e]);
+                            w4[e] = pack2<BF16>(pv.x, pv.y);
+                        }
+                        *reinterpret_cast<uint4*>(sZown + half * 16384 + sw128_offset(r, u)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&sh.p_full);
+                    if (ew == 0) {
+                        // all 256 threads wrote it: store it, and report once the store read it
+                        if (mbar_wait(&sh.p_full, s & 1, abort_flag, status, lim, XS_ZFULL)) {
+                            if (t < n_ct) {
+                                tma_store_4d_hint(&tP, sZown, col_row0(t), row_co(r0), col_head(t), bco, pol);
+                                tma_store_4d_hint(&tP, sZown + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco,
+                                                  pol);
+                                bulk_commit_group();
+                                bulk_wait_read_all();
+                            }
+                            mbar_arrive(&sh.p_read);
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t y[32];
+                        tmem_ld32(ty + col0 + q2 * 32, y);
+                        tmem_ld_wait(y);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = col0 + q2 * 32 + 2 * e;
+                            const float2 pv = unpack2<false>(pp[q2 * 16 + e]);
+                            z[q2 * 16 + e] = pack2<BF16>(pv.x * (__uint_as_float(y[2 * e]) - s_dl[j]),
+                                                         pv.y * (__uint_as_float(y[2 * e + 1]) - s_dl[j + 1]));
+                        }
+                    }
+                } else {
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
                     uint32_t x[32], y[32];
@@ -637,18 +725,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         z[q2 * 16 + e] = pack2<BF16>(zz[0], zz[1]);
                     }
                 }
+                }
             }
             // X (and Y) are read: the next score products into this buffer may start
             tc_fence_before();
             mbar_arrive(&bar_x_free[sb]);
-            // The own slot may be rewritten once the previous step's value MMAs here
-            // (acc) and every peer (slot_free: it consumed our copy, so the copy has
-            // read the slot) are done with it.
-            if (s > 0 && !warp_ok(mbar_wait(&bar_acc, (s - 1) & 1, abort_flag, status, lim, XS_ACC))) {
-                ok = false;
-                break;
-            }
-            if (!wait_slots()) {
+            if (OP == XOP_DK && st_p) {
+                // the P^T written to the own slot has been read by its store
+                if (!warp_ok(mbar_wait(&sh.p_read, s & 1, abort_flag, status, lim, XS_ZFULL))) {
+                    ok = false;
+                    break;
+                }
+            } else if (!own_free()) {
                 ok = false;
                 break;
             }
@@ -658,19 +746,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(z[4 * u], z[4 * u + 1], z[4 * u + 2], z[4 * u + 3]);
             fence_proxy_async_smem();
             mbar_arrive(&bar_z_full);
-            if (C > 1 && ew == 0) {
+            if ((C > 1 || st_ds) && ew == 0) {
                 // one bulk copy of the whole slot into every peer, once all 256 threads
                 // have written it (on a time-out the copies are skipped; the abort flag
-                // then ends every wait of this CTA and of its peers)
+                // then ends every wait of this CTA and of its peers); dK storing dS then
+                // also stores the slot and reports once the store read it
                 if (mbar_wait(&bar_z_full, s & 1, abort_flag, status, lim, XS_ZFULL)) {
                     for (int p = 0; p < C; ++p) {
                         if (p == c) continue;
                         bulk_copy_s2cluster(mapa_shared(smem_u32(sZ + slot_of(c, p) * 32768), p), sZown, 32768,
                                             mapa_shared(smem_u32(&bar_zpeer[slot_of(c, p)]), p));
                     }
+                    if (st_ds) {
+                        if (t < n_ct) {
+                            tma_store_4d_hint(&tS, sZown, col_row0(t), row_co(r0), col_head(t), bco, pol);
+                            tma_store_4d_hint(&tS, sZown + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco, pol);
+                            bulk_commit_group();
+                            bulk_wait_read_all();
+                        }
+                        mbar_arrive(&sh.stored);
+                    }
                 }
             }
         }
+        // the tile stores are complete before the CTA leaves
+        if ((st_ds || st_p) && ew == 0) bulk_wait_all();
         // ------------------------------------------------------ epilogue
         if (ok && n_steps > 0) {
             ok = warp_ok(mbar_wait(&bar_acc, (n_steps - 1) & 1, abort_flag, status, lim, XS_EPI));
@@ -787,7 +887,7 @@ cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const Geo& gm, in
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], a, gm);
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], a, gm);
 }
 
 template <int OP>
@@ -840,7 +940,7 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
     const Src sdo = q_empty ? Src{a.k, pb.vk, true} : (a.dO ? Src{a.dO, pb.vdo, false} : sq);
     const Src sk = kv_empty ? Src{a.q, pb.vq, false} : Src{a.k, pb.vk, true};
     const Src sv = kv_empty ? Src{a.q, pb.vq, false} : Src{a.v, pb.vv, true};
-    CUtensorMap m[5];
+    CUtensorMap m[7];
     bool okm = true;
     auto mk = [&](int i, const Src& x, int rows) {
         // value operand: one box of 32 rows x the slab's chunks, or (D % 64 != 0) a
@@ -867,6 +967,12 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
         n_rt = (pb.Nkv + 127) / 128; bz = pb.B * pb.Hkv;
         break;
     }
+    // dK storing dS^T / P^T: those buffers as stored tiles (64 queries x 128 key rows)
+    if (op == XOP_DK && (a.store_ds || a.store_p) && pb.varlen) return cudaErrorInvalidConfiguration;
+    if (op == XOP_DK && a.store_ds) okm = okm && make_ds_map(&m[5], a.ds, pb, a.bf16, 128);
+    else m[5] = m[0];
+    if (op == XOP_DK && a.store_p) okm = okm && make_ds_map(&m[6], a.p, pb, a.bf16, 128);
+    else m[6] = m[0];
     if (!okm) return cudaErrorInvalidValue;
     if (n_rt == 0 || bz == 0) return cudaSuccess;
     switch (op) {

@@ -173,8 +173,8 @@ FFPA_API ffpa_status ffpa_fwd_fp8_quantized(ffpa_dtype dt, ffpa_view o, float* l
 FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 /*
  * Workspace bytes that also hold dS^T and P^T for the stored-tile backward:
- * on a dense problem whose head dim is a multiple of 128 up to 768 (the
- * range of the CTA-pair kernels), ffpa_bwd / ffpa_bwd_strided given a
+ * on a dense problem whose head dim is a multiple of 64 up to 1024,
+ * ffpa_bwd / ffpa_bwd_strided given a
  * workspace at least this large
  *   - have the dK launch also store every P^T tile (in the input dtype) and
  *     form dV = P^T dO with one GEMM after it, instead of a dV launch that
@@ -224,7 +224,7 @@ FFPA_API ffpa_status ffpa_bwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, f
  * workspace the preprocess stage wrote, so a caller that splits them issues
  * bit 0 first (the FFPA docs' CuTe-DSL page, "Blackwell status", describes the
  * same four launches). ffpa_bwd(...) == ffpa_bwd_stages(..., 15).
- * With the workspace of ffpa_bwd_workspace_bytes_ds (dense, D % 128 == 0, D <= 768),
+ * With the workspace of ffpa_bwd_workspace_bytes_ds (dense, D % 64 == 0, D <= 1024),
  * a dK stage also stores dS and a dQ stage in the same call is the
  * dS K GEMM; bit 4 runs that GEMM alone on the dS an earlier dK stage stored
  * in this workspace for the same inputs (bit 2 alone recomputes S and dP).

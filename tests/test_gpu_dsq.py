@@ -1,5 +1,5 @@
-"""GPU parity of the stored-tile backward (dense, D a multiple of 128 up to 768,
-causal or not):
+"""GPU parity of the stored-tile backward (dense, D a multiple of 64 up to 1024,
+either kernel family, causal or not):
 the dK launch also writes dS^T to the workspace and dQ = scale dS K is one
 GEMM; with room for P^T as well, the dK launch also writes P^T and
 dV = P^T dO is one GEMM instead of a launch that recomputes S^T.
@@ -8,11 +8,14 @@ Every case runs the backward three times on the same inputs: with the small
 workspace (dQ recomputes S and dP), with room for dS only, and with room for
 dS and P. All three are checked against the fp64 oracle with the usual
 gradient tolerance. dV must be bit-identical between the first two (the same
-kernel); dK between the last two (storing P does not change it) and, when
-non-causal, between the first two (causal storing starts at an even query
-tile: an extra all-masked tile shifts the summation order).
+kernel). dK must be bit-identical between the first two when non-causal
+(causal storing starts at an even query tile: an extra all-masked tile
+shifts the summation order), and between the last two in the CTA-pair
+family (storing P does not change it there; the one-CTA family then forms
+dS^T from P rounded to fp16 instead of fp32).
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -34,6 +37,14 @@ def _lib():
 
     build.build()
     oracle.build()
+
+
+def pair_family(D):
+    """Whether the backward kernels run as CTA pairs for this head dim."""
+    forced = os.environ.get("FFPA_KERNEL")
+    if forced in ("pair", "single"):
+        return forced == "pair"
+    return D % 128 == 0 and D <= 768
 
 
 def tile_buffer_bytes(q, k):
@@ -64,7 +75,8 @@ def run_both(B, Hq, Hkv, Nq, Nkv, D, dtype=torch.bfloat16, seed=0, causal=False)
         for name, got, r in zip(("dQ", "dK", "dV"), gs, ref):
             check_grad(got, r, name)
     assert torch.equal(g_small[2], g_ds[2])
-    assert torch.equal(g_ds[1], g_big[1])
+    if pair_family(D):
+        assert torch.equal(g_ds[1], g_big[1])
     if not causal:
         assert torch.equal(g_small[1], g_ds[1])
     return inp, (q, k, v, do, o, lse, scale, big, ds_only), g_big, g_ds
@@ -76,15 +88,17 @@ def test_stored_ds_backward(D, Nq, Nkv):
     run_both(1, 2, 2, Nq, Nkv, D, seed=Nq + D)
 
 
-@pytest.mark.parametrize("D", [128, 384, 640, 768])
+@pytest.mark.parametrize("D", [128, 320, 384, 448, 576, 640, 768, 1024])
 def test_stored_tile_backward_other_head_dims(D):
-    # slabs of 128 / 384 / 640 columns end in an N = 128 MMA; D > 512 takes two
-    # slabs per row tile
+    # CTA pairs up to 768 (multiples of 128), one CTA per slab otherwise; GEMM
+    # slabs that end 64 or 128 columns past a multiple of 256 end in an N = 128
+    # MMA; D > 512 takes two slabs per row tile
     run_both(1, 2, 1, 300, 333, D, dtype=torch.float16, seed=D)
 
 
-def test_stored_tile_backward_other_head_dims_causal():
-    run_both(1, 2, 2, 400, 300, 640, seed=11, causal=True)
+@pytest.mark.parametrize("D", [640, 1024])
+def test_stored_tile_backward_other_head_dims_causal(D):
+    run_both(1, 2, 2, 400, 300, D, seed=11, causal=True)
 
 
 def test_stored_ds_backward_gqa_fp16():
@@ -134,16 +148,20 @@ def test_stored_ds_backward_causal(Nq, Nkv):
 
 
 def test_varlen_and_other_head_dims_keep_the_recompute_path():
-    for D in (320, 896, 1024):
+    for D in (96, 352):
         q = torch.zeros(1, 2, 64, D, dtype=torch.bfloat16, device="cuda")
         assert api.bwd_workspace_bytes(q, q, True) == api.bwd_workspace_bytes(q, q)
-    for D in (128, 512, 768):
+    for D in (128, 320, 512, 768, 1024):
         q5 = torch.zeros(1, 2, 64, D, dtype=torch.bfloat16, device="cuda")
         assert api.bwd_workspace_bytes(q5, q5, True) > api.bwd_workspace_bytes(q5, q5)
 
 
-def test_one_cta_family_forced_keeps_the_recompute_path(monkeypatch):
-    # only the CTA-pair dK kernel stores dS: with the one-CTA family forced, the
-    # large workspace must still give the recompute path's (correct) dQ
-    monkeypatch.setenv("FFPA_KERNEL", "single")
+@pytest.mark.parametrize("family", ["single", "pair"])
+def test_either_family_forced_stores_the_tiles(monkeypatch, family):
+    # the dK kernels of both families store the tiles: forcing either one (the
+    # one-CTA family at D = 512, CTA pairs at D = 576) keeps the parity
+    monkeypatch.setenv("FFPA_KERNEL", family)
+    if family == "pair":
+        run_both(1, 2, 1, 200, 333, 576, dtype=torch.float16, seed=553, causal=True)
+        return
     run_both(1, 4, 2, 150, 333, 512, dtype=torch.float16, seed=552, causal=True)

@@ -560,6 +560,12 @@ def run_ours(args):
         # packed batch: forward and the whole backward through the varlen entry points
         cu = inp["cu_seqlens"].to(dev)
         mx = max(w.seqlens)
+        # the stored-tile backward when varlen_bwd's own workspace holds the tiles
+        sizes = (_ffi.BF16 if w.dtype == torch.bfloat16 else _ffi.FP16, len(w.seqlens), sum(w.seqlens),
+                 sum(w.seqlens), mx, mx, w.Hq, w.Hkv, w.D)
+        big = int(_ffi.ffpa_varlen_bwd_workspace_bytes_ds(*sizes, int(w.causal)))
+        ds_path = big > int(_ffi.ffpa_varlen_bwd_workspace_bytes(*sizes)) and \
+            big <= api.DS_WORKSPACE_FRACTION * torch.cuda.mem_get_info(dev)[0]
         names = ("fwd", "bwd")
         state = {}
 
@@ -660,7 +666,9 @@ def run_ours(args):
     # 2*B*Hq*Nq*Nkv*D (halved causal)
     gemm = f_fwd / 2.0
     if w.varlen:
-        algo = {"fwd": 2 * gemm, "bwd": 8 * gemm}  # bwd: preprocess + dV (2) + dK (3) + dQ (3) units
+        # bwd: preprocess + dK (3) + dV (1) + dQ (1) units on the stored tiles, else
+        # preprocess + dV (2) + dK (3) + dQ (3)
+        algo = {"fwd": 2 * gemm, "bwd": (5 if ds_path else 8) * gemm}
     else:
         algo = {"fwd": 2 * gemm, "dv": (1 if ds_path else 2) * gemm, "dk": 3 * gemm,
                 "dq": (1 if ds_path else 3) * gemm}
@@ -694,9 +702,9 @@ def run_ours(args):
             "bwd": {"tflops": world * f_bwd / (bwd_ms / 1e3) / 1e12, "ms": bwd_ms,
                     "pct_peak_burst": 100 * f_bwd / (bwd_ms / 1e3) / 1e12 / pk["bf16_tflops"]},
             "kernel_ms": per_ms,
-            "dq_path": ("one GEMM over the dS stored by the dK launch" if not w.varlen and ds_path
+            "dq_path": ("one GEMM over the dS stored by the dK launch" if ds_path
                         else "S and dP recomputed"),
-            "dv_path": ("one GEMM over the P^T stored by the dK launch" if not w.varlen and ds_path
+            "dv_path": ("one GEMM over the P^T stored by the dK launch" if ds_path
                         else "S^T recomputed"),
             "kernel_ms_note": "each kernel launched alone (one call per stage), after the timed region"
             if not w.varlen else "fwd and bwd calls of the timed region",

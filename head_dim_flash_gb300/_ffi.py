@@ -35,6 +35,7 @@ EXPORTS = (
     "ffpa_bwd_noalloc",
     "ffpa_varlen_fwd",
     "ffpa_varlen_bwd_workspace_bytes",
+    "ffpa_varlen_bwd_workspace_bytes_ds",
     "ffpa_varlen_bwd",
     "ffpa_get_status",
     "ffpa_last_error",
@@ -97,6 +98,8 @@ def _declare(lib):
     lib.ffpa_varlen_fwd.restype = _i
     lib.ffpa_varlen_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i]
     lib.ffpa_varlen_bwd_workspace_bytes.restype = _sz
+    lib.ffpa_varlen_bwd_workspace_bytes_ds.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i]
+    lib.ffpa_varlen_bwd_workspace_bytes_ds.restype = _sz
     lib.ffpa_varlen_bwd.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i,
                                     _i, _f, _p, _sz, _p]
     lib.ffpa_varlen_bwd.restype = _i
@@ -218,6 +221,10 @@ def ffpa_varlen_fwd(*args):
 
 def ffpa_varlen_bwd_workspace_bytes(*args):
     return load().ffpa_varlen_bwd_workspace_bytes(*args)
+
+
+def ffpa_varlen_bwd_workspace_bytes_ds(*args):
+    return load().ffpa_varlen_bwd_workspace_bytes_ds(*args)
 
 
 def ffpa_varlen_bwd(*args):

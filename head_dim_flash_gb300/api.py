@@ -338,17 +338,23 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, 
 
 def varlen_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False,
                scale=None, workspace=None):
-    """Packed backward through ffpa_varlen_bwd. Returns (dq, dk, dv)."""
+    """Packed backward through ffpa_varlen_bwd. Without a workspace, one with
+    room for the stored dS and P tiles is allocated where that path applies and
+    takes at most DS_WORKSPACE_FRACTION of the free device memory. Returns
+    (dq, dk, dv)."""
     q, k, v, o, dout = _prep(q, k, v, o, dout)
     lse = lse.contiguous()
     Tq, Hq, D = q.shape
     Tk, Hkv, _ = k.shape
     cq, ck = _cu(cu_seqlens_q, q.device), _cu(cu_seqlens_k, q.device)
     batch = cq.numel() - 1
-    ws_bytes = int(_ffi.ffpa_varlen_bwd_workspace_bytes(_dt(q), batch, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k),
-                                                        Hq, Hkv, D))
+    sizes = (_dt(q), batch, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D)
     if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+        n = int(_ffi.ffpa_varlen_bwd_workspace_bytes(*sizes))
+        big = int(_ffi.ffpa_varlen_bwd_workspace_bytes_ds(*sizes, int(bool(causal))))
+        if big > n and big <= DS_WORKSPACE_FRACTION * torch.cuda.mem_get_info(q.device)[0]:
+            n = big
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     st = _ffi.ffpa_varlen_bwd(_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                               dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cq.data_ptr(),

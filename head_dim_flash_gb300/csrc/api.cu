@@ -598,6 +598,20 @@ size_t ffpa_varlen_bwd_workspace_bytes(ffpa_dtype, int batch, int total_q, int, 
     return ws_bytes(static_cast<long>(total_q) * Hq);
 }
 
+size_t ffpa_varlen_bwd_workspace_bytes_ds(ffpa_dtype dt, int batch, int total_q, int total_k, int max_seqlen_q,
+                                          int max_seqlen_k, int Hq, int Hkv, int D, int causal)
+{
+    const size_t small =
+        ffpa_varlen_bwd_workspace_bytes(dt, batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, Hkv, D);
+    if (batch <= 0 || total_q <= 0 || total_k <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || Hq <= 0 ||
+        Hkv <= 0 || Hq % Hkv != 0)
+        return small;
+    const ffpa::Problem pb = varlen_problem(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, causal,
+                                            1.f, nullptr, nullptr);
+    // dS^T, then P^T at the next 256-byte boundary
+    return ffpa::dsq_supported(pb) ? small + align256(ffpa::dsq_ds_bytes(pb)) + ffpa::dsq_ds_bytes(pb) : small;
+}
+
 ffpa_status ffpa_varlen_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
                             const int* cu_seqlens_k, int batch, int total_q, int total_k, int max_seqlen_q,

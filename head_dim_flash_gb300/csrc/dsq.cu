@@ -62,24 +62,38 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int rh = rank & 1;
     const bool leader = rh == 0;
     const int G = pb.Hq / pb.Hkv;
-    const int off = pb.Nkv - pb.Nq;  // causal: key j legal for query i iff j <= i + off
     // dQ: (b, query head h); dV: (b, KV head hk), the group's query heads hk*G ..
     const int hb = DV ? pb.Hkv : pb.Hq;
     const int b = blockIdx.z / hb, h = blockIdx.z % hb, hk = DV ? h : h / G;
+    // the sequence: lengths, and (packed batches) its first query / key token
+    // and the first row of its key rows in the tile buffers (one 256-row pad
+    // per sequence, so that no row tile reaches the next sequence's rows)
+    int lq = pb.Nq, lk = pb.Nkv, tq0 = 0, tk0 = 0, tr0 = 0, bco = b;
+    if (pb.varlen) {
+        tq0 = pb.cu_q[b];
+        lq = pb.cu_q[b + 1] - tq0;
+        tk0 = pb.cu_k[b];
+        lk = pb.cu_k[b + 1] - tk0;
+        tr0 = tk0 + 256 * b;
+        bco = 0;
+    }
+    const int off = lk - lq;  // causal: key j legal for query i iff j <= i + off
+    const int n_rows = DV ? lk : lq;
+    const int n_rt_seq = (n_rows + 255) / 256;
+    if (static_cast<int>(blockIdx.y) >= n_rt_seq) return;  // uniform over the pair, before any barrier
     // causal: the longest tiles first (dQ: the last query tiles, dV: the first key tiles)
-    const int tile = (pb.causal && !DV) ? static_cast<int>(gridDim.y - 1 - blockIdx.y) : static_cast<int>(blockIdx.y);
+    const int tile = (pb.causal && !DV) ? n_rt_seq - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
     const int row0 = tile * 256;
     const int rc = row0 + 128 * rh;  // my first row (query for dQ, key for dV)
-    const int n_rows = DV ? pb.Nkv : pb.Nq;
     // K blocks of 64 (both CTAs of the pair alike): dQ keys [0, key_end);
-    // dV per query head: queries [64 qb_lo, Nq)
+    // dV per query head: queries [64 qb_lo, lq)
     int kb_lo = 0, n_kb;
     if constexpr (DV) {
         const int i_lo = pb.causal ? max(0, row0 - off) : 0;
         kb_lo = i_lo / 64;
-        n_kb = i_lo < pb.Nq ? (pb.Nq + 63) / 64 - kb_lo : 0;
+        n_kb = i_lo < lq ? (lq + 63) / 64 - kb_lo : 0;
     } else {
-        const int key_end = pb.causal ? min(pb.Nkv, row0 + 255 + off + 1) : pb.Nkv;
+        const int key_end = pb.causal ? min(lk, row0 + 255 + off + 1) : lk;
         n_kb = key_end > 0 ? (key_end + 63) / 64 : 0;
     }
     const int n_it = DV ? G * n_kb : n_kb;  // K iterations
@@ -147,25 +161,25 @@ __global__ void __launch_bounds__(kQThreads, 1)
                     const int i0 = (kb_lo + it % n_kb) * 64;  // first query of the block
                     if (lane == 0) {
                         // A: P^T rows = my 128 keys, queries [i0, +64)
-                        tma_load_4d_pair(st, &tA, fb, i0, rc, hq, b);
+                        tma_load_4d_pair(st, &tA, fb, i0, tr0 + rc, hq, bco);
                     } else {
                         // B: dO rows = queries [i0, +64), my half of each MMA's N columns
                         // (a 128-column box; an N = 128 MMA reads its first 64)
                         for (int j = 0; j < nj; ++j)
-                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, i0, (c0 + j * 256 + rh * n_of(j) / 2) / 64,
-                                             hq, b);
+                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, tq0 + i0,
+                                             (c0 + j * 256 + rh * n_of(j) / 2) / 64, hq, bco);
                     }
                 } else {
                     const int kb = it;
                     if (lane == 0) {
                         // A: dS^T rows = keys [64 kb, +64), my 128 queries as two 64-query boxes
-                        tma_load_4d_pair(st, &tA, fb, rc, kb * 64, h, b);
-                        tma_load_4d_pair(st + 8192, &tA, fb, rc + 64, kb * 64, h, b);
+                        tma_load_4d_pair(st, &tA, fb, rc, tr0 + kb * 64, h, bco);
+                        tma_load_4d_pair(st + 8192, &tA, fb, rc + 64, tr0 + kb * 64, h, bco);
                     } else {
                         // B: K rows = keys [64 kb, +64), my half of each MMA's N columns
                         for (int j = 0; j < nj; ++j)
-                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, kb * 64,
-                                             (c0 + j * 256 + rh * n_of(j) / 2) / 64, hk, b);
+                            tma_load_5d_pair(st + 16384 * (1 + j), &tB, fb, 0, tk0 + kb * 64,
+                                             (c0 + j * 256 + rh * n_of(j) / 2) / 64, hk, bco);
                     }
                 }
                 rp.advance(kQStages);
@@ -222,8 +236,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
             // no K block for any row of the pair: zero rows (the accumulator was never written)
             const float mul = n_it > 0 ? (DV ? 1.f : pb.scale) : 0.f;
             const View& vo = DV ? pb.vdv : pb.vdq;
-            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + static_cast<size_t>(b) * vo.sb +
-                            static_cast<size_t>(h) * vo.sh + static_cast<size_t>(q) * vo.sn + c0;
+            const size_t tok = static_cast<size_t>((DV ? tk0 : tq0) + q);  // row (packed: token)
+            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + static_cast<size_t>(bco) * vo.sb +
+                            static_cast<size_t>(h) * vo.sh + tok * vo.sn + c0;
             for (int cc = 0; cc < w; cc += 32) {
                 uint32_t v[32];
                 if (n_it > 0) {
@@ -262,24 +277,33 @@ __global__ void __launch_bounds__(kQThreads, 1)
 bool dsq_supported(const Problem& pb)
 {
     // whole 64-column chunks (the 5-D operand maps), at most two 512-column slabs
-    return !pb.varlen && pb.D % 64 == 0 && pb.D <= 1024 && pb.Nq > 0 && pb.Nkv > 0;
+    if (pb.varlen) return pb.D % 64 == 0 && pb.D <= 1024 && pb.total_q > 0 && pb.total_k > 0 && pb.Nq > 0;
+    return pb.D % 64 == 0 && pb.D <= 1024 && pb.Nq > 0 && pb.Nkv > 0;
+}
+
+// Tile buffer rows per (batch, head): the keys (dense), or every sequence's
+// keys plus a 256-row pad each (packed: sequence b starts at row cu_k[b] + 256 b)
+static size_t tile_rows(const Problem& pb)
+{
+    return pb.varlen ? static_cast<size_t>(pb.total_k) + 256 * static_cast<size_t>(pb.B) : static_cast<size_t>(pb.Nkv);
 }
 
 size_t dsq_ds_bytes(const Problem& pb)
 {
     const size_t ldq = (static_cast<size_t>(pb.Nq) + 7) & ~static_cast<size_t>(7);
-    return static_cast<size_t>(pb.B) * pb.Hq * pb.Nkv * ldq * 2;
+    return static_cast<size_t>(pb.varlen ? 1 : pb.B) * pb.Hq * tile_rows(pb) * ldq * 2;
 }
 
 bool make_ds_map(CUtensorMap* m, const void* ds, const Problem& pb, bool bf16, int box_rows)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
+    // (packed batches: Nq is the longest sequence, and one batch of tile_rows rows)
     const cuuint64_t ldq = (static_cast<cuuint64_t>(pb.Nq) + 7) & ~static_cast<cuuint64_t>(7);
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(pb.Nq), static_cast<cuuint64_t>(pb.Nkv),
-                                static_cast<cuuint64_t>(pb.Hq), static_cast<cuuint64_t>(pb.B)};
-    const cuuint64_t strides[3] = {ldq * 2, static_cast<cuuint64_t>(pb.Nkv) * ldq * 2,
-                                   static_cast<cuuint64_t>(pb.Hq) * pb.Nkv * ldq * 2};
+    const cuuint64_t rows = tile_rows(pb);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(pb.Nq), rows, static_cast<cuuint64_t>(pb.Hq),
+                                static_cast<cuuint64_t>(pb.varlen ? 1 : pb.B)};
+    const cuuint64_t strides[3] = {ldq * 2, rows * ldq * 2, static_cast<cuuint64_t>(pb.Hq) * rows * ldq * 2};
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ds),

@@ -268,6 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_head = T::kRowsQ ? h : hk;
     auto row_co = [&](int row) { return VARLEN ? (T::kRowsQ ? tq0 : tk0) + row : row; };
     auto col_co = [&](int row) { return VARLEN ? (T::kRowsQ ? tk0 : tq0) + row : row; };
+    // key row -> row of the stored tile buffers (packed batches: sequence b's rows
+    // start at cu_k[b] + 256 b, so that no tile reaches the next sequence's rows)
+    auto tile_row = [&](int row) { return VARLEN ? tk0 + 256 * b + row : row; };
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -673,8 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // all 256 threads wrote it: store it, and report once the store read it
                         if (mbar_wait(&sh.p_full, s & 1, abort_flag, status, lim, XS_ZFULL)) {
                             if (t < n_ct) {
-                                tma_store_4d_hint(&tP, sZown, col_row0(t), row_co(r0), col_head(t), bco, pol);
-                                tma_store_4d_hint(&tP, sZown + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco,
+                                tma_store_4d_hint(&tP, sZown, col_row0(t), tile_row(r0), col_head(t), bco, pol);
+                                tma_store_4d_hint(&tP, sZown + 16384, col_row0(t) + 64, tile_row(r0), col_head(t), bco,
                                                   pol);
                                 bulk_commit_group();
                                 bulk_wait_read_all();
@@ -759,8 +762,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (st_ds) {
                         if (t < n_ct) {
-                            tma_store_4d_hint(&tS, sZown, col_row0(t), row_co(r0), col_head(t), bco, pol);
-                            tma_store_4d_hint(&tS, sZown + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco, pol);
+                            tma_store_4d_hint(&tS, sZown, col_row0(t), tile_row(r0), col_head(t), bco, pol);
+                            tma_store_4d_hint(&tS, sZown + 16384, col_row0(t) + 64, tile_row(r0), col_head(t), bco, pol);
                             bulk_commit_group();
                             bulk_wait_read_all();
                         }
@@ -968,7 +971,6 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
         break;
     }
     // dK storing dS^T / P^T: those buffers as stored tiles (64 queries x 128 key rows)
-    if (op == XOP_DK && (a.store_ds || a.store_p) && pb.varlen) return cudaErrorInvalidConfiguration;
     if (op == XOP_DK && a.store_ds) okm = okm && make_ds_map(&m[5], a.ds, pb, a.bf16, 128);
     else m[5] = m[0];
     if (op == XOP_DK && a.store_p) okm = okm && make_ds_map(&m[6], a.p, pb, a.bf16, 128);

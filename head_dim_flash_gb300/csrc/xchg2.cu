@@ -307,6 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_head = T::kRowsQ ? h : hk;
     auto row_co = [&](int row) { return VARLEN ? (T::kRowsQ ? tq0 : tk0) + row : row; };
     auto col_co = [&](int row) { return VARLEN ? (T::kRowsQ ? tk0 : tq0) + row : row; };
+    // key row -> row of the stored tile buffers (packed batches: sequence b's rows
+    // start at cu_k[b] + 256 b, so that no tile reaches the next sequence's rows)
+    auto tile_row = [&](int row) { return VARLEN ? tk0 + 256 * b + row : row; };
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producers
@@ -667,8 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(&sh.p_full[bb], zpar(s), abort_flag, status, lim, PS_COPY);
                     if (ok) {
                         if (t < n_ct) {
-                            tma_store_4d_hint(&tP, zown_base, col_row0(t), row_co(r0), col_head(t), bco, pol);
-                            tma_store_4d_hint(&tP, zown_base + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco,
+                            tma_store_4d_hint(&tP, zown_base, col_row0(t), tile_row(r0), col_head(t), bco, pol);
+                            tma_store_4d_hint(&tP, zown_base + 16384, col_row0(t) + 64, tile_row(r0), col_head(t), bco,
                                               pol);
                             bulk_commit_group();
                             bulk_wait_read_all();
@@ -688,8 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ok && store_ds) {
                     if (t < n_ct) {
-                        tma_store_4d_hint(&tS, zown_base, col_row0(t), row_co(r0), col_head(t), bco, pol);
-                        tma_store_4d_hint(&tS, zown_base + 16384, col_row0(t) + 64, row_co(r0), col_head(t), bco, pol);
+                        tma_store_4d_hint(&tS, zown_base, col_row0(t), tile_row(r0), col_head(t), bco, pol);
+                        tma_store_4d_hint(&tS, zown_base + 16384, col_row0(t) + 64, tile_row(r0), col_head(t), bco, pol);
                         bulk_commit_group();
                         bulk_wait_read_all();
                     }

@@ -284,6 +284,17 @@ FFPA_API ffpa_status ffpa_varlen_fwd(ffpa_dtype dt, const void* q, const void* k
 
 FFPA_API size_t ffpa_varlen_bwd_workspace_bytes(ffpa_dtype dt, int batch, int total_q, int total_k, int max_seqlen_q,
                                        int max_seqlen_k, int Hq, int Hkv, int D);
+/*
+ * Workspace bytes of the stored-tile varlen backward (as
+ * ffpa_bwd_workspace_bytes_ds, for packed batches with D a multiple of 64 up
+ * to 1024). The two tile buffers are Hq x (total_k + 256 * batch) x
+ * round_up(max_seqlen_q, 8) 16-bit values each: sequence b's key rows start
+ * at row cu_seqlens_k[b] + 256 b, and its queries are the columns from 0.
+ * Returns ffpa_varlen_bwd_workspace_bytes() where the path does not apply.
+ */
+FFPA_API size_t ffpa_varlen_bwd_workspace_bytes_ds(ffpa_dtype dt, int batch, int total_q, int total_k,
+                                                   int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                                                   int causal);
 
 /* Packed varlen backward; layouts as in ffpa_varlen_fwd, dq like q, dk/dv like k. */
 FFPA_API ffpa_status ffpa_varlen_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,

@@ -119,6 +119,13 @@ def test_stored_tile_workspace_and_stage_bits(lib):
     def stages(ws_bytes, bits):
         return lib.ffpa_bwd_stages(0, *ptrs, FAKE, ws_bytes, B, Hq, Hkv, Nq, Nkv, D, 0, 0.05, bits, None)
 
+    # packed batches: Hq x (total_k + 256 batch) x round_up(max_q, 8) per buffer
+    vsmall = lib.ffpa_varlen_bwd_workspace_bytes(0, 3, 700, 500, 300, 250, Hq, Hkv, D)
+    vtile = Hq * (500 + 256 * 3) * 304 * 2
+    assert lib.ffpa_varlen_bwd_workspace_bytes_ds(0, 3, 700, 500, 300, 250, Hq, Hkv, D, 1) == (
+        vsmall + (vtile + 255) // 256 * 256 + vtile)
+    assert lib.ffpa_varlen_bwd_workspace_bytes_ds(0, 3, 700, 500, 300, 250, Hq, Hkv, 352, 1) == (
+        lib.ffpa_varlen_bwd_workspace_bytes(0, 3, 700, 500, 300, 250, Hq, Hkv, 352))
     assert stages(big, 64) == 1 and "bits 0..5" in lib.ffpa_last_error().decode()
     assert stages(small, 16) == 1 and "stage bit 4" in lib.ffpa_last_error().decode()
     assert stages(small + tile, 1 | 8 | 32) == 1 and "stage bit 5" in lib.ffpa_last_error().decode()

@@ -147,6 +147,37 @@ def test_stored_ds_backward_causal(Nq, Nkv):
     run_both(1, 4, 2, Nq, Nkv, 512, seed=Nq + 2 * Nkv, causal=True)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [512, 1024])
+def test_stored_tile_varlen_backward(causal, D):
+    # packed batches: every sequence's key rows start at cu_seqlens_k[b] + 256 b
+    # in the tile buffers; empty sequences on either side, lengths that end
+    # mid-tile, more queries than keys (causal rows with no legal key)
+    lq = [5, 0, 130, 300, 64, 257]
+    lk = [7, 3, 130, 200, 0, 513]
+    inp = workloads.random_varlen(lq, lk, 4, 2, D, seed=71 + D)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dO"))
+    cq, ck = inp["cu_seqlens_q"].cuda(), inp["cu_seqlens_k"].cuda()
+    scale = 1 / math.sqrt(D)
+    o, lse = api.varlen_fwd(q, k, v, cq, ck, max(lq), max(lk), causal, scale)
+    sizes = (0, len(lq), sum(lq), sum(lk), max(lq), max(lk), 4, 2, D)
+    from head_dim_flash_gb300 import _ffi
+    small_n = int(_ffi.ffpa_varlen_bwd_workspace_bytes(*sizes))
+    big_n = int(_ffi.ffpa_varlen_bwd_workspace_bytes_ds(*sizes, int(causal)))
+    rows = sum(lk) + 256 * len(lk)
+    one = 4 * rows * ((max(lq) + 7) // 8 * 8) * 2
+    assert big_n == small_n + (one + 255) // 256 * 256 + one
+    ref = oracle.varlen_bwd(inp["q"], inp["k"], inp["v"], inp["dO"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                            causal, scale)
+    got = {}
+    for name, n in (("small", small_n), ("big", big_n)):
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        got[name] = api.varlen_bwd(q, k, v, o, lse, do, cq, ck, max(lq), max(lk), causal, scale, workspace=ws)
+        api.get_status()
+        for gname, g, r in zip(("dQ", "dK", "dV"), got[name], ref):
+            check_grad(g, r, f"{name} {gname}")
+
+
 def test_varlen_and_other_head_dims_keep_the_recompute_path():
     for D in (96, 352):
         q = torch.zeros(1, 2, 64, D, dtype=torch.bfloat16, device="cuda")

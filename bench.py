@@ -206,16 +206,16 @@ PAIR_SOURCES = ("xchg.cu", "xchg2.cu", "ptx.cuh", "tile_common.cuh", "kernels.h"
 DECODE_SOURCES = ("decode.cu", "ptx.cuh", "tile_common.cuh", "kernels.h")
 FP8_SOURCES = ("xchg2.cu", "fp8.cu", "ptx.cuh", "tile_common.cuh", "kernels.h", "host.cu")
 TRAFFIC = {
-    # dK (also storing P^T and dS^T) at 16 heads (764,000,768 + 4,367,750,144 bytes) scaled to 32
-    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 10263501824, "files": PAIR_SOURCES,
-                                             "sources": "2e8a8fae1772c025"},
+    # dK (also storing P^T and dS^T) at 16 heads (756,822,528 + 4,367,949,056 bytes) scaled to 32
+    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 10249543168, "files": PAIR_SOURCES,
+                                             "sources": "265788a84d2f68de"},
     # one ffpa_decode_fwd call: split kernel + combine (means over six calls)
-    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2156703957, "files": DECODE_SOURCES,
-                                                                "sources": "452646d840e0c29f"},
+    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2156501035, "files": DECODE_SOURCES,
+                                                                "sources": "0b80c2d43c6c915b"},
     # the e4m3 attention kernel (reads q8, k8, V^T codes; writes O, LSE)
-    ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 638421043,
+    ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 639294413,
                                                                              "files": FP8_SOURCES,
-                                                                             "sources": "32d8ddba290d320a"},
+                                                                             "sources": "79e5b087ccadda46"},
 }
 
 
@@ -730,7 +730,8 @@ def measure_e2e(w, args, dev, stream, inp, step_flops, world):
 
     from head_dim_flash_gb300 import api
 
-    host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "dO")}
+    names = ("q", "k", "v", "dO") + (("cu_seqlens",) if w.varlen else ())
+    host = {n: inp[n].pin_memory() for n in names}
     bufs = [{n: torch.empty_like(host[n], device=dev) for n in host} for _ in range(2)]
     out_h = {n: torch.empty(inp[src].shape, dtype=inp[src].dtype).pin_memory()
              for n, src in (("dq", "q"), ("dk", "k"), ("dv", "v"))}
@@ -753,8 +754,13 @@ def measure_e2e(w, args, dev, stream, inp, step_flops, world):
         b = i % 2
         x = bufs[b]
         stream.wait_event(in_ready[b])
-        o, lse = api.fwd(x["q"], x["k"], x["v"], w.causal, w.scale)
-        grads = api.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], w.causal, w.scale)
+        if w.varlen:
+            cu, mx = x["cu_seqlens"], max(w.seqlens)
+            o, lse = api.varlen_fwd(x["q"], x["k"], x["v"], cu, cu, mx, mx, w.causal, w.scale)
+            grads = api.varlen_bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], cu, cu, mx, mx, w.causal, w.scale)
+        else:
+            o, lse = api.fwd(x["q"], x["k"], x["v"], w.causal, w.scale)
+            grads = api.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], w.causal, w.scale)
         done = torch.cuda.Event()
         done.record(stream)
         buf_free[b] = done

@@ -180,20 +180,32 @@ def cpu_baseline(w, inp, n_rows=8192):
     Returns (tflops, seconds, cores, description)."""
     import oracle
 
-    rows = min(n_rows, w.Nq)
-    q = inp["q"][0:1, 0:1, :rows]
-    k = inp["k"][0:1, 0:1]
-    v = inp["v"][0:1, 0:1]
-    do = inp["dO"][0:1, 0:1, :rows]
+    if w.varlen:
+        # packed [T, H, D]: the first sequence, head 0, as a [1, 1, N, D] problem
+        n_keys = w.seqlens[0]
+        rows = min(n_rows, n_keys)
+
+        def dense(x, n):
+            return x[:n, 0:1, :].permute(1, 0, 2).unsqueeze(0).contiguous()
+
+        q, do = dense(inp["q"], rows), dense(inp["dO"], rows)
+        k, v = dense(inp["k"], n_keys), dense(inp["v"], n_keys)
+    else:
+        n_keys = w.Nkv
+        rows = min(n_rows, w.Nq)
+        q = inp["q"][0:1, 0:1, :rows]
+        k = inp["k"][0:1, 0:1]
+        v = inp["v"][0:1, 0:1]
+        do = inp["dO"][0:1, 0:1, :rows]
     oracle.build()
     cores = oracle.num_threads()
     t0 = time.perf_counter()
     oracle.attention_fwd(q, k, v, False, w.scale)
     oracle.attention_bwd(q, k, v, do, False, w.scale)
     dt = time.perf_counter() - t0
-    f = 3.5 * 4.0 * rows * w.Nkv * w.D  # fwd + bwd counted flops of the sample
-    desc = (f"fwd+bwd of {rows} query rows x {w.Nkv} keys of head 0 (D={w.D}, non-causal sample), "
-            f"fp64 C oracle, OpenMP")
+    f = 3.5 * 4.0 * rows * n_keys * w.D  # fwd + bwd counted flops of the sample
+    desc = (f"fwd+bwd of {rows} query rows x {n_keys} keys of head 0 (D={w.D}, non-causal sample"
+            f"{', first sequence' if w.varlen else ''}), fp64 C oracle, OpenMP")
     return f / dt / 1e12, dt, cores, desc
 
 

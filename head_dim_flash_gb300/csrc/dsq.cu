@@ -1,14 +1,15 @@
-// dQ and dV from the tiles the dK kernel stored: plain GEMMs for dense
-// problems whose dS^T and P^T the dK kernel wrote to the backward workspace
-// (FFPA docs, "CuTe-DSL Backend" page, "Blackwell status": the backward as a
+// dQ and dV from the tiles the dK kernel stored: plain GEMMs for problems
+// whose dS^T and P^T the dK kernel wrote to the backward workspace (FFPA
+// docs, "CuTe-DSL Backend" page, "Blackwell status": the backward as a
 // preprocess plus separate gradient launches; here the dQ and dV launches
 // reuse the dK launch's tiles instead of recomputing S (and dP), which turns
 // 3 + 2 GEMM units into 1 + 1).
 //
 // The dK kernel stores dS^T and P^T, each [B, Hq, Nkv, ldq] (keys x queries,
-// queries contiguous), tile by tile; masked entries are stored zeros, and
-// under the bottom-right causal mask every tile that holds a legal entry is
-// stored. A CTA pair owns 256 output rows (128 per CTA, in its TMEM lanes)
+// queries contiguous; packed batches: [1, Hq, total_k + 256 B, ldq], sequence
+// b's key rows from cu_k[b] + 256 b, its queries from column 0), tile by
+// tile; masked entries are stored zeros, and under the bottom-right causal
+// mask every tile that holds a legal entry is stored. A CTA pair owns 256 output rows (128 per CTA, in its TMEM lanes)
 // and one slab of at most 512 head-dim columns (fp32 in TMEM; D > 512 takes
 // two pairs, each reading the stored tiles); a ring of 4 stages feeds M=256,
 // N=256 pair MMAs (the last one N=128 when the slab ends 64 or 128 columns

@@ -14,9 +14,14 @@
 // library keeps those 4 MiB until the process exits. All calls on a device
 // share it, so two calls whose kernels overlap on the GPU (different streams
 // without ordering between them) race on it; calls on one stream are fine.
-// Nothing in it has to start at zero: the preprocess kernel of each call
-// overwrites every entry the two gradient kernels of that call read, and the
-// contents left by the previous call are never used.
+// Each call hands ffpa_bwd exactly the workspace size that ffpa_bwd asks for
+// (the per-row statistics only), never the whole array: the backward then
+// always runs the same kernels (preprocess, dV, dK, dQ, each recomputing its
+// scores), whatever the problem size, and never the stored-tile path that a
+// larger workspace would select. Nothing in the array has to start at zero:
+// the preprocess kernel of each call writes delta and the scaled LSE of every
+// row before the gradient kernels of that call read them, and the contents
+// left by the previous call are never read.
 #include <mutex>
 
 #include "../../include/ffpa.h"
@@ -38,6 +43,9 @@ void* g_scratch_addr[kMaxDevices];
 
 // Device address of the scratch array on the current device. Looked up once
 // per device, with that device current, on the first call that needs it.
+// A cudaDeviceReset unloads the library's device image, after which that
+// address is stale: the call is not valid after a reset of its device in the
+// same process.
 void* scratch_address(const char** why)
 {
     int dev = -1;
@@ -81,8 +89,10 @@ ffpa_status ffpa_bwd_noalloc(ffpa_dtype dt, const void* q, const void* k, const 
     if (!scratch)
         return static_cast<ffpa_status>(
             ffpa::set_error(FFPA_ERR_CUDA, "ffpa_bwd_noalloc: scratch address lookup failed: %s", why));
-    return ffpa_bwd(dt, q, k, v, o, lse, dO, dq, dk, dv, scratch, kNoAllocBytes, B, Hq, Hkv, Nq, Nkv, D, causal,
-                    scale, stream);
+    // the size ffpa_bwd asks for (row statistics only; within kNoAllocBytes by the check above)
+    const size_t bytes = ffpa_bwd_workspace_bytes(dt, B, Hq, Hkv, Nq, Nkv, D);
+    return ffpa_bwd(dt, q, k, v, o, lse, dO, dq, dk, dv, scratch, bytes, B, Hq, Hkv, Nq, Nkv, D, causal, scale,
+                    stream);
 }
 
 }  // extern "C"

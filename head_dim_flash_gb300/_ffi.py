@@ -26,6 +26,7 @@ EXPORTS = (
     "ffpa_decode_workspace_bytes",
     "ffpa_decode_fwd",
     "ffpa_bwd_workspace_bytes_ds",
+    "ffpa_bwd_workspace_bytes_budget",
     "ffpa_fp8_workspace_bytes",
     "ffpa_fp8_workspace_layout",
     "ffpa_fp8_quantize",
@@ -36,6 +37,7 @@ EXPORTS = (
     "ffpa_varlen_fwd",
     "ffpa_varlen_bwd_workspace_bytes",
     "ffpa_varlen_bwd_workspace_bytes_ds",
+    "ffpa_varlen_bwd_workspace_bytes_budget",
     "ffpa_varlen_bwd",
     "ffpa_get_status",
     "ffpa_last_error",
@@ -71,6 +73,8 @@ def _declare(lib):
     lib.ffpa_bwd_strided.restype = _i
     lib.ffpa_bwd_workspace_bytes_ds.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i]
     lib.ffpa_bwd_workspace_bytes_ds.restype = _sz
+    lib.ffpa_bwd_workspace_bytes_budget.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _sz]
+    lib.ffpa_bwd_workspace_bytes_budget.restype = _sz
     lib.ffpa_fp8_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i]
     lib.ffpa_fp8_workspace_bytes.restype = _sz
     lib.ffpa_fp8_workspace_layout.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]
@@ -100,6 +104,8 @@ def _declare(lib):
     lib.ffpa_varlen_bwd_workspace_bytes.restype = _sz
     lib.ffpa_varlen_bwd_workspace_bytes_ds.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i]
     lib.ffpa_varlen_bwd_workspace_bytes_ds.restype = _sz
+    lib.ffpa_varlen_bwd_workspace_bytes_budget.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _sz]
+    lib.ffpa_varlen_bwd_workspace_bytes_budget.restype = _sz
     lib.ffpa_varlen_bwd.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i,
                                     _i, _f, _p, _sz, _p]
     lib.ffpa_varlen_bwd.restype = _i
@@ -168,6 +174,10 @@ def ffpa_bwd_workspace_bytes_ds(*args):
     return load().ffpa_bwd_workspace_bytes_ds(*args)
 
 
+def ffpa_bwd_workspace_bytes_budget(*args):
+    return load().ffpa_bwd_workspace_bytes_budget(*args)
+
+
 def ffpa_fp8_workspace_bytes(*args):
     return load().ffpa_fp8_workspace_bytes(*args)
 
@@ -225,6 +235,10 @@ def ffpa_varlen_bwd_workspace_bytes(*args):
 
 def ffpa_varlen_bwd_workspace_bytes_ds(*args):
     return load().ffpa_varlen_bwd_workspace_bytes_ds(*args)
+
+
+def ffpa_varlen_bwd_workspace_bytes_budget(*args):
+    return load().ffpa_varlen_bwd_workspace_bytes_budget(*args)
 
 
 def ffpa_varlen_bwd(*args):

@@ -123,7 +123,7 @@ def decode_supported(q, k) -> bool:
     Hkv = k.shape[1]
     if Hkv <= 0 or Hq % Hkv != 0 or D % 64 != 0:
         return False
-    return B * Hkv * -(-(Hq // Hkv) * Nq // DECODE_ROWS) <= 65535
+    return B * Hkv * -(-(Hq // Hkv) * Nq // DECODE_ROWS) <= 65535 * 65535
 
 
 def decode_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, workspace=None):
@@ -146,7 +146,9 @@ def decode_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=No
     return o, l
 
 
-FP8_HEAD_DIMS = (256, 512, 768)
+def fp8_supported(D: int) -> bool:
+    """Head dims of the FP8 forward: every multiple of 32 in [64, 1024]."""
+    return D % 32 == 0 and 64 <= D <= 1024
 
 
 def fp8_workspace(q, k):
@@ -165,7 +167,9 @@ def _fp8_args(q, k, v):
 
 def fp8_quantize(q, k, v, workspace=None):
     """Runs only the e4m3 quantization; returns (workspace, {name: view}) with
-    q8, k8 (uint8 codes), v8t ([B, Hkv, D, ldv] codes of V^T) and the fp32 scales sq, sk, sv."""
+    q8, k8 (uint8 codes), v8t ([B, Hkv, D, ldv] codes of V^T) and the fp32 scales sq, sk, sv.
+    The code views cover the D real columns; the workspace pads each code row
+    to Dp = D rounded up to 128 with zero codes (q8_padded, k8_padded, v8t_padded)."""
     q, k, v = _fp8_args(q, k, v)
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape
@@ -180,20 +184,24 @@ def fp8_quantize(q, k, v, workspace=None):
         t = ws[off[i]:off[i] + n * (4 if dtype == torch.float32 else 1)]
         return t.view(dtype).view(shape)
 
+    Dp = (D + 127) // 128 * 128
     views = {
-        "q8": region(0, B * Hq * Nq * D, (B, Hq, Nq, D)),
-        "k8": region(1, B * Hkv * Nkv * D, (B, Hkv, Nkv, D)),
-        "v8t": region(2, B * Hkv * D * ldv, (B, Hkv, D, ldv)),
+        "q8_padded": region(0, B * Hq * Nq * Dp, (B, Hq, Nq, Dp)),
+        "k8_padded": region(1, B * Hkv * Nkv * Dp, (B, Hkv, Nkv, Dp)),
+        "v8t_padded": region(2, B * Hkv * Dp * ldv, (B, Hkv, Dp, ldv)),
         "sq": region(3, B * Hq, (B, Hq), torch.float32),
         "sk": region(4, B * Hkv, (B, Hkv), torch.float32),
         "sv": region(5, B * Hkv, (B, Hkv), torch.float32),
     }
+    views["q8"] = views["q8_padded"][..., :D]
+    views["k8"] = views["k8_padded"][..., :D]
+    views["v8t"] = views["v8t_padded"][:, :, :D]
     return ws, views
 
 
 def fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, workspace=None):
     """FP8 (e4m3) forward through ffpa_fwd_fp8: bf16/fp16 in, O in the input
-    dtype and fp32 LSE out. D in FP8_HEAD_DIMS. Returns (o, lse)."""
+    dtype and fp32 LSE out; D a multiple of 32 in [64, 1024]. Returns (o, lse)."""
     q, k, v = _fp8_args(q, k, v)
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape
@@ -220,31 +228,32 @@ def fwd_fp8_quantized(workspace, shape_q, shape_k, dtype, causal: bool = False, 
     return o, l
 
 
-def bwd_workspace_bytes(q, k, causal: bool | None = None) -> int:
-    """Backward workspace bytes: the row statistics only (causal None), or with
-    room for the stored dS and P where that path applies
-    (ffpa_bwd_workspace_bytes_ds)."""
+# Default cap of the backward workspace bwd() and varlen_bwd() allocate: the
+# stored P^T / dS^T tiles of every head when they fit in it (8.6 GB at
+# B1 H32 N8192 D512), else of as many kv groups per chunk as fit. A fixed
+# size, so that the path a call takes never depends on what else is allocated.
+BWD_WORKSPACE_BUDGET = 16 << 30
+
+
+def bwd_workspace_bytes(q, k, causal: bool | None = None, budget: int | None = None) -> int:
+    """Backward workspace bytes: the row statistics only (causal None); with
+    room for the stored dS and P tiles of every head where that path applies
+    (budget None: ffpa_bwd_workspace_bytes_ds); or the largest useful size
+    within `budget` bytes (ffpa_bwd_workspace_bytes_budget: the tiles of every
+    head, else of a chunk of kv groups, else the row statistics)."""
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape
     if causal is None:
         return int(_ffi.ffpa_bwd_workspace_bytes(_dt(q), B, Hq, Hkv, Nq, Nkv, D))
-    return int(_ffi.ffpa_bwd_workspace_bytes_ds(_dt(q), B, Hq, Hkv, Nq, Nkv, D, int(bool(causal))))
+    if budget is None:
+        return int(_ffi.ffpa_bwd_workspace_bytes_ds(_dt(q), B, Hq, Hkv, Nq, Nkv, D, int(bool(causal))))
+    return int(_ffi.ffpa_bwd_workspace_bytes_budget(_dt(q), B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)),
+                                                     int(budget)))
 
 
-DS_WORKSPACE_FRACTION = 0.25  # largest share of free device memory bwd() spends on the stored dS and P
-
-
-def bwd_workspace(q, k, causal: bool):
-    """A backward workspace: with the stored-dS and -P room when it applies and
-    takes at most DS_WORKSPACE_FRACTION of the free device memory, else the
-    small one."""
-    small = bwd_workspace_bytes(q, k)
-    big = bwd_workspace_bytes(q, k, causal)
-    n = small
-    if big > small:
-        free, _ = torch.cuda.mem_get_info(q.device)
-        if big <= DS_WORKSPACE_FRACTION * free:
-            n = big
+def bwd_workspace(q, k, causal: bool, budget: int = BWD_WORKSPACE_BUDGET):
+    """A backward workspace of the largest useful size within `budget` bytes."""
+    n = bwd_workspace_bytes(q, k, causal, budget)
     return torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
 
 
@@ -253,8 +262,9 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
     """Dense backward through ffpa_bwd_strided (views, no copy), or ffpa_bwd_stages
     for a subset of its launches (bit 0 preprocess, bit 1 dV, bit 2 dQ, bit 3 dK,
     bit 4 dQ from the dS a dK stage stored, bit 5 dV storing P / dK reading it;
-    contiguous tensors). Without a workspace, one with room for the stored dS
-    and P is allocated where that path applies (bwd_workspace). Returns
+    contiguous tensors). Without a workspace, one of at most
+    BWD_WORKSPACE_BUDGET bytes is allocated (bwd_workspace): the stored-tile
+    path for every head, or in chunks of kv groups, where it applies. Returns
     (dq, dk, dv)."""
     q, k, v, o, dout = _dense(q, k, v, o, dout)
     lse = lse.contiguous()
@@ -336,11 +346,23 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, 
     return o, lse
 
 
+def varlen_workspace_bytes(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k, causal: bool,
+                           budget: int = BWD_WORKSPACE_BUDGET) -> int:
+    """Largest useful packed-backward workspace within `budget` bytes
+    (ffpa_varlen_bwd_workspace_bytes_budget)."""
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    batch = cu_seqlens_q.numel() - 1
+    return int(_ffi.ffpa_varlen_bwd_workspace_bytes_budget(_dt(q), batch, Tq, Tk, int(max_seqlen_q),
+                                                            int(max_seqlen_k), Hq, Hkv, D, int(bool(causal)),
+                                                            int(budget)))
+
+
 def varlen_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False,
                scale=None, workspace=None):
-    """Packed backward through ffpa_varlen_bwd. Without a workspace, one with
-    room for the stored dS and P tiles is allocated where that path applies and
-    takes at most DS_WORKSPACE_FRACTION of the free device memory. Returns
+    """Packed backward through ffpa_varlen_bwd. Without a workspace, one of at
+    most BWD_WORKSPACE_BUDGET bytes is allocated (the stored-tile path for
+    every head, or in chunks of kv groups, where it applies). Returns
     (dq, dk, dv)."""
     q, k, v, o, dout = _prep(q, k, v, o, dout)
     lse = lse.contiguous()
@@ -350,10 +372,7 @@ def varlen_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, 
     batch = cq.numel() - 1
     sizes = (_dt(q), batch, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D)
     if workspace is None:
-        n = int(_ffi.ffpa_varlen_bwd_workspace_bytes(*sizes))
-        big = int(_ffi.ffpa_varlen_bwd_workspace_bytes_ds(*sizes, int(bool(causal))))
-        if big > n and big <= DS_WORKSPACE_FRACTION * torch.cuda.mem_get_info(q.device)[0]:
-            n = big
+        n = int(_ffi.ffpa_varlen_bwd_workspace_bytes_budget(*sizes, int(bool(causal)), BWD_WORKSPACE_BUDGET))
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     st = _ffi.ffpa_varlen_bwd(_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),

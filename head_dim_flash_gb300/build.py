@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libffpa.so")
-SOURCES = ("api.cu", "host.cu", "fwd.cu", "bwd.cu", "xchg.cu", "xchg2.cu", "decode.cu", "fp8.cu", "dsq.cu", "noalloc.cu")
+SOURCES = ("api.cu", "host.cu", "bwd.cu", "xchg.cu", "xchg2.cu", "decode.cu", "fp8.cu", "dsq.cu", "noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,6 +1,7 @@
 // C ABI entry points (declared in include/ffpa.h): argument validation,
 // workspace carving, device status word, and dispatch to the kernels.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -107,6 +108,9 @@ ffpa_status launch_result(cudaError_t e, const char* what)
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Work units one launch can index (unit_grid: 65535 x 65535 clusters).
+constexpr long long kMaxUnits = 65535LL * 65535LL;
+
 size_t ws_bytes(long rows) { return rows <= 0 ? 0 : 2 * align256(static_cast<size_t>(rows) * sizeof(float)); }
 
 // Strides of a contiguous [B, H, N, D] tensor, and of a packed [T, H, D] one.
@@ -160,7 +164,10 @@ ffpa::Problem dense_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int 
 ffpa_status check_dense_sizes(int B, int Hq, int Nq, int Nkv)
 {
     if (B < 0 || Nq < 0 || Nkv < 0) return fail(FFPA_ERR_INVALID_VALUE, "negative size B=%d Nq=%d Nkv=%d", B, Nq, Nkv);
-    if (static_cast<long>(B) * Hq > 65535) return fail(FFPA_ERR_NOT_SUPPORTED, "B*Hq=%ld exceeds 65535", (long)B * Hq);
+    // (batch, head) pairs index the launch grids as int
+    if (static_cast<long>(B) * Hq > INT_MAX || static_cast<long>(B) * Hq * ((Nq > Nkv ? Nq : Nkv) / 128 + 1) > kMaxUnits)
+        return fail(FFPA_ERR_NOT_SUPPORTED, "B*Hq=%ld with N=%d exceeds the launch grid's %lld work units", (long)B * Hq,
+                    Nq > Nkv ? Nq : Nkv, kMaxUnits);
     return FFPA_OK;
 }
 
@@ -169,8 +176,10 @@ ffpa_status check_varlen_sizes(int batch, int total_q, int total_k, int max_q, i
 {
     if (batch < 0 || total_q < 0 || total_k < 0 || max_q < 0 || max_k < 0)
         return fail(FFPA_ERR_INVALID_VALUE, "negative varlen size");
-    if (static_cast<long>(batch) * Hq > 65535)
-        return fail(FFPA_ERR_NOT_SUPPORTED, "batch*Hq=%ld exceeds 65535", (long)batch * Hq);
+    if (static_cast<long>(batch) * Hq > INT_MAX ||
+        static_cast<long>(batch) * Hq * ((max_q > max_k ? max_q : max_k) / 128 + 1) > kMaxUnits)
+        return fail(FFPA_ERR_NOT_SUPPORTED, "batch*Hq=%ld with max_seqlen %d exceeds the launch grid's %lld work units",
+                    (long)batch * Hq, max_q > max_k ? max_q : max_k, kMaxUnits);
     if (batch > 0 && (!cu_q || !cu_k))
         return fail(FFPA_ERR_INVALID_VALUE, "cu_seqlens_q and cu_seqlens_k are both required (varlen-one-sided)");
     if ((reinterpret_cast<uintptr_t>(cu_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_k) & 3u))
@@ -193,7 +202,10 @@ ffpa_status run_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v, 
     FFPA_TRY(check_ptr(k, q_rows > 0 && k_rows > 0, "k"));
     FFPA_TRY(check_ptr(v, q_rows > 0 && k_rows > 0, "v"));
     if (q_rows == 0) return ok();
-    ffpa::FwdArgs a{};
+    // the forward operation of the cluster-exchange kernel: each unit of a
+    // cluster scores its own key tiles, the units agree on the running row
+    // maximum and exchange P, and every unit accumulates its head-dim slab of O
+    ffpa::XArgs a{};
     a.pb = pb;
     FFPA_TRY(device_ctl(&a.ctl));
     a.bf16 = dt == FFPA_BF16;
@@ -202,7 +214,57 @@ ffpa_status run_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v, 
     a.v = v;
     a.o = o;
     a.lse = lse;
-    return launch_result(ffpa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)), "forward launch");
+    return launch_result(ffpa::launch_xchg(ffpa::XOP_FWD, a, reinterpret_cast<cudaStream_t>(stream)),
+                         "forward launch");
+}
+
+// Layout of the stored-tile part of a backward workspace (byte offsets; 0 =
+// absent) for a workspace of `bytes` whose row statistics take `need`.
+struct StoredPlan {
+    size_t ds_off, p_off;
+    int chunk_groups;  // > 0: chunks of this many kv groups
+    size_t used;       // bytes the plan uses
+};
+
+StoredPlan stored_plan(const ffpa::Problem& pb, size_t need, size_t bytes, bool chunks_allowed)
+{
+    StoredPlan s{0, 0, 0, need};
+    if (!ffpa::dsq_supported(pb)) return s;
+    const size_t t_all = ffpa::dsq_ds_bytes(pb), t_g = ffpa::dsq_group_bytes(pb);
+    if (bytes >= need + align256(t_all) + t_all) {  // every head at once
+        s.ds_off = need;
+        s.p_off = need + align256(t_all);
+        s.used = s.p_off + t_all;
+        return s;
+    }
+    if (chunks_allowed && t_g > 0 && bytes >= need + align256(t_g) + t_g) {
+        // as many kv groups per chunk as fit, then the chunks evened out
+        // (ceil(Hkv / chunks) groups each), so that no launch is a small tail
+        long ng = static_cast<long>((bytes - need) / (2 * t_g + 256));
+        if (ng < 1) ng = 1;
+        while (ng > 1 && need + align256(ng * t_g) + ng * t_g > bytes) --ng;
+        const long chunks = (pb.Hkv + ng - 1) / ng;
+        ng = (pb.Hkv + chunks - 1) / chunks;
+        s.chunk_groups = static_cast<int>(ng);
+        s.ds_off = need;
+        s.p_off = need + align256(ng * t_g);
+        s.used = s.p_off + ng * t_g;
+        return s;
+    }
+    if (bytes >= need + t_all) {  // dS^T of every head
+        s.ds_off = need;
+        s.used = need + t_all;
+    }
+    return s;
+}
+
+// Largest useful backward workspace within `budget` bytes: every head's tiles
+// if they fit, else the largest chunk of kv groups that fits (evened out),
+// else the row statistics alone.
+size_t budget_bytes(const ffpa::Problem& pb, size_t need, size_t budget)
+{
+    if (budget <= need) return need;
+    return stored_plan(pb, need, budget, true).used;
 }
 
 ffpa_status run_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -229,16 +291,19 @@ ffpa_status run_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, 
     ffpa::BwdArgs a{};
     a.pb = pb;
     a.stages = stages & 63u;
-    // a workspace with room for dS^T after the row statistics has the dK launch
-    // store dS and dQ formed by a GEMM over it (where that path applies); room
-    // for P^T after that as well has it store P^T and dV formed the same way
+    // The workspace after the row statistics decides the stored-tile path
+    // (where it applies): room for dS^T and P^T of every head has the dK
+    // launch store both, and dV and dQ are GEMMs over them; room for both
+    // tile sets of at least one kv group (and a call that runs dV, dK and dQ)
+    // runs that path in chunks of as many groups as fit; room for dS^T of
+    // every head alone stores dS only (dV recomputes); less recomputes.
     a.ds = nullptr;
     a.p = nullptr;
-    if (ffpa::dsq_supported(pb) && workspace_bytes >= need + ffpa::dsq_ds_bytes(pb)) {
-        a.ds = static_cast<char*>(workspace) + need;
-        const size_t p_off = need + align256(ffpa::dsq_ds_bytes(pb));
-        if (workspace_bytes >= p_off + ffpa::dsq_ds_bytes(pb)) a.p = static_cast<char*>(workspace) + p_off;
-    }
+    a.chunk_groups = 0;
+    const StoredPlan plan = stored_plan(pb, need, workspace_bytes, (stages & 14u) == 14u && !(stages & 48u));
+    if (plan.ds_off) a.ds = static_cast<char*>(workspace) + plan.ds_off;
+    if (plan.p_off) a.p = static_cast<char*>(workspace) + plan.p_off;
+    a.chunk_groups = plan.chunk_groups;
     if ((a.stages & 16u) && a.ds == nullptr)
         return fail(FFPA_ERR_INVALID_VALUE, "stage bit 4 (dQ from stored dS) needs the larger workspace of "
                                             "ffpa_bwd_workspace_bytes_ds on a dense problem with D % 64 == 0, D <= 1024");
@@ -345,10 +410,10 @@ ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v
     FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
     FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
     if (D % 64 != 0) return fail(FFPA_ERR_NOT_SUPPORTED, "decode path: D=%d must be a multiple of 64", D);
-    if (Hq > 0 && static_cast<long>(B) * Hkv * ((static_cast<long>(Hq / Hkv) * Nq + ffpa::kDecodeRows - 1) /
-                                                ffpa::kDecodeRows) > 65535)
-        return fail(FFPA_ERR_NOT_SUPPORTED, "decode path: B*Hkv*ceil((Hq/Hkv)*Nq/%d) exceeds the grid limit 65535",
-                    ffpa::kDecodeRows);
+    if (Hq > 0 && static_cast<long long>(B) * Hkv * ((static_cast<long long>(Hq / Hkv) * Nq + ffpa::kDecodeRows - 1) /
+                                                     ffpa::kDecodeRows) > kMaxUnits)
+        return fail(FFPA_ERR_NOT_SUPPORTED, "decode path: B*Hkv*ceil((Hq/Hkv)*Nq/%d) exceeds the grid's %lld units",
+                    ffpa::kDecodeRows, kMaxUnits);
     const long q_rows = static_cast<long>(B) * Hq * Nq;
     const long k_rows = static_cast<long>(B) * Hkv * Nkv;
     FFPA_TRY(check_view(q, q_rows > 0, "q", B, Hq, Nq));
@@ -381,7 +446,8 @@ ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v
 
 size_t ffpa_fp8_workspace_layout(int B, int Hq, int Hkv, int Nq, int Nkv, int D, size_t* offsets)
 {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nkv < 0 || D <= 0 || Hq % Hkv != 0 || D % 128 != 0) return 0;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nkv < 0 || D < 64 || D > 1024 || Hq % Hkv != 0 || D % 32 != 0)
+        return 0;
     const ffpa::Fp8Layout L = ffpa::fp8_layout(B, Hq, Hkv, Nq, Nkv, D);
     if (offsets) {
         offsets[0] = L.q8;
@@ -411,8 +477,6 @@ ffpa_status check_fp8(ffpa_dtype dt, const ffpa_view& q, const ffpa_view& k, con
 {
     FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
     FFPA_TRY(check_dense_sizes(B, Hq, Nq, Nkv));
-    if (D % 256 != 0 || D > 768)
-        return fail(FFPA_ERR_NOT_SUPPORTED, "fp8 forward: D=%d must be 256, 512 or 768", D);
     const long q_rows = static_cast<long>(B) * Hq * Nq;
     if (q_rows > 0 && Nkv < 1) return fail(FFPA_ERR_NOT_SUPPORTED, "fp8 forward: Nkv must be >= 1");
     FFPA_TRY(check_view(q, q_rows > 0, "q", B, Hq, Nq));
@@ -515,6 +579,14 @@ size_t ffpa_bwd_workspace_bytes_ds(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq
     return ffpa::dsq_supported(pb) ? small + align256(ffpa::dsq_ds_bytes(pb)) + ffpa::dsq_ds_bytes(pb) : small;
 }
 
+size_t ffpa_bwd_workspace_bytes_budget(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal,
+                                       size_t budget)
+{
+    const size_t small = ffpa_bwd_workspace_bytes(dt, B, Hq, Hkv, Nq, Nkv, D);
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nkv <= 0 || Hq % Hkv != 0) return small;
+    return budget_bytes(dense_problem(B, Hq, Hkv, Nq, Nkv, D, causal, 1.f), small, budget);
+}
+
 size_t ffpa_bwd_workspace_bytes(ffpa_dtype, int B, int Hq, int, int Nq, int, int)
 {
     if (B < 0 || Hq < 0 || Nq < 0) return 0;
@@ -612,6 +684,19 @@ size_t ffpa_varlen_bwd_workspace_bytes_ds(ffpa_dtype dt, int batch, int total_q,
     return ffpa::dsq_supported(pb) ? small + align256(ffpa::dsq_ds_bytes(pb)) + ffpa::dsq_ds_bytes(pb) : small;
 }
 
+size_t ffpa_varlen_bwd_workspace_bytes_budget(ffpa_dtype dt, int batch, int total_q, int total_k, int max_seqlen_q,
+                                              int max_seqlen_k, int Hq, int Hkv, int D, int causal, size_t budget)
+{
+    const size_t small =
+        ffpa_varlen_bwd_workspace_bytes(dt, batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, Hkv, D);
+    if (batch <= 0 || total_q <= 0 || total_k <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || Hq <= 0 ||
+        Hkv <= 0 || Hq % Hkv != 0)
+        return small;
+    return budget_bytes(varlen_problem(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, causal, 1.f,
+                                       nullptr, nullptr),
+                        small, budget);
+}
+
 ffpa_status ffpa_varlen_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
                             const int* cu_seqlens_k, int batch, int total_q, int total_k, int max_seqlen_q,
@@ -640,6 +725,12 @@ ffpa_status ffpa_get_status(ffpa_stream_t stream)
     cudaMemcpyToSymbol(g_ffpa_status_word, &zero, sizeof(zero));
     if ((word & 0xffu) == ffpa::DEV_TIMEOUT)
         return fail(FFPA_ERR_TIMEOUT, "a device wait timed out (site %u, block %u)", (word >> 8) & 0xffu, word >> 16);
+    if ((word & 0xffu) == ffpa::DEV_INVALID)
+        return fail(FFPA_ERR_INVALID_VALUE,
+                    "packed sequence %u breaks the varlen contract: its cu_seqlens entries are negative, decrease or "
+                    "run past total_q / total_k, or its length exceeds max_seqlen_q / max_seqlen_k (which size the "
+                    "launch); the outputs of that call are undefined (site 0x%02x)",
+                    word >> 16, (word >> 8) & 0xffu);
     return fail(FFPA_ERR_CUDA, "device status word 0x%08x", word);
 }
 

@@ -119,7 +119,7 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
     const bool use_p = use_ds && a.p != nullptr;
     if ((a.stages & 32u) && !use_p) return cudaErrorInvalidConfiguration;  // no P buffer
     const bool p_mode = use_p && ((a.stages & 32u) || ((a.stages & 2u) && (a.stages & 8u)));
-    auto tile_gemm = [&](bool dv) {
+    auto tile_gemm = [&](bool dv, int g0 = 0, int ng = 0) {
         DsqArgs d{};
         d.pb = pb;
         d.bf16 = BF16;
@@ -127,11 +127,37 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
         d.tiles = dv ? a.p : a.ds;
         d.rhs = dv ? a.dO : a.k;
         d.out = dv ? a.dv : a.dq;
+        d.g0 = g0;
+        d.ng = ng;
         d.ctl = a.ctl;
         // a plain launch: the GEMM reads what the dK launch wrote
         return launch_dsq(d, st);
     };
     x.pdl = 0;
+    if (a.chunk_groups > 0) {
+        // Stored tiles in chunks of kv groups (the workspace holds one chunk's
+        // P^T and dS^T): per chunk, dK over its kv heads (storing the tiles of
+        // their query heads), then dV = P^T dO for those kv heads and
+        // dQ = scale dS K for those query heads. A group's gradients are
+        // complete within its chunk, so nothing accumulates across chunks.
+        // Every launch is a plain one: a chunk's dK rewrites the buffers the
+        // previous chunk's GEMMs read.
+        if (!use_p || (a.stages & 14u) != 14u || (a.stages & 48u)) return cudaErrorInvalidConfiguration;
+        for (int g0 = 0; g0 < pb.Hkv; g0 += a.chunk_groups) {
+            const int ng = min(a.chunk_groups, pb.Hkv - g0);
+            XArgs xk = x;
+            xk.store_ds = 1;
+            xk.ds = a.ds;
+            xk.store_p = 1;
+            xk.p = a.p;
+            xk.g0 = g0;
+            xk.ng = ng;
+            if ((e = launch_xchg(XOP_DK, xk, st)) != cudaSuccess) return e;
+            if ((e = tile_gemm(true, g0, ng)) != cudaSuccess) return e;
+            if ((e = tile_gemm(false, g0, ng)) != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     if (!kv_empty && (a.stages & 2u) && !p_mode) {
         if ((e = launch_xchg(XOP_DV, x, st)) != cudaSuccess) return e;
         x.pdl = 1;

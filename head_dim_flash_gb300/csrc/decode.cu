@@ -106,8 +106,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const Problem& pb = a.pb;
     const int G = pb.Hq / pb.Hkv;
     const int R = G * pb.Nq;            // query rows of the group
-    const int rb = blockIdx.y % gm.rblocks;  // this CTA's block of kDecRows of them
-    const int unit = blockIdx.y / gm.rblocks;
+    // (batch, kv head, row block) in linear order, row block fastest
+    const long long u = unit_id();
+    if (u >= static_cast<long long>(pb.B) * pb.Hkv * gm.rblocks) return;  // past the last unit
+    const int rb = static_cast<int>(u % gm.rblocks);  // this CTA's block of kDecRows of them
+    const int unit = static_cast<int>(u / gm.rblocks);
     const int r0 = rb * kDecRows;        // group row of the CTA's row 0
     const int split = blockIdx.x;
     const int b = unit / pb.Hkv;
@@ -467,7 +470,8 @@ DecodePlan decode_plan(const Problem& pb)
     DecodePlan p{};
     p.chunks = (pb.D + 63) / 64;
     p.kt = p.chunks > 8 ? 16 : 32;
-    p.rblocks = max(1, (pb.Hq / max(1, pb.Hkv) * pb.Nq + kDecodeRows - 1) / kDecodeRows);
+    const long long rb = (static_cast<long long>(pb.Hq / max(1, pb.Hkv)) * pb.Nq + kDecodeRows - 1) / kDecodeRows;
+    p.rblocks = static_cast<int>(rb < 1 ? 1 : (rb > 0x7fffffffLL ? 0x7fffffffLL : rb));
     const long units = max(1L, static_cast<long>(pb.B) * pb.Hkv * p.rblocks);
     const int tiles = max(1, (pb.Nkv + p.kt - 1) / p.kt);
     const long sms = num_sms() > 0 ? num_sms() : 148;
@@ -515,7 +519,9 @@ cudaError_t launch_variant(const FwdArgs& a, const DecGeo& gm, const CUtensorMap
     const int smem = kDecStages * gm.stage_bytes + kDecRedBytes;
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(gm.splits, a.pb.B * a.pb.Hkv * gm.rblocks);
+    dim3 grid;
+    if (!unit_grid(gm.splits, static_cast<long long>(a.pb.B) * a.pb.Hkv * gm.rblocks, &grid))
+        return cudaErrorInvalidConfiguration;
     decode_kernel<BF16><<<grid, kDecThreads, smem, s>>>(tk, tv, a, gm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long rows = static_cast<long>(a.pb.B) * a.pb.Hq * a.pb.Nq;

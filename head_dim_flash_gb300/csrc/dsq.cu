@@ -51,6 +51,8 @@ static_assert(sizeof(QStatic) == 1024, "static shared block must be exactly 1 Ki
 struct QGeo {
     int nj_max;       // pair MMAs (N = 256, the last one of a slab N = 128 if it is narrower) of the widest slab
     int stage_bytes;  // ring slot per CTA: A (16 KiB) + B (nj_max x 16 KiB)
+    int n_rt;         // row tiles of 256 per (batch, head) in the grid (of the longest sequence)
+    int n_bz;         // (batch, head) entries in the grid
 };
 
 template <bool BF16, bool DV>
@@ -64,26 +66,32 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const bool leader = rh == 0;
     const int G = pb.Hq / pb.Hkv;
     // dQ: (b, query head h); dV: (b, KV head hk), the group's query heads hk*G ..
-    const int hb = DV ? pb.Hkv : pb.Hq;
-    const int b = blockIdx.z / hb, h = blockIdx.z % hb, hk = DV ? h : h / G;
+    // units in linear pair order: row tile fastest, then (b, head)
+    const long long unit = unit_id();
+    if (unit >= static_cast<long long>(gm.n_rt) * gm.n_bz) return;  // past the last unit: uniform over the pair
+    const int rtile = static_cast<int>(unit % gm.n_rt), bz = static_cast<int>(unit / gm.n_rt);
+    // (b, head) over the kv groups [g0, g0 + ng) of the launch: dV takes their
+    // kv heads, dQ their query heads; the tile buffer holds those query heads
+    // only, the first at index 0
+    const int ng = a.ng > 0 ? a.ng : pb.Hkv;
+    const int hb = DV ? ng : ng * G;
+    const int b = bz / hb, h = (DV ? a.g0 : a.g0 * G) + bz % hb, hk = DV ? h : h / G;
+    const int th0 = a.g0 * G;  // query head of tile buffer head 0
     // the sequence: lengths, and (packed batches) its first query / key token
     // and the first row of its key rows in the tile buffers (one 256-row pad
     // per sequence, so that no row tile reaches the next sequence's rows)
     int lq = pb.Nq, lk = pb.Nkv, tq0 = 0, tk0 = 0, tr0 = 0, bco = b;
     if (pb.varlen) {
-        tq0 = pb.cu_q[b];
-        lq = pb.cu_q[b + 1] - tq0;
-        tk0 = pb.cu_k[b];
-        lk = pb.cu_k[b + 1] - tk0;
+        if (!varlen_seq(pb, b, a.ctl.status, VS_GEMM, tq0, lq, tk0, lk)) return;  // uniform over the pair
         tr0 = tk0 + 256 * b;
         bco = 0;
     }
     const int off = lk - lq;  // causal: key j legal for query i iff j <= i + off
     const int n_rows = DV ? lk : lq;
     const int n_rt_seq = (n_rows + 255) / 256;
-    if (static_cast<int>(blockIdx.y) >= n_rt_seq) return;  // uniform over the pair, before any barrier
+    if (rtile >= n_rt_seq) return;  // uniform over the pair, before any barrier
     // causal: the longest tiles first (dQ: the last query tiles, dV: the first key tiles)
-    const int tile = (pb.causal && !DV) ? n_rt_seq - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
+    const int tile = (pb.causal && !DV) ? n_rt_seq - 1 - rtile : rtile;
     const int row0 = tile * 256;
     const int rc = row0 + 128 * rh;  // my first row (query for dQ, key for dV)
     // K blocks of 64 (both CTAs of the pair alike): dQ keys [0, key_end);
@@ -162,7 +170,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                     const int i0 = (kb_lo + it % n_kb) * 64;  // first query of the block
                     if (lane == 0) {
                         // A: P^T rows = my 128 keys, queries [i0, +64)
-                        tma_load_4d_pair(st, &tA, fb, i0, tr0 + rc, hq, bco);
+                        tma_load_4d_pair(st, &tA, fb, i0, tr0 + rc, hq - th0, bco);
                     } else {
                         // B: dO rows = queries [i0, +64), my half of each MMA's N columns
                         // (a 128-column box; an N = 128 MMA reads its first 64)
@@ -174,8 +182,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
                     const int kb = it;
                     if (lane == 0) {
                         // A: dS^T rows = keys [64 kb, +64), my 128 queries as two 64-query boxes
-                        tma_load_4d_pair(st, &tA, fb, rc, tr0 + kb * 64, h, bco);
-                        tma_load_4d_pair(st + 8192, &tA, fb, rc + 64, tr0 + kb * 64, h, bco);
+                        tma_load_4d_pair(st, &tA, fb, rc, tr0 + kb * 64, h - th0, bco);
+                        tma_load_4d_pair(st + 8192, &tA, fb, rc + 64, tr0 + kb * 64, h - th0, bco);
                     } else {
                         // B: K rows = keys [64 kb, +64), my half of each MMA's N columns
                         for (int j = 0; j < nj; ++j)
@@ -295,16 +303,21 @@ size_t dsq_ds_bytes(const Problem& pb)
     return static_cast<size_t>(pb.varlen ? 1 : pb.B) * pb.Hq * tile_rows(pb) * ldq * 2;
 }
 
-bool make_ds_map(CUtensorMap* m, const void* ds, const Problem& pb, bool bf16, int box_rows)
+size_t dsq_group_bytes(const Problem& pb)
+{
+    return pb.Hkv > 0 ? dsq_ds_bytes(pb) / pb.Hkv : 0;  // G query heads of every batch entry
+}
+
+bool make_ds_map(CUtensorMap* m, const void* ds, const Problem& pb, bool bf16, int box_rows, int heads)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     // (packed batches: Nq is the longest sequence, and one batch of tile_rows rows)
     const cuuint64_t ldq = (static_cast<cuuint64_t>(pb.Nq) + 7) & ~static_cast<cuuint64_t>(7);
     const cuuint64_t rows = tile_rows(pb);
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(pb.Nq), rows, static_cast<cuuint64_t>(pb.Hq),
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(pb.Nq), rows, static_cast<cuuint64_t>(heads),
                                 static_cast<cuuint64_t>(pb.varlen ? 1 : pb.B)};
-    const cuuint64_t strides[3] = {ldq * 2, rows * ldq * 2, static_cast<cuuint64_t>(pb.Hq) * rows * ldq * 2};
+    const cuuint64_t strides[3] = {ldq * 2, rows * ldq * 2, static_cast<cuuint64_t>(heads) * rows * ldq * 2};
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ds),
@@ -319,9 +332,12 @@ cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s)
     CUtensorMap tA, tB;
     // dQ: dS^T as 64 queries x 64 key rows boxes, K rows; dV: P^T as 64 queries x
     // 128 key rows boxes, dO rows (the query side)
-    const bool okm = a.dv ? make_ds_map(&tA, a.tiles, pb, a.bf16, 128) &&
+    const int G = pb.Hq / pb.Hkv;
+    const int ng = a.ng > 0 ? a.ng : pb.Hkv;  // kv groups of this launch (their query heads in the tiles)
+    if (a.g0 < 0 || a.g0 + ng > pb.Hkv) return cudaErrorInvalidValue;
+    const bool okm = a.dv ? make_ds_map(&tA, a.tiles, pb, a.bf16, 128, ng * G) &&
                                 make_slab_map(&tB, a.rhs, pb, false, a.bf16, 64, 2, pb.vdo)
-                          : make_ds_map(&tA, a.tiles, pb, a.bf16, 64) &&
+                          : make_ds_map(&tA, a.tiles, pb, a.bf16, 64, ng * G) &&
                                 make_slab_map(&tB, a.rhs, pb, true, a.bf16, 64, 2, pb.vk);
     if (!okm) return cudaErrorInvalidValue;
     QGeo gm{};
@@ -329,9 +345,11 @@ cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s)
     gm.stage_bytes = 16384 * (1 + gm.nj_max);
     const int n_slab = (pb.D + 511) / 512;
     const int smem = kQStages * gm.stage_bytes;
-    const dim3 grid = a.dv ? dim3(2 * n_slab, (pb.Nkv + 255) / 256, pb.B * pb.Hkv)
-                           : dim3(2 * n_slab, (pb.Nq + 255) / 256, pb.B * pb.Hq);
-    if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
+    gm.n_rt = a.dv ? (pb.Nkv + 255) / 256 : (pb.Nq + 255) / 256;
+    gm.n_bz = a.dv ? pb.B * ng : pb.B * ng * G;
+    if (gm.n_rt == 0 || gm.n_bz == 0) return cudaSuccess;
+    dim3 grid;
+    if (!unit_grid(2 * n_slab, static_cast<long long>(gm.n_rt) * gm.n_bz, &grid)) return cudaErrorInvalidConfiguration;
     auto kern = a.dv ? (a.bf16 ? dsq_kernel<true, true> : dsq_kernel<false, true>)
                      : (a.bf16 ? dsq_kernel<true, false> : dsq_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

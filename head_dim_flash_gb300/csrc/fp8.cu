@@ -5,10 +5,13 @@
 // Here the quantization is one pass ahead of the attention kernel (every
 // K/V tile is read by many row tiles, so it is quantized once, not once per
 // use) and writes the operands in the layouts the tensor cores read:
-//   q8  [B, Hq,  Nq,  D] e4m3, rows of D bytes (K-major for S = Q K^T)
-//   k8  [B, Hkv, Nkv, D] e4m3
-//   v8t [B, Hkv, D, ldv] e4m3, V transposed (keys contiguous, ldv = Nkv
+//   q8  [B, Hq,  Nq,  Dp] e4m3, rows of Dp bytes (K-major for S = Q K^T)
+//   k8  [B, Hkv, Nkv, Dp] e4m3
+//   v8t [B, Hkv, Dp, ldv] e4m3, V transposed (keys contiguous, ldv = Nkv
 //       rounded up to 16) so that O += P V reads it K-major
+// with the head dim padded to Dp = D rounded up to 128 (whole 128-byte code
+// chunks for the tensor maps and the MMAs): the pad holds zero codes, which
+// add nothing to the scores, and the output columns past D are not stored.
 //   sq [B*Hq], sk [B*Hkv], sv [B*Hkv] fp32 dequantization scales
 // One scale per (batch, head) and tensor: amax = max |x| over the head,
 // scale = amax / 448, inv = 448 / amax (fp32, correctly rounded; 1 and 1 for
@@ -19,6 +22,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_common.cuh"
 
 namespace ffpa {
 namespace {
@@ -33,6 +37,7 @@ struct QArgs {
     const void *q, *k, *v;
     View vq, vk, vv;
     int B, Hq, Hkv, Nq, Nkv, D, ldv;
+    int Dp;                 // code row length: D rounded up to 128 (zero codes past D)
     int nsq, nsk;           // row blocks per q head / per k or v head
     uint8_t *q8, *k8, *v8t;
     float *sq, *sk, *sv;
@@ -80,8 +85,10 @@ __device__ __forceinline__ float block_max(float m, float* red)
 __global__ void __launch_bounds__(256) amax_kernel(const QArgs a, bool bf16)
 {
     __shared__ float red[8];
+    const long long y = unit_id();  // head of q, k or v
+    if (y >= static_cast<long long>(a.B) * (a.Hq + 2 * a.Hkv)) return;
     int t, hi;
-    tensor_of(a, blockIdx.y, t, hi);
+    tensor_of(a, static_cast<int>(y), t, hi);
     const int N = t == 0 ? a.Nq : a.Nkv;
     const int ns = t == 0 ? a.nsq : a.nsk;
     if (static_cast<int>(blockIdx.x) >= ns) return;
@@ -128,20 +135,23 @@ __device__ __forceinline__ void head_scale(const QArgs& a, int t, int hi, float*
 __global__ void __launch_bounds__(256) quant_rows_kernel(const QArgs a, bool bf16)
 {
     __shared__ float sm[2];
+    const long long y = unit_id();  // head of q or k
+    if (y >= static_cast<long long>(a.B) * (a.Hq + a.Hkv)) return;
     int t, hi;
-    tensor_of(a, blockIdx.y, t, hi);
+    tensor_of(a, static_cast<int>(y), t, hi);
     const int N = t == 0 ? a.Nq : a.Nkv;
     const int ns = t == 0 ? a.nsq : a.nsk;
     if (static_cast<int>(blockIdx.x) >= ns) return;
     head_scale(a, t, hi, sm);
     const float inv = sm[1];
     if (blockIdx.x == 0 && threadIdx.x == 0) (t == 0 ? a.sq : a.sk)[hi] = sm[0];
-    uint8_t* out = (t == 0 ? a.q8 : a.k8) + static_cast<size_t>(hi) * N * a.D;
+    uint8_t* out = (t == 0 ? a.q8 : a.k8) + static_cast<size_t>(hi) * N * a.Dp;
     const int n0 = blockIdx.x * kQRows, n1 = min(N, n0 + kQRows);
-    const int units = a.D / 8;
+    const int units = a.Dp / 8, in_units = a.D / 8;  // 8 codes per unit; units past D write zero codes
     for (int e = threadIdx.x; e < (n1 - n0) * units; e += blockDim.x) {
         const int n = n0 + e / units, u8 = e % units;
-        const uint4 w = *reinterpret_cast<const uint4*>(row_ptr(a, t, hi, n) + u8 * 8);
+        const uint4 w = u8 < in_units ? *reinterpret_cast<const uint4*>(row_ptr(a, t, hi, n) + u8 * 8)
+                                      : make_uint4(0, 0, 0, 0);
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[2];
 #pragma unroll
@@ -152,7 +162,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const QArgs a, bool bf1
             const float x3 = to_f(static_cast<uint16_t>(u[2 * i + 1] >> 16), bf16) * inv;
             o[i] = static_cast<uint32_t>(cvt_e4m3x2(x0, x1)) | (static_cast<uint32_t>(cvt_e4m3x2(x2, x3)) << 16);
         }
-        *reinterpret_cast<uint2*>(out + static_cast<size_t>(n) * a.D + u8 * 8) = make_uint2(o[0], o[1]);
+        *reinterpret_cast<uint2*>(out + static_cast<size_t>(n) * a.Dp + u8 * 8) = make_uint2(o[0], o[1]);
     }
 }
 
@@ -162,19 +172,21 @@ __global__ void __launch_bounds__(256) quant_vt_kernel(const QArgs a, bool bf16)
 {
     __shared__ float sm[2];
     __shared__ float tile[kVKeys][64 + 1];
-    const int hi = blockIdx.y;  // b * Hkv + hk
+    const long long y = unit_id();
+    if (y >= static_cast<long long>(a.B) * a.Hkv) return;
+    const int hi = static_cast<int>(y);  // b * Hkv + hk
     head_scale(a, 2, hi, sm);
     const float inv = sm[1];
     if (blockIdx.x == 0 && threadIdx.x == 0) a.sv[hi] = sm[0];
     const int k0 = blockIdx.x * kVKeys;
     const int nk = min(kVKeys, a.Nkv - k0);
-    uint8_t* out = a.v8t + static_cast<size_t>(hi) * a.D * a.ldv;
-    for (int d0 = 0; d0 < a.D; d0 += 64) {
-        // load kVKeys x 64 (16-byte units: 8 per row)
+    uint8_t* out = a.v8t + static_cast<size_t>(hi) * a.Dp * a.ldv;
+    for (int d0 = 0; d0 < a.Dp; d0 += 64) {
+        // load kVKeys x 64 (16-byte units: 8 per row; zeros past the keys and past D)
         for (int e = threadIdx.x; e < kVKeys * 8; e += blockDim.x) {
             const int r = e / 8, u = e % 8;
             uint4 w = make_uint4(0, 0, 0, 0);
-            if (r < nk) w = *reinterpret_cast<const uint4*>(row_ptr(a, 2, hi, k0 + r) + d0 + u * 8);
+            if (r < nk && d0 + u * 8 < a.D) w = *reinterpret_cast<const uint4*>(row_ptr(a, 2, hi, k0 + r) + d0 + u * 8);
             const uint32_t uu[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -208,13 +220,15 @@ Fp8Layout fp8_layout(int B, int Hq, int Hkv, int Nq, int Nkv, int D)
 {
     Fp8Layout L{};
     L.ldv = (Nkv + 15) & ~15;
+    L.dp = (D + 127) & ~127;
+    const size_t Dp = static_cast<size_t>(L.dp);
     size_t off = 0;
     L.q8 = off;
-    off = align256(off + static_cast<size_t>(B) * Hq * Nq * D);
+    off = align256(off + static_cast<size_t>(B) * Hq * Nq * Dp);
     L.k8 = off;
-    off = align256(off + static_cast<size_t>(B) * Hkv * Nkv * D);
+    off = align256(off + static_cast<size_t>(B) * Hkv * Nkv * Dp);
     L.v8t = off;
-    off = align256(off + static_cast<size_t>(B) * Hkv * D * L.ldv);
+    off = align256(off + static_cast<size_t>(B) * Hkv * Dp * L.ldv);
     L.sq = off;
     off = align256(off + static_cast<size_t>(B) * Hq * sizeof(float));
     L.sk = off;
@@ -246,6 +260,7 @@ cudaError_t launch_fp8_quantize(const FwdArgs& f, void* workspace, cudaStream_t 
     a.Nq = pb.Nq;
     a.Nkv = pb.Nkv;
     a.D = pb.D;
+    a.Dp = L.dp;
     a.ldv = L.ldv;
     a.nsq = (pb.Nq + kQRows - 1) / kQRows;
     a.nsk = (pb.Nkv + kQRows - 1) / kQRows;
@@ -256,16 +271,21 @@ cudaError_t launch_fp8_quantize(const FwdArgs& f, void* workspace, cudaStream_t 
     a.sk = reinterpret_cast<float*>(ws + L.sk);
     a.sv = reinterpret_cast<float*>(ws + L.sv);
     a.part = reinterpret_cast<float*>(ws + L.part);
-    const int heads = pb.B * pb.Hq + 2 * pb.B * pb.Hkv;
+    const long long heads = static_cast<long long>(pb.B) * (pb.Hq + 2 * pb.Hkv);
     const int splits = max(a.nsq, a.nsk);
-    if (heads > 65535 || pb.B * pb.Hkv > 65535) return cudaErrorInvalidConfiguration;
-    amax_kernel<<<dim3(splits, heads), 256, 0, s>>>(a, f.bf16);
+    // grids of (row block, head) over x and the heads spread by unit_grid
+    dim3 g_amax, g_rows, g_vt;
+    if (!unit_grid(splits, heads, &g_amax) || !unit_grid(splits, static_cast<long long>(pb.B) * (pb.Hq + pb.Hkv), &g_rows) ||
+        !unit_grid((pb.Nkv + kVKeys - 1) / kVKeys > 0 ? (pb.Nkv + kVKeys - 1) / kVKeys : 1,
+                   static_cast<long long>(pb.B) * pb.Hkv, &g_vt))
+        return cudaErrorInvalidConfiguration;
+    amax_kernel<<<g_amax, 256, 0, s>>>(a, f.bf16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    quant_rows_kernel<<<dim3(splits, pb.B * pb.Hq + pb.B * pb.Hkv), 256, 0, s>>>(a, f.bf16);
+    quant_rows_kernel<<<g_rows, 256, 0, s>>>(a, f.bf16);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (pb.Nkv > 0) {
-        quant_vt_kernel<<<dim3((pb.Nkv + kVKeys - 1) / kVKeys, pb.B * pb.Hkv), 256, 0, s>>>(a, f.bf16);
+        quant_vt_kernel<<<g_vt, 256, 0, s>>>(a, f.bf16);
         e = cudaGetLastError();
     }
     return e;
@@ -282,6 +302,8 @@ cudaError_t launch_fwd_fp8(const FwdArgs& f, void* workspace, cudaStream_t s, bo
     const uint8_t* ws = static_cast<const uint8_t*>(workspace);
     XArgs x{};
     x.pb = pb;
+    x.pb.D = L.dp;     // the tiles run over the padded head dim (zero codes past D) ...
+    x.d_out = pb.D;    // ... and the epilogue stores the D real columns
     x.bf16 = f.bf16;
     x.q = ws + L.q8;
     x.k = ws + L.k8;

@@ -131,6 +131,15 @@ bool make_vt_map(CUtensorMap* m, const void* base, int B, int Hkv, int D, int N,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool unit_grid(unsigned x, long long n_units, dim3* grid)
+{
+    constexpr long long kMaxDim = 65535;
+    if (n_units < 1 || n_units > kMaxDim * kMaxDim) return false;
+    const long long y = n_units < kMaxDim ? n_units : kMaxDim;
+    *grid = dim3(x, static_cast<unsigned>(y), static_cast<unsigned>((n_units + y - 1) / y));
+    return true;
+}
+
 int num_sms()
 {
     int dev = 0, n = 0;

@@ -59,6 +59,11 @@ struct BwdArgs {
                        // bit 5 stored P (dK stores it, dV is the GEMM over it)
     void* ds;          // dS^T buffer of dsq_ds_bytes() bytes, or null (dQ recomputes S and dP)
     void* p;           // P^T buffer of the same size, or null (dV recomputes S)
+    // > 0: the stored-tile backward runs in chunks of this many kv groups (a kv
+    // head and its query heads), each chunk dK (storing its tiles), then the dV
+    // and dQ GEMMs over them; ds and p then hold one chunk's tiles
+    // (dsq_group_bytes() per group each). 0: all groups at once.
+    int chunk_groups;
     DeviceCtl ctl;
 };
 
@@ -90,6 +95,13 @@ struct XArgs {
     // dK: also store every P^T tile (input dtype) to p, the same layout
     int store_p;
     void* p;
+    // output columns the epilogue stores (0: pb.D); the FP8 forward runs its
+    // tiles over the head dim padded to 128 and stores the real ones
+    int d_out;
+    // dV / dK (rows = keys): only the kv heads [g0, g0 + ng) of every batch
+    // entry (ng = 0: all of them); the stored tile buffers then hold the query
+    // heads of those groups only, [B, ng * G, Nkv, ldq] (packed: [1, ng * G, ...])
+    int g0, ng;
 };
 
 // The GEMMs over the tiles the dK kernel stored (dense, D a multiple of 64 up to 1024;
@@ -103,17 +115,23 @@ struct DsqArgs {
     const void* tiles;  // dS^T (dv = 0) or P^T (dv = 1)
     const void* rhs;    // K (dv = 0) or dO (dv = 1)
     void* out;          // dQ (dv = 0) or dV (dv = 1), in its view
+    // only the kv groups [g0, g0 + ng) (ng = 0: all): dV rows of those kv heads,
+    // dQ rows of their query heads; `tiles` holds those groups' heads only
+    int g0, ng;
     DeviceCtl ctl;
 };
 bool dsq_supported(const Problem& pb);
-size_t dsq_ds_bytes(const Problem& pb);
-bool make_ds_map(CUtensorMap* m, const void* ds, const Problem& pb, bool bf16, int box_rows);
+size_t dsq_ds_bytes(const Problem& pb);     // one tile buffer, every head
+size_t dsq_group_bytes(const Problem& pb);  // one tile buffer, the G query heads of one kv group
+// map over a tile buffer of `heads` query heads (box: 64 queries x box_rows key rows)
+bool make_ds_map(CUtensorMap* m, const void* ds, const Problem& pb, bool bf16, int box_rows, int heads);
 cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s);
 
 // Workspace of the FP8 forward (byte offsets, 256-byte aligned regions).
 struct Fp8Layout {
     size_t q8, k8, v8t, sq, sk, sv, part, total;
     int ldv;
+    int dp;  // code rows: the head dim rounded up to 128 (zero codes past D)
 };
 Fp8Layout fp8_layout(int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 cudaError_t launch_fp8_quantize(const FwdArgs& a, void* workspace, cudaStream_t s);
@@ -158,11 +176,16 @@ bool make_u8_slab_map(CUtensorMap* m, const void* base, int B, int H, int N, int
 bool make_vt_map(CUtensorMap* m, const void* base, int B, int Hkv, int D, int N, int ldv, int box_rows);
 int num_sms();
 
+// Grid for n_units work units of x CTAs each (x along the grid's x, one
+// cluster per unit): the units are spread over y and z (unit_id() in device
+// code), so that their number is not bounded by the 65535 of one dimension.
+// Units past n_units (in the last z row) must return at once. False when
+// n_units exceeds 65535 * 65535.
+bool unit_grid(unsigned x, long long n_units, dim3* grid);
+
 // Records `fmt` as the thread's last-error message (ffpa_last_error) and
 // returns `status` (an ffpa_status value).
 int set_error(int status, const char* fmt, ...);
-
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
 
 // Decode / short-query forward (split over the keys), D % 64 == 0: a CTA
 // takes kDecodeRows query rows of one kv head's group (G * Nq rows in all)

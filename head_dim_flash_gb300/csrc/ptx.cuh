@@ -112,7 +112,9 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
 
 // Status word layout shared with the host: low 8 bits = error code,
 // bits 8..15 = which wait gave up (a site id), upper bits = block index.
-enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 4 };
+// Codes of the device status word (low byte; the next byte is a site, the
+// high half a block or sequence index): the ffpa_status of the failure.
+enum : uint32_t { DEV_OK = 0, DEV_INVALID = 1, DEV_TIMEOUT = 4 };
 
 // Bounded wait on the phase `parity` of `bar`. Gives up when the CTA-wide
 // abort flag is raised, when another block has already recorded a failure in

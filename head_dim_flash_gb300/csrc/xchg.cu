@@ -53,6 +53,8 @@ struct Geo {
     int slab_chunks;  // 64-wide head-dim chunks per slab (the last slab may be smaller)
     int stages;       // TMA ring depth
     int res;          // leading 64-wide chunks of the first row operand kept resident in shared memory
+    int n_rt;         // row tiles of 128 per (batch, head) in the grid (of the longest sequence)
+    int n_bz;         // (batch, head) entries in the grid
 };
 
 template <int OP>
@@ -105,28 +107,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ work unit
     // All CTAs of a cluster share blockIdx.y / blockIdx.z, hence the same unit.
-    // Grid (cluster ranks, row tile, b*H), or (cluster ranks, b*H, row tile)
-    // under causal masking. The hardware starts clusters in linear block order:
+    // Units in linear cluster order: row tile fastest, then b*H, or (causal)
+    // b*H fastest, then row tile. The hardware starts clusters in that order:
     // the first keeps the clusters that run together on few heads (their K/V
     // tiles stay in L2); the second starts every head's longest tile before any
     // head's next one, which balances the unequal causal tiles.
-    const int bz = pb.causal ? blockIdx.y : blockIdx.z;
-    const int tile = pb.causal ? blockIdx.z : blockIdx.y;
+    const long long unit = unit_id();
+    if (unit >= static_cast<long long>(gm.n_rt) * gm.n_bz) return;  // past the last unit: uniform over the cluster
+    const int bz = static_cast<int>(pb.causal ? unit % gm.n_bz : unit / gm.n_rt);
+    const int tile = static_cast<int>(pb.causal ? unit / gm.n_bz : unit % gm.n_rt);
     int b, h = 0, hk;
     if (T::kRowsQ) {
         b = bz / pb.Hq;
         h = bz % pb.Hq;
         hk = h / G;
     } else {
-        b = bz / pb.Hkv;
-        hk = bz % pb.Hkv;
+        // the kv heads [g0, g0 + ng) of the launch (all of them unless the
+        // stored-tile backward runs in chunks of kv groups)
+        const int ng = a.ng > 0 ? a.ng : pb.Hkv;
+        b = bz / ng;
+        hk = a.g0 + bz % ng;
     }
     int lq, lk, tq0 = 0, tk0 = 0;
     if constexpr (VARLEN) {
-        tq0 = pb.cu_q[b];
-        lq = pb.cu_q[b + 1] - tq0;
-        tk0 = pb.cu_k[b];
-        lk = pb.cu_k[b + 1] - tk0;
+        if (!varlen_seq(pb, b, a.ctl.status, VS_SINGLE, tq0, lq, tk0, lk)) return;  // uniform over the cluster
     } else {
         lq = pb.Nq;
         lk = pb.Nkv;
@@ -676,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // all 256 threads wrote it: store it, and report once the store read it
                         if (mbar_wait(&sh.p_full, s & 1, abort_flag, status, lim, XS_ZFULL)) {
                             if (t < n_ct) {
-                                tma_store_4d_hint(&tP, sZown, col_row0(t), tile_row(r0), col_head(t), bco, pol);
-                                tma_store_4d_hint(&tP, sZown + 16384, col_row0(t) + 64, tile_row(r0), col_head(t), bco,
+                                tma_store_4d_hint(&tP, sZown, col_row0(t), tile_row(r0), col_head(t) - a.g0 * G, bco, pol);
+                                tma_store_4d_hint(&tP, sZown + 16384, col_row0(t) + 64, tile_row(r0), col_head(t) - a.g0 * G, bco,
                                                   pol);
                                 bulk_commit_group();
                                 bulk_wait_read_all();
@@ -762,8 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (st_ds) {
                         if (t < n_ct) {
-                            tma_store_4d_hint(&tS, sZown, col_row0(t), tile_row(r0), col_head(t), bco, pol);
-                            tma_store_4d_hint(&tS, sZown + 16384, col_row0(t) + 64, tile_row(r0), col_head(t), bco, pol);
+                            tma_store_4d_hint(&tS, sZown, col_row0(t), tile_row(r0), col_head(t) - a.g0 * G, bco, pol);
+                            tma_store_4d_hint(&tS, sZown + 16384, col_row0(t) + 64, tile_row(r0), col_head(t) - a.g0 * G, bco, pol);
                             bulk_commit_group();
                             bulk_wait_read_all();
                         }
@@ -870,14 +874,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int OP, bool BF16, bool VARLEN>
-cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const Geo& gm, int n_rt, int bz, int smem,
-                      cudaStream_t s)
+cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, Geo gm, int n_rt, int bz, int smem, cudaStream_t s)
 {
     auto kern = xchg_kernel<OP, BF16, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    gm.n_rt = n_rt;
+    gm.n_bz = bz;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = a.pb.causal ? dim3(gm.C, bz, n_rt) : dim3(gm.C, n_rt, bz);
+    if (!unit_grid(gm.C, static_cast<long long>(n_rt) * bz, &cfg.gridDim)) return cudaErrorInvalidConfiguration;
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -952,6 +957,9 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
                                                    : make_row_map(&m[i], x.p, pb, x.kv_side, a.bf16, rows, x.v));
     };
     int n_rt, bz;
+    // dV / dK: the kv groups [g0, g0 + ng) (all unless the stored-tile backward runs in chunks)
+    const int ng = a.ng > 0 ? a.ng : pb.Hkv;
+    if (a.g0 < 0 || a.g0 + ng > pb.Hkv) return cudaErrorInvalidValue;
     switch (op) {
     case XOP_FWD:
         mk(0, sq, 128); mk(1, sq, 128); mk(2, sk, 128); mk(3, sk, 128); mk(4, sv, 32);
@@ -963,17 +971,17 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
         break;
     case XOP_DV:
         mk(0, sk, 128); mk(1, sk, 128); mk(2, sq, 128); mk(3, sq, 128); mk(4, sdo, 32);
-        n_rt = (pb.Nkv + 127) / 128; bz = pb.B * pb.Hkv;
+        n_rt = (pb.Nkv + 127) / 128; bz = pb.B * ng;
         break;
     default:  // XOP_DK
         mk(0, sk, 128); mk(1, sv, 128); mk(2, sq, 128); mk(3, sdo, 128); mk(4, sq, 32);
-        n_rt = (pb.Nkv + 127) / 128; bz = pb.B * pb.Hkv;
+        n_rt = (pb.Nkv + 127) / 128; bz = pb.B * ng;
         break;
     }
     // dK storing dS^T / P^T: those buffers as stored tiles (64 queries x 128 key rows)
-    if (op == XOP_DK && a.store_ds) okm = okm && make_ds_map(&m[5], a.ds, pb, a.bf16, 128);
+    if (op == XOP_DK && a.store_ds) okm = okm && make_ds_map(&m[5], a.ds, pb, a.bf16, 128, ng * (pb.Hq / pb.Hkv));
     else m[5] = m[0];
-    if (op == XOP_DK && a.store_p) okm = okm && make_ds_map(&m[6], a.p, pb, a.bf16, 128);
+    if (op == XOP_DK && a.store_p) okm = okm && make_ds_map(&m[6], a.p, pb, a.bf16, 128, ng * (pb.Hq / pb.Hkv));
     else m[6] = m[0];
     if (!okm) return cudaErrorInvalidValue;
     if (n_rt == 0 || bz == 0) return cudaSuccess;

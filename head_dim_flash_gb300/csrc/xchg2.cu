@@ -68,6 +68,8 @@ struct PGeo {
     int res;     // leading 64-wide chunks of the first row operand kept resident in shared memory
     int nbuf;    // Z buffers per slot (1 or 2)
     int nprod;   // producer lanes (ring positions are dealt round-robin)
+    int n_rt;    // row tiles of 256 per (batch, head) in the grid (of the longest sequence)
+    int n_bz;    // (batch, head) entries in the grid
 };
 
 template <int OP>
@@ -127,28 +129,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = pb.Hq / pb.Hkv;
 
     // ------------------------------------------------------------ work unit
-    // Grid (cluster ranks, row tile, b*H), or (cluster ranks, b*H, row tile)
-    // under causal masking. The hardware starts clusters in linear block order:
+    // Units in linear cluster order: row tile fastest, then b*H, or (causal)
+    // b*H fastest, then row tile. The hardware starts clusters in that order:
     // the first keeps the clusters that run together on few heads (their K/V
     // tiles stay in L2); the second starts every head's longest tile before any
     // head's next one, which balances the unequal causal tiles.
-    const int bz = pb.causal ? blockIdx.y : blockIdx.z;
-    const int tile = pb.causal ? blockIdx.z : blockIdx.y;
+    const long long unit = unit_id();
+    if (unit >= static_cast<long long>(gm.n_rt) * gm.n_bz) return;  // past the last unit: uniform over the cluster
+    const int bz = static_cast<int>(pb.causal ? unit % gm.n_bz : unit / gm.n_rt);
+    const int tile = static_cast<int>(pb.causal ? unit / gm.n_bz : unit % gm.n_rt);
     int b, h = 0, hk;
     if (T::kRowsQ) {
         b = bz / pb.Hq;
         h = bz % pb.Hq;
         hk = h / G;
     } else {
-        b = bz / pb.Hkv;
-        hk = bz % pb.Hkv;
+        // the kv heads [g0, g0 + ng) of the launch (all of them unless the
+        // stored-tile backward runs in chunks of kv groups)
+        const int ng = a.ng > 0 ? a.ng : pb.Hkv;
+        b = bz / ng;
+        hk = a.g0 + bz % ng;
     }
     int lq, lk, tq0 = 0, tk0 = 0;
     if constexpr (VARLEN) {
-        tq0 = pb.cu_q[b];
-        lq = pb.cu_q[b + 1] - tq0;
-        tk0 = pb.cu_k[b];
-        lk = pb.cu_k[b + 1] - tk0;
+        if (!varlen_seq(pb, b, a.ctl.status, VS_PAIR, tq0, lq, tk0, lk)) return;  // uniform over the cluster
     } else {
         lq = pb.Nq;
         lk = pb.Nkv;
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // keys, two tiles per slot, the second repeated when C is odd)
             auto load_value = [&](int s) -> bool {
                 if constexpr (F8) {
-                    const int vt_row = d0 + rh * 128;
+                    const int vt_row = d0 + rh * (sw / 2);  // my half of the slab's V^T rows
                     for (int k = 0; k < C; k += 2) {
                         const int ta = s * C + (c + k) % C;
                         const int tb = s * C + (c + min(k + 1, C - 1)) % C;
@@ -670,8 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(&sh.p_full[bb], zpar(s), abort_flag, status, lim, PS_COPY);
                     if (ok) {
                         if (t < n_ct) {
-                            tma_store_4d_hint(&tP, zown_base, col_row0(t), tile_row(r0), col_head(t), bco, pol);
-                            tma_store_4d_hint(&tP, zown_base + 16384, col_row0(t) + 64, tile_row(r0), col_head(t), bco,
+                            tma_store_4d_hint(&tP, zown_base, col_row0(t), tile_row(r0), col_head(t) - a.g0 * G, bco, pol);
+                            tma_store_4d_hint(&tP, zown_base + 16384, col_row0(t) + 64, tile_row(r0), col_head(t) - a.g0 * G, bco,
                                               pol);
                             bulk_commit_group();
                             bulk_wait_read_all();
@@ -691,8 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ok && store_ds) {
                     if (t < n_ct) {
-                        tma_store_4d_hint(&tS, zown_base, col_row0(t), tile_row(r0), col_head(t), bco, pol);
-                        tma_store_4d_hint(&tS, zown_base + 16384, col_row0(t) + 64, tile_row(r0), col_head(t), bco, pol);
+                        tma_store_4d_hint(&tS, zown_base, col_row0(t), tile_row(r0), col_head(t) - a.g0 * G, bco, pol);
+                        tma_store_4d_hint(&tS, zown_base + 16384, col_row0(t) + 64, tile_row(r0), col_head(t) - a.g0 * G, bco, pol);
                         bulk_commit_group();
                         bulk_wait_read_all();
                     }
@@ -1096,7 +1100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t orow = static_cast<size_t>(bco) * ov.sb + static_cast<size_t>(row_head) * ov.sh +
                                 static_cast<size_t>(row_co(row)) * ov.sn;
             uint16_t* dst = reinterpret_cast<uint16_t*>(out) + orow + d0;
-            const int c_end = min((half + 1) * (sw / 2), pb.D - d0);  // columns past D are not stored
+            // columns past the output's head dim are not stored
+            const int c_end = min((half + 1) * (sw / 2), (a.d_out > 0 ? a.d_out : pb.D) - d0);
             for (int cc = half * (sw / 2); cc < c_end; cc += 32) {
                 uint32_t v[32];
                 if (n_steps > 0) {
@@ -1142,14 +1147,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int OP, bool BF16, bool VARLEN, bool F8 = false>
-cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, const PGeo& gm, int n_rt, int bz, int smem,
-                      cudaStream_t s)
+cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, PGeo gm, int n_rt, int bz, int smem, cudaStream_t s)
 {
     auto kern = pair_kernel<OP, BF16, VARLEN, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    gm.n_rt = n_rt;
+    gm.n_bz = bz;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = a.pb.causal ? dim3(2 * gm.C, bz, n_rt) : dim3(2 * gm.C, n_rt, bz);
+    if (!unit_grid(2 * gm.C, static_cast<long long>(n_rt) * bz, &cfg.gridDim)) return cudaErrorInvalidConfiguration;
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -1184,9 +1190,9 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const bool rows_q = (op == XOP_FWD || op == XOP_DQ);
     if (rows_q ? q_empty : kv_empty) return cudaSuccess;  // no output rows
     if (pb.D % 64 != 0) return cudaErrorInvalidConfiguration;  // chunked 5-D maps need D % 64 == 0
-    // FP8 forward: dense, head dims with whole 256-column slabs (2 or 3 pairs, or 1)
+    // FP8 forward: dense, the head dim padded to whole 128-column chunks (1 to 4 pairs)
     const bool f8 = a.f8 != 0;
-    if (f8 && (op != XOP_FWD || pb.varlen || pb.D % 256 != 0 || pb.D > 768)) return cudaErrorInvalidConfiguration;
+    if (f8 && (op != XOP_FWD || pb.varlen || pb.D % 128 != 0 || pb.D > 1024)) return cudaErrorInvalidConfiguration;
     const int nd = f8 ? pb.D / 128 : pb.D / 64;  // 128-byte chunks
     const int zb = f8 ? 16384 : 32768;           // bytes of one Z tile half
     const int d_pad = (pb.D + 127) & ~127;
@@ -1231,6 +1237,9 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     auto val = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 128, 2, x.v); };
     int n_rows;
     int bz;
+    // dV / dK: the kv groups [g0, g0 + ng) (all unless the stored-tile backward runs in chunks)
+    const int ng = a.ng > 0 ? a.ng : pb.Hkv;
+    if (a.g0 < 0 || a.g0 + ng > pb.Hkv) return cudaErrorInvalidValue;
     if (f8) {
         // e4m3 codes: q8 (rows), k8 (columns), V^T (value operand, 128 head-dim rows per CTA)
         okm = make_u8_slab_map(&m[0], a.q, pb.B, pb.Hq, pb.Nq, pb.D, 128, 2) &&
@@ -1258,18 +1267,18 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
         break;
     case XOP_DV:
         row(0, sk); row(1, sk); col(2, sq); col(3, sq); val(4, sdo);
-        n_rows = pb.Nkv; bz = pb.B * pb.Hkv;
+        n_rows = pb.Nkv; bz = pb.B * ng;
         break;
     default:  // XOP_DK
         row(0, sk); row(1, sv); col(2, sq); col(3, sdo); val(4, sq);
-        n_rows = pb.Nkv; bz = pb.B * pb.Hkv;
+        n_rows = pb.Nkv; bz = pb.B * ng;
         break;
     }
     // dK storing dS: the dS^T buffer as stored tiles (64 queries x 128 key rows)
-    if (op == XOP_DK && a.store_ds) okm = okm && make_ds_map(&m[5], a.ds, pb, a.bf16, 128);
+    if (op == XOP_DK && a.store_ds) okm = okm && make_ds_map(&m[5], a.ds, pb, a.bf16, 128, ng * (pb.Hq / pb.Hkv));
     else m[5] = m[0];
     // dK storing P: the P^T buffer, the same layout
-    if (op == XOP_DK && a.store_p) okm = okm && make_ds_map(&m[6], a.p, pb, a.bf16, 128);
+    if (op == XOP_DK && a.store_p) okm = okm && make_ds_map(&m[6], a.p, pb, a.bf16, 128, ng * (pb.Hq / pb.Hkv));
     else m[6] = m[0];
     if (!okm) return cudaErrorInvalidValue;
     const int n_rt = (n_rows + 255) / 256;

@@ -129,8 +129,9 @@ FFPA_API ffpa_status ffpa_fwd_strided(ffpa_dtype dt, ffpa_view q, ffpa_view k, f
  *   workspace: device scratch of at least ffpa_decode_workspace_bytes()
  *   bytes, 256-byte aligned, sized on the current device (the split count
  *   follows its SM count); one call at a time per workspace.
- * Returns FFPA_ERR_NOT_SUPPORTED for D % 64 != 0 or B * Hkv * ceil(G * Nq /
- * 16) > 65535 (use ffpa_fwd_strided), otherwise as ffpa_fwd_strided.
+ * Returns FFPA_ERR_NOT_SUPPORTED for D % 64 != 0 (use ffpa_fwd_strided) or
+ * B * Hkv * ceil(G * Nq / 16) > 65535^2 (the launch grid), otherwise as
+ * ffpa_fwd_strided.
  */
 FFPA_API size_t ffpa_decode_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 FFPA_API ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_view v, ffpa_view o, float* lse,
@@ -145,12 +146,15 @@ FFPA_API ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ff
  * then O = softmax(scale * S) V runs on the e4m3 operands with fp32
  * accumulation; P is rounded to e4m3 for the P V product. O (bf16/fp16 as
  * the inputs) and LSE (fp32 [B, Hq, Nq]) as in ffpa_fwd_strided.
- *   D must be 256, 512 or 768 and Nkv >= 1 (else FFPA_ERR_NOT_SUPPORTED);
- *   dense views only. workspace: device scratch of at least
- *   ffpa_fp8_workspace_bytes() bytes, 256-byte aligned; it holds the codes
- *   and scales afterwards, at the offsets ffpa_fp8_workspace_layout() gives:
- *   offsets[0] q8 [B, Hq, Nq, D], [1] k8 [B, Hkv, Nkv, D], [2] V^T codes
- *   [B, Hkv, D, ldv], [3] sq fp32 [B*Hq], [4] sk fp32 [B*Hkv], [5] sv fp32
+ *   D: any multiple of 32 in [64, 1024] (the pages' FP8 range, "Backends
+ *   Overview", capability matrix), and Nkv >= 1 (else FFPA_ERR_NOT_SUPPORTED);
+ *   dense views only (the pages' FP8 rows have no packed varlen layout).
+ *   workspace: device scratch of at least ffpa_fp8_workspace_bytes() bytes,
+ *   256-byte aligned; it holds the codes and scales afterwards, at the
+ *   offsets ffpa_fp8_workspace_layout() gives, with the head dim of the codes
+ *   padded to Dp = D rounded up to 128 (zero codes past D):
+ *   offsets[0] q8 [B, Hq, Nq, Dp], [1] k8 [B, Hkv, Nkv, Dp], [2] V^T codes
+ *   [B, Hkv, Dp, ldv], [3] sq fp32 [B*Hq], [4] sk fp32 [B*Hkv], [5] sv fp32
  *   [B*Hkv], [6] ldv (Nkv rounded up to 16), [7] total bytes.
  * ffpa_fp8_quantize runs only the quantization into the workspace.
  */
@@ -189,6 +193,29 @@ FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, 
  */
 FFPA_API size_t ffpa_bwd_workspace_bytes_ds(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                                             int causal);
+
+/*
+ * The stored-tile backward within a memory budget (the FFPA pages' training
+ * path is FlashAttention-style, "Backends Overview", "Choosing a backend":
+ * its scratch stays bounded however long the sequences are). A workspace
+ * smaller than ffpa_bwd_workspace_bytes_ds() but with room for both tile sets
+ * (dS^T and P^T) of at least one kv group (a kv head and its Hq / Hkv query
+ * heads: 2 * B * (Hq / Hkv) * Nkv * round_up(Nq, 8) * 2 bytes, plus 256) runs
+ * the same kernels in chunks of kv groups: per chunk, dK over the chunk's kv
+ * heads storing their tiles, then the dV and dQ GEMMs over them. Each group's
+ * gradients are complete within its chunk (no cross-chunk accumulation, the
+ * same results as the one-chunk path). The chunks hold as many groups as fit,
+ * evened out over the kv heads. Chunks apply to calls that run the dV, dK and
+ * dQ stages together (ffpa_bwd, ffpa_bwd_strided, ffpa_varlen_bwd, or
+ * ffpa_bwd_stages with bits 1..3 and neither bit 4 nor 5).
+ * This query returns the workspace size to pass for at most `budget` bytes:
+ * ffpa_bwd_workspace_bytes_ds() when it fits, else the bytes of the largest
+ * evened-out chunk that fits, else ffpa_bwd_workspace_bytes() (the
+ * recomputing backward). Its result depends only on the problem and the
+ * budget, not on the device's free memory.
+ */
+FFPA_API size_t ffpa_bwd_workspace_bytes_budget(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                                                int causal, size_t budget);
 
 /*
  * Dense backward (FFPA docs, CuTe-DSL Backend page, "Blackwell status": a
@@ -252,8 +279,13 @@ FFPA_API ffpa_status ffpa_bwd_stages(ffpa_dtype dt, const void* q, const void* k
  *   device image, which holds B*Hq*Nq <= 524288 query rows; larger problems
  *   return FFPA_ERR_INVALID_VALUE (use ffpa_bwd). Every GPU that loads the
  *   library keeps that array until the process exits.
+ *   It always runs the four launches of ffpa_bwd with the small workspace
+ *   (preprocess, then dV, dK and dQ, each recomputing its scores), never the
+ *   stored-tile path.
  *   The first call on a device looks up the array's device address (once per
- *   device); make that first call before any stream capture.
+ *   device); make that first call before any stream capture. The address is
+ *   not looked up again: the call is not valid after a cudaDeviceReset of its
+ *   device in the same process.
  *   All calls on a device share the array: calls whose kernels overlap on the
  *   GPU (unordered streams) race on it. Calls ordered on one stream do not;
  *   nothing in the array needs to start at zero.
@@ -274,8 +306,15 @@ FFPA_API ffpa_status ffpa_bwd_noalloc(ffpa_dtype dt, const void* q, const void* 
  *     nondecreasing, last entries equal total_q / total_k (both required; pass
  *     the same pointer twice for self-attention). Read on the device only.
  *   max_seqlen_q / max_seqlen_k : upper bounds of the per-sequence lengths
- *     (they size the launch grid; a sequence longer than the bound is not
- *     fully processed).
+ *     (they size the launch grid).
+ * cu_seqlens live on the device, so their contract is checked there: a
+ * sequence whose offsets are negative or decreasing, run past total_q /
+ * total_k, or whose length exceeds max_seqlen_q / max_seqlen_k is not
+ * processed, and the kernels record the error in the device status word;
+ * the next ffpa_get_status() returns FFPA_ERR_INVALID_VALUE naming the
+ * sequence (the FFPA varlen API raises instead of silently unpacking a batch
+ * it cannot process). Outputs of such a call are undefined; nothing is read
+ * or written outside the caller's tensors.
  */
 FFPA_API ffpa_status ffpa_varlen_fwd(ffpa_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
                             const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int total_q,
@@ -296,7 +335,14 @@ FFPA_API size_t ffpa_varlen_bwd_workspace_bytes_ds(ffpa_dtype dt, int batch, int
                                                    int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
                                                    int causal);
 
-/* Packed varlen backward; layouts as in ffpa_varlen_fwd, dq like q, dk/dv like k. */
+/* As ffpa_bwd_workspace_bytes_budget, for packed batches (one group's tiles are
+ * 2 * (Hq / Hkv) * (total_k + 256 * batch) * round_up(max_seqlen_q, 8) * 2 bytes). */
+FFPA_API size_t ffpa_varlen_bwd_workspace_bytes_budget(ffpa_dtype dt, int batch, int total_q, int total_k,
+                                                       int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                                                       int causal, size_t budget);
+
+/* Packed varlen backward; layouts as in ffpa_varlen_fwd, dq like q, dk/dv like k.
+ * cu_seqlens and max_seqlen_* are checked on the device as in ffpa_varlen_fwd. */
 FFPA_API ffpa_status ffpa_varlen_bwd(ffpa_dtype dt, const void* q, const void* k, const void* v, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
                             const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int total_q,
@@ -307,8 +353,9 @@ FFPA_API ffpa_status ffpa_varlen_bwd(ffpa_dtype dt, const void* q, const void* k
 /*
  * Synchronises `stream`, then reports and clears the device status word:
  * FFPA_OK, FFPA_ERR_TIMEOUT (a bounded device wait ran out; the kernel
- * returned early and its outputs are undefined) or FFPA_ERR_CUDA (the stream
- * reported an error).
+ * returned early and its outputs are undefined), FFPA_ERR_INVALID_VALUE (a
+ * packed varlen sequence broke the cu_seqlens / max_seqlen contract; see
+ * ffpa_varlen_fwd) or FFPA_ERR_CUDA (the stream reported an error).
  */
 FFPA_API ffpa_status ffpa_get_status(ffpa_stream_t stream);
 

@@ -5,14 +5,20 @@ GEMM; with room for P^T as well, the dK launch also writes P^T and
 dV = P^T dO is one GEMM instead of a launch that recomputes S^T.
 
 Every case runs the backward three times on the same inputs: with the small
-workspace (dQ recomputes S and dP), with room for dS only, and with room for
-dS and P. All three are checked against the fp64 oracle with the usual
-gradient tolerance. dV must be bit-identical between the first two (the same
-kernel). dK must be bit-identical between the first two when non-causal
-(causal storing starts at an even query tile: an extra all-masked tile
-shifts the summation order), and between the last two in the CTA-pair
-family (storing P does not change it there; the one-CTA family then forms
-dS^T from P rounded to fp16 instead of fp32).
+workspace (dQ recomputes S and dP), with a middle one, and with room for dS
+and P of every head. All three are checked against the fp64 oracle with the
+usual gradient tolerance.
+- With one kv head, the middle workspace holds dS for every head and stores
+  dS only (dV recomputes): dV must be bit-identical to the small workspace's
+  (the same kernel); dK too when non-causal (causal storing starts at an even
+  query tile: an extra all-masked tile shifts the summation order), and dK
+  must equal the big workspace's in the CTA-pair family (storing P does not
+  change it there; the one-CTA family then forms dS^T from P rounded to fp16
+  instead of fp32).
+- With several kv heads, the middle workspace holds both tile sets of one kv
+  group: the backward runs in chunks of one group (dK, then the dV and dQ
+  GEMMs, per chunk), and every gradient must be bit-identical to the big
+  workspace's (the same kernels on the same tiles).
 """
 import math
 import os
@@ -67,18 +73,23 @@ def run_both(B, Hq, Hkv, Nq, Nkv, D, dtype=torch.bfloat16, seed=0, causal=False)
     ds_only = torch.empty(small_n + one, dtype=torch.uint8, device="cuda")
     big = torch.empty(big_n, dtype=torch.uint8, device="cuda")
     g_small = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=small)
-    g_ds = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=ds_only)
+    mid = ds_only if Hkv == 1 else group_chunk_workspace(q, k, causal, 1)
+    g_ds = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=mid)
     g_big = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=big)
     api.get_status()
     ref = oracle.attention_bwd(inp["q"], inp["k"], inp["v"], inp["dO"], causal, scale)
     for gs in (g_small, g_ds, g_big):
         for name, got, r in zip(("dQ", "dK", "dV"), gs, ref):
             check_grad(got, r, name)
-    assert torch.equal(g_small[2], g_ds[2])
-    if pair_family(D):
-        assert torch.equal(g_ds[1], g_big[1])
-    if not causal:
-        assert torch.equal(g_small[1], g_ds[1])
+    if Hkv == 1:  # dS stored, dV recomputed
+        assert torch.equal(g_small[2], g_ds[2])
+        if pair_family(D):
+            assert torch.equal(g_ds[1], g_big[1])
+        if not causal:
+            assert torch.equal(g_small[1], g_ds[1])
+    else:  # both tile sets in chunks of kv groups
+        for name, a, b in zip(("dQ", "dK", "dV"), g_ds, g_big):
+            assert torch.equal(a, b), f"{name}: chunked and one-chunk results differ"
     return inp, (q, k, v, do, o, lse, scale, big, ds_only), g_big, g_ds
 
 
@@ -176,6 +187,85 @@ def test_stored_tile_varlen_backward(causal, D):
         api.get_status()
         for gname, g, r in zip(("dQ", "dK", "dV"), got[name], ref):
             check_grad(g, r, f"{name} {gname}")
+
+
+def group_chunk_workspace(q, k, causal, groups):
+    """A workspace with room for both tile sets of `groups` kv groups (the budget query's answer)."""
+    B, Hq, Nq, _ = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    per_group = B * (Hq // Hkv) * Nkv * ((Nq + 7) // 8 * 8) * 2
+    n = api.bwd_workspace_bytes(q, k, causal, budget=api.bwd_workspace_bytes(q, k) + 2 * groups * per_group + 512)
+    assert api.bwd_workspace_bytes(q, k) < n < api.bwd_workspace_bytes(q, k, causal)
+    return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+# Several chunks of kv groups (one or two groups per chunk, the last chunk
+# evened out), dense: both kernel families, causal and not, GQA; against the
+# fp64 oracle and bit for bit against the one-chunk path.
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nkv,D,causal,groups", [
+    (1, 6, 3, 300, 333, 512, False, 1),
+    (2, 8, 4, 257, 513, 512, True, 1),
+    (1, 12, 6, 200, 300, 256, True, 2),
+    (1, 4, 4, 130, 700, 320, False, 1),   # one-CTA family
+    (1, 10, 5, 400, 300, 1024, True, 2),  # one-CTA family, two GEMM slabs, more queries than keys
+])
+def test_stored_tiles_in_kv_group_chunks(B, Hq, Hkv, Nq, Nkv, D, causal, groups):
+    inp = workloads.random_dense(B, Hq, Hkv, Nq, Nkv, D, torch.bfloat16, seed=Nq + D + Hq)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dO"))
+    scale = 1.0 / math.sqrt(D)
+    o, lse = api.fwd(q, k, v, causal, scale)
+    chunk_ws = group_chunk_workspace(q, k, causal, groups)
+    full_ws = torch.empty(api.bwd_workspace_bytes(q, k, causal), dtype=torch.uint8, device="cuda")
+    g_chunk = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=chunk_ws)
+    g_full = api.bwd(q, k, v, o, lse, do, causal, scale, workspace=full_ws)
+    api.get_status()
+    ref = oracle.attention_bwd(inp["q"], inp["k"], inp["v"], inp["dO"], causal, scale)
+    for name, got, r, full in zip(("dQ", "dK", "dV"), g_chunk, ref, g_full):
+        check_grad(got, r, name)
+        assert torch.equal(got, full), f"{name}: chunked and one-chunk results differ"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_stored_tiles_in_kv_group_chunks_varlen(causal):
+    from head_dim_flash_gb300 import _ffi
+
+    lq = [5, 0, 130, 300, 64, 257]
+    lk = [7, 3, 130, 200, 0, 513]
+    Hq, Hkv, D = 6, 3, 512
+    inp = workloads.random_varlen(lq, lk, Hq, Hkv, D, seed=91)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dO"))
+    cq, ck = inp["cu_seqlens_q"].cuda(), inp["cu_seqlens_k"].cuda()
+    scale = 1 / math.sqrt(D)
+    o, lse = api.varlen_fwd(q, k, v, cq, ck, max(lq), max(lk), causal, scale)
+    sizes = (0, len(lq), sum(lq), sum(lk), max(lq), max(lk), Hq, Hkv, D)
+    small_n = int(_ffi.ffpa_varlen_bwd_workspace_bytes(*sizes))
+    big_n = int(_ffi.ffpa_varlen_bwd_workspace_bytes_ds(*sizes, int(causal)))
+    per_group = (Hq // Hkv) * (sum(lk) + 256 * len(lk)) * ((max(lq) + 7) // 8 * 8) * 2
+    chunk_n = api.varlen_workspace_bytes(q, k, cq, max(lq), max(lk), causal, budget=small_n + 2 * per_group + 512)
+    assert small_n < chunk_n < big_n
+    ref = oracle.varlen_bwd(inp["q"], inp["k"], inp["v"], inp["dO"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                            causal, scale)
+    got = {}
+    for name, n in (("chunks", chunk_n), ("one chunk", big_n)):
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        got[name] = api.varlen_bwd(q, k, v, o, lse, do, cq, ck, max(lq), max(lk), causal, scale, workspace=ws)
+        api.get_status()
+        for gname, g, r in zip(("dQ", "dK", "dV"), got[name], ref):
+            check_grad(g, r, f"{name} {gname}")
+    for gname, a, b in zip(("dQ", "dK", "dV"), got["chunks"], got["one chunk"]):
+        assert torch.equal(a, b), f"{gname}: chunked and one-chunk results differ"
+
+
+def test_default_workspace_is_fixed_by_the_budget():
+    # the size bwd() allocates depends on the problem and the budget only: the
+    # every-head tiles within the budget, a chunk of groups beyond it
+    q = torch.zeros(1, 8, 1024, 512, dtype=torch.bfloat16, device="cuda")
+    full = api.bwd_workspace_bytes(q, q, False)
+    assert api.bwd_workspace(q, q, False).numel() == full
+    per_group = 1024 * 1024 * 2
+    n = api.bwd_workspace(q, q, False, budget=full - 1).numel()
+    assert api.bwd_workspace_bytes(q, q) + 2 * 4 * per_group <= n < full  # 8 groups in 2 chunks of 4
+    assert api.bwd_workspace(q, q, False, budget=1).numel() == api.bwd_workspace_bytes(q, q)
 
 
 def test_varlen_and_other_head_dims_keep_the_recompute_path():

@@ -227,8 +227,8 @@ TRAFFIC = {
     ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 10253297152, "files": PAIR_SOURCES,
                                              "sources": "b4ae15d955073a85"},
     # one ffpa_decode_fwd call: split kernel + combine (means over six calls)
-    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2156501035, "files": DECODE_SOURCES,
-                                                                "sources": "0b80c2d43c6c915b"},
+    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2156553558, "files": DECODE_SOURCES,
+                                                                "sources": "d7fa58a72259511f"},
     # the e4m3 attention kernel (reads q8, k8, V^T codes; writes O, LSE)
     ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 639294413,
                                                                              "files": FP8_SOURCES,

@@ -230,9 +230,9 @@ TRAFFIC = {
     ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2156553558, "files": DECODE_SOURCES,
                                                                 "sources": "d7fa58a72259511f"},
     # the e4m3 attention kernel (reads q8, k8, V^T codes; writes O, LSE)
-    ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 639294413,
+    ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 638752666,
                                                                              "files": FP8_SOURCES,
-                                                                             "sources": "79e5b087ccadda46"},
+                                                                             "sources": "c0568c01721855ba"},
 }
 
 

@@ -208,9 +208,11 @@ def group_chunk_workspace(q, k, causal, groups):
     (1, 12, 6, 200, 300, 256, True, 2),
     (1, 4, 4, 130, 700, 320, False, 1),   # one-CTA family
     (1, 10, 5, 400, 300, 1024, True, 2),  # one-CTA family, two GEMM slabs, more queries than keys
+    (2, 16, 4, 257, 300, 512, True, 1),   # GQA with 4 query heads per kv head, fp16 below
 ])
 def test_stored_tiles_in_kv_group_chunks(B, Hq, Hkv, Nq, Nkv, D, causal, groups):
-    inp = workloads.random_dense(B, Hq, Hkv, Nq, Nkv, D, torch.bfloat16, seed=Nq + D + Hq)
+    dtype = torch.float16 if Hq // Hkv == 4 else torch.bfloat16
+    inp = workloads.random_dense(B, Hq, Hkv, Nq, Nkv, D, dtype, seed=Nq + D + Hq)
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dO"))
     scale = 1.0 / math.sqrt(D)
     o, lse = api.fwd(q, k, v, causal, scale)

@@ -961,7 +961,9 @@ def measure_e2e(w, args, dev, stream, inp, step_flops, world):
 
     run(2)
     torch.cuda.synchronize()
-    n = max(1, min(args.steps, 10))
+    # 30 steps: the first copy-in and the last copy-out (a few ms) that no
+    # compute overlaps are spread over a run of training-loop length
+    n = max(1, min(args.steps, 30))
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
     run(n, start=s)

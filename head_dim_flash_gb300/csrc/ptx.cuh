@@ -351,6 +351,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// The same descriptor `bytes` further on (a multiple of 16): only the 14-bit
+// start-address field (address >> 4) changes, and it cannot carry into the
+// next field while the address stays below 256 KiB (all of shared memory).
+// Lets an MMA issue loop build one descriptor per tile and step through it
+// with one add.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes)
+{
+    return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16 with an fp32 accumulator.
 // bf16 selects BF16 inputs (else FP16); a_mn / b_mn select MN-major operands.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a_mn, bool b_mn)

@@ -488,14 +488,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     b_slot = rp.slot;
                                     rp.advance(gm.stages);
                                 }
+                                // one descriptor per tile, stepped by offsets (K-major, 32 bytes per MMA)
+                                const uint64_t da = sdesc_sw128(smem_u32(A), 16, 1024);
+                                const uint64_t db = sdesc_sw128(smem_u32(B), 16, 1024);
                                 for (int u2 = 0; u2 < 2; ++u2) {
                                     const int d = d_first + u2;
                                     if (d >= nd) break;
 #pragma unroll
                                     for (int kk = 0; kk < 4; ++kk)
-                                        mma(dst, sdesc_sw128(smem_u32(A + u2 * 16384 + kk * 32), 16, 1024),
-                                            sdesc_sw128(smem_u32(B + (2 * h2 + u2) * 8192 + kk * 32), 16, 1024),
-                                            idesc_s, (d | kk) != 0);
+                                        mma(dst, sdesc_advance(da, u2 * 16384 + kk * 32),
+                                            sdesc_advance(db, (2 * h2 + u2) * 8192 + kk * 32), idesc_s, (d | kk) != 0);
                                 }
                                 if (a_slot >= 0) give(a_slot);
                             }
@@ -539,12 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (!w8) return false;
                             }
                             const uint8_t* W = w8 + (k & 1) * 16384;
+                            const uint64_t dz = sdesc_sw128(smem_u32(zs), 16, 1024);
+                            const uint64_t dw = sdesc_sw128(smem_u32(W), 16, 1024);
 #pragma unroll
                             for (int t = 0; t < 4; ++t) {
                                 // keys 32 t of the tile: 32 bytes into Z's and V^T's 128-byte rows
                                 const uint32_t acc = (s | k | t) != 0;
-                                mma(t_acc, sdesc_sw128(smem_u32(zs + t * 32), 16, 1024),
-                                    sdesc_sw128(smem_u32(W + t * 32), 16, 1024), idesc_v, acc);
+                                mma(t_acc, sdesc_advance(dz, t * 32), sdesc_advance(dw, t * 32), idesc_v, acc);
                             }
                             if ((k & 1) == 1 || k == C - 1) {
                                 give(rp.slot);
@@ -553,14 +556,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
                             const uint8_t* W = take();
                             if (!W) return false;
+                            const uint64_t dz = sdesc_sw128(smem_u32(zs), 16, 1024);
+                            const uint64_t dw = sdesc_sw128(smem_u32(W), 128 * 128, 1024);
 #pragma unroll
                             for (int t = 0; t < 8; ++t) {
                                 // keys 16 t of the tile: Z chunk t / 4, W rows 16 t (MN-major,
                                 // 64-column blocks 128 keys x 128 bytes apart)
-                                const uint64_t bd = sdesc_sw128(smem_u32(W + t * 2048), 128 * 128, 1024);
                                 const uint32_t acc = (s | k | t) != 0;
-                                umma_f16_pair(t_acc, sdesc_sw128(smem_u32(zs + (t >> 2) * 16384 + (t & 3) * 32), 16, 1024),
-                                              bd, idesc_v, acc);
+                                umma_f16_pair(t_acc, sdesc_advance(dz, (t >> 2) * 16384 + (t & 3) * 32),
+                                              sdesc_advance(dw, t * 2048), idesc_v, acc);
                             }
                             give(rp.slot);
                             rp.advance(gm.stages);

@@ -398,10 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         const uint8_t* B = take();
                         if (!B) return false;
+                        // one descriptor per tile, stepped by 32 bytes per MMA (K-major)
+                        const uint64_t da = sdesc_sw128(smem_u32(A), 16, 1024);
+                        const uint64_t db = sdesc_sw128(smem_u32(B), 16, 1024);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            umma_f16(dst, sdesc_sw128(smem_u32(A + kk * 32), 16, 1024),
-                                     sdesc_sw128(smem_u32(B + kk * 32), 16, 1024), idesc_s, (d | kk) != 0);
+                            umma_f16(dst, sdesc_advance(da, kk * 32), sdesc_advance(db, kk * 32), idesc_s, (d | kk) != 0);
                         if (a_slot >= 0) give(a_slot);
                         give(rp.slot);
                         rp.advance(gm.stages);
@@ -423,16 +425,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 for (int cc = 0; cc < C; ++cc) {
                     const uint8_t* zs = (cc == c) ? sZown : sZ + slot_of(cc, c) * 32768;
+                    const uint64_t dz = sdesc_sw128(smem_u32(zs), 16, 1024);
                     for (int vc = 0; vc < 4; ++vc) {
                         const uint8_t* W = take();
                         if (!W) return false;
+                        const uint64_t dw = sdesc_sw128(smem_u32(W), 32 * 128, 1024);
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
                             const int kt = vc * 32 + t * 16;
-                            const uint64_t bd = sdesc_sw128(smem_u32(W + t * 2048), 32 * 128, 1024);
                             const uint32_t acc = (s | cc | vc | t) != 0;
-                            umma_f16(t_acc, sdesc_sw128(smem_u32(zs + (kt / 64) * 16384 + (kt % 64) * 2), 16, 1024),
-                                     bd, idesc_v, acc);
+                            umma_f16(t_acc, sdesc_advance(dz, (kt / 64) * 16384 + (kt % 64) * 2), sdesc_advance(dw, t * 2048),
+                                     idesc_v, acc);
                         }
                         give(rp.slot);
                         rp.advance(gm.stages);

@@ -923,6 +923,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool full = j_lo <= col0 && j_hi >= col0 + 64;
                 const float* s_l2 = stats + sbuf * 128;
                 const float* s_dl = stats + 256 + sbuf * 128;
+                // column statistics of my columns col0 + 4 i .. + 3 in one 16-byte load
+                // (the statistics area is 1 KiB aligned, col0 a multiple of 64)
+                auto stat4 = [&](const float* base, int jj) { return *reinterpret_cast<const float4*>(base + jj); };
                 if constexpr (!T::kTwo) {
                     // dV: Z = P^T of my 64 columns
 #pragma unroll
@@ -930,14 +933,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t x[32];
                         tmem_ld32(tx + col0 + q2 * 32, x);
                         tmem_ld_wait(x);
+                        float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
+                            if ((e & 1) == 0) l4 = stat4(s_l2, col0 + q2 * 32 + 2 * e);
+                            const float l2e[2] = {(e & 1) ? l4.z : l4.x, (e & 1) ? l4.w : l4.y};
                             float zz[2];
 #pragma unroll
                             for (int u = 0; u < 2; ++u) {
                                 const int j = col0 + q2 * 32 + 2 * e + u;
                                 const bool legal = full || (j >= j_lo && j < j_hi);
-                                zz[u] = legal ? ex2_approx(fmaf(__uint_as_float(x[2 * e + u]), c2, -s_l2[j])) : 0.f;
+                                zz[u] = legal ? ex2_approx(fmaf(__uint_as_float(x[2 * e + u]), c2, -l2e[u])) : 0.f;
                             }
                             z[q2 * 16 + e] = pack2<BF16>(zz[0], zz[1]);
                         }
@@ -953,15 +959,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q2 = 0; q2 < 2; ++q2) {
                         const uint32_t (&x)[32] = q2 ? xb : xa;
+                        float4 l4 = make_float4(l2_row, l2_row, l2_row, l2_row);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
+                            if (!T::kRowsQ && (e & 1) == 0) l4 = stat4(s_l2, col0 + q2 * 32 + 2 * e);
+                            const float l2e[2] = {(e & 1) ? l4.z : l4.x, (e & 1) ? l4.w : l4.y};
                             float pv[2];
 #pragma unroll
                             for (int u = 0; u < 2; ++u) {
                                 const int j = col0 + q2 * 32 + 2 * e + u;
                                 const bool legal = full || (j >= j_lo && j < j_hi);
-                                const float l2 = T::kRowsQ ? l2_row : s_l2[j];
-                                pv[u] = legal ? ex2_approx(fmaf(__uint_as_float(x[2 * e + u]), c2, -l2)) : 0.f;
+                                pv[u] = legal ? ex2_approx(fmaf(__uint_as_float(x[2 * e + u]), c2, -l2e[u])) : 0.f;
                             }
                             pp[q2 * 16 + e] = pack2<false>(pv[0], pv[1]);
                         }
@@ -1006,12 +1014,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q2 = 0; q2 < 2; ++q2) {
                         const uint32_t (&y)[32] = q2 ? yb : ya;
+                        float4 d4 = make_float4(dl_row, dl_row, dl_row, dl_row);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const float2 pv = unpack2<false>(pp[q2 * 16 + e]);
-                            const int j = col0 + q2 * 32 + 2 * e;
-                            const float d0v = T::kRowsQ ? dl_row : s_dl[j];
-                            const float d1v = T::kRowsQ ? dl_row : s_dl[j + 1];
+                            if (!T::kRowsQ && (e & 1) == 0) d4 = stat4(s_dl, col0 + q2 * 32 + 2 * e);
+                            const float d0v = (e & 1) ? d4.z : d4.x;
+                            const float d1v = (e & 1) ? d4.w : d4.y;
                             z[q2 * 16 + e] = pack2<BF16>(pv.x * (__uint_as_float(y[2 * e]) - d0v),
                                                          pv.y * (__uint_as_float(y[2 * e + 1]) - d1v));
                         }

@@ -641,6 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool full = j_lo <= col0 && j_hi >= col0 + 64;
                 const float* s_l2 = stats + sbuf * 128;
                 const float* s_dl = stats + 256 + sbuf * 128;
+                // column statistics of my columns col0 + 4 i .. + 3 in one 16-byte load
+                // (the statistics area is 1 KiB aligned, col0 a multiple of 64)
+                auto stat4 = [&](const float* base, int jj) { return *reinterpret_cast<const float4*>(base + jj); };
                 if (OP == XOP_DK && st_p) {
                     // dK storing P: P^T (input dtype) goes through the own slot first;
                     // its store runs while dS^T is formed, then dS^T replaces it
@@ -650,14 +653,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t x[32];
                         tmem_ld32(tx + col0 + q2 * 32, x);
                         tmem_ld_wait(x);
+                        float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
+                            if ((e & 1) == 0) l4 = stat4(s_l2, col0 + q2 * 32 + 2 * e);
+                            const float l2e[2] = {(e & 1) ? l4.z : l4.x, (e & 1) ? l4.w : l4.y};
                             float pv[2];
 #pragma unroll
                             for (int u = 0; u < 2; ++u) {
                                 const int j = col0 + q2 * 32 + 2 * e + u;
                                 const bool legal = full || (j >= j_lo && j < j_hi);
-                                pv[u] = legal ? ex2_approx(fmaf(__uint_as_float(x[2 * e + u]), c2, -s_l2[j])) : 0.f;
+                                pv[u] = legal ? ex2_approx(fmaf(__uint_as_float(x[2 * e + u]), c2, -l2e[u])) : 0.f;
                             }
                             pp[q2 * 16 + e] = pack2<false>(pv[0], pv[1]);
                         }
@@ -698,12 +704,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t y[32];
                         tmem_ld32(ty + col0 + q2 * 32, y);
                         tmem_ld_wait(y);
+                        float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const int j = col0 + q2 * 32 + 2 * e;
+                            if ((e & 1) == 0) d4 = stat4(s_dl, col0 + q2 * 32 + 2 * e);
                             const float2 pv = unpack2<false>(pp[q2 * 16 + e]);
-                            z[q2 * 16 + e] = pack2<BF16>(pv.x * (__uint_as_float(y[2 * e]) - s_dl[j]),
-                                                         pv.y * (__uint_as_float(y[2 * e + 1]) - s_dl[j + 1]));
+                            z[q2 * 16 + e] = pack2<BF16>(pv.x * (__uint_as_float(y[2 * e]) - ((e & 1) ? d4.z : d4.x)),
+                                                         pv.y * (__uint_as_float(y[2 * e + 1]) - ((e & 1) ? d4.w : d4.y)));
                         }
                     }
                 } else {
@@ -714,8 +721,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (T::kTwo) tmem_ld32(ty + col0 + q2 * 32, y);
                     tmem_ld_wait(x);
                     if (T::kTwo) tmem_ld_wait(y);
+                    float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = l4;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
+                        if (!T::kRowsQ && (e & 1) == 0) {
+                            l4 = stat4(s_l2, col0 + q2 * 32 + 2 * e);
+                            if (OP == XOP_DK) d4 = stat4(s_dl, col0 + q2 * 32 + 2 * e);
+                        }
                         float zz[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
@@ -727,8 +739,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const float p = legal ? ex2_approx(fmaf(sv, c2, -l2_row)) : 0.f;
                                 v = p * (__uint_as_float(y[2 * e + u]) - dl_row);
                             } else {          // dV: P^T; dK: dS^T = P^T (dP^T - delta)
-                                const float p = legal ? ex2_approx(fmaf(sv, c2, -s_l2[j])) : 0.f;
-                                v = (OP == XOP_DK) ? p * (__uint_as_float(y[2 * e + u]) - s_dl[j]) : p;
+                                const float l2c = u ? ((e & 1) ? l4.w : l4.y) : ((e & 1) ? l4.z : l4.x);
+                                const float dlc = u ? ((e & 1) ? d4.w : d4.y) : ((e & 1) ? d4.z : d4.x);
+                                const float p = legal ? ex2_approx(fmaf(sv, c2, -l2c)) : 0.f;
+                                v = (OP == XOP_DK) ? p * (__uint_as_float(y[2 * e + u]) - dlc) : p;
                             }
                             zz[u] = v;
                         }

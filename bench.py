@@ -223,16 +223,16 @@ PAIR_SOURCES = ("xchg.cu", "xchg2.cu", "ptx.cuh", "tile_common.cuh", "kernels.h"
 DECODE_SOURCES = ("decode.cu", "ptx.cuh", "tile_common.cuh", "kernels.h")
 FP8_SOURCES = ("xchg2.cu", "fp8.cu", "ptx.cuh", "tile_common.cuh", "kernels.h", "host.cu")
 TRAFFIC = {
-    # dK (also storing P^T and dS^T) at 16 heads (759,003,392 + 4,367,645,184 bytes) scaled to 32
-    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 10253297152, "files": PAIR_SOURCES,
-                                             "sources": "b4ae15d955073a85"},
+    # dK (also storing P^T and dS^T) at 16 heads (742,801,920 + 4,366,761,984 bytes) scaled to 32
+    ("dense B1 H32 N8192 D512 bf16", "dk"): {"bytes": 10219127808, "files": PAIR_SOURCES,
+                                             "sources": "efbfe1587254af17"},
     # one ffpa_decode_fwd call: split kernel + combine (means over six calls)
-    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2156553558, "files": DECODE_SOURCES,
-                                                                "sources": "d7fa58a72259511f"},
+    ("decode B8 Hq32 Hkv8 Nq1 Nkv16384 D512 bf16", "decode"): {"bytes": 2156532053, "files": DECODE_SOURCES,
+                                                                "sources": "02d0bf078ccf84aa"},
     # the e4m3 attention kernel (reads q8, k8, V^T codes; writes O, LSE)
-    ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 638752666,
+    ("fp8 forward dense B1 H32 N8192 D512 (bf16 in, e4m3 compute)", "fp8"): {"bytes": 638714573,
                                                                              "files": FP8_SOURCES,
-                                                                             "sources": "c0568c01721855ba"},
+                                                                             "sources": "e6211f2e55439bed"},
 }
 
 
@@ -484,32 +484,17 @@ def run_fp8(args, w):
 
     e2e = None
     if not args.no_e2e:
+        # q, k, v in and O, LSE out every step; the quantization workspace is
+        # reused (the steps run in order on the compute stream)
         host = {n: inp[n].pin_memory() for n in ("q", "k", "v")}
-        dev_t = {n: torch.empty_like(q if n == "q" else k) for n in host}
-        oh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
-        def e2e_step():
-            for n in host:
-                dev_t[n].copy_(host[n], non_blocking=True)
-            api.fwd_fp8(dev_t["q"], dev_t["k"], dev_t["v"], w.causal, w.scale, out=o, lse=lse, workspace=ws)
-            oh.copy_(o, non_blocking=True)
-            lh.copy_(lse, non_blocking=True)
+        def call(x):
+            o_, l_ = api.fwd_fp8(x["q"], x["k"], x["v"], w.causal, w.scale, workspace=ws)
+            return {"o": o_, "lse": l_}
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        n = max(1, min(args.steps, 5))
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(n):
-            e2e_step()
-        s1.record(stream)
-        torch.cuda.synchronize()
-        ems = s0.elapsed_time(s1) / n
+        ems, h2d, d2h = overlapped_e2e(dev, stream, host, call, max(1, min(args.steps, 30)))
         e2e = {"value": world * f_fwd / (ems / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ems,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
-               "d2h_bytes_per_step": oh.numel() * oh.element_size() + lh.numel() * lh.element_size()}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "overlap": E2E_OVERLAP}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = fp8_cpu_baseline(w, inp)
@@ -895,26 +880,19 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def measure_e2e(w, args, dev, stream, inp, step_flops, world):
-    """Same metric through the public API with pinned host buffers: every step
-    copies q, k, v, dO host->device and reads dq, dk, dv back.
-
-    The copies run as a training loop runs them: on two copy streams, into
-    two device input buffers, so that step i+1's inputs move in and step i's
-    gradients move out while the GPU computes (the C2C link is full duplex).
+def overlapped_e2e(dev, stream, host, call, n):
+    """Steps through the public API from pinned host buffers, as a training or
+    serving loop runs them: each step copies its inputs (`host`) to the
+    device, runs `call` on them (which returns the step's outputs by name) and
+    reads every output back. The copies run on two copy streams, into two
+    device input buffers, so that step i+1's inputs move in and step i's
+    outputs move out while the GPU computes (the C2C link is full duplex).
     The timed region starts before the first input copy and ends after the
-    last gradient copy."""
+    last output copy. Returns (ms per step, h2d bytes, d2h bytes per step)."""
     import torch
 
-    from head_dim_flash_gb300 import api
-
-    names = ("q", "k", "v", "dO") + (("cu_seqlens",) if w.varlen else ())
-    host = {n: inp[n].pin_memory() for n in names}
-    bufs = [{n: torch.empty_like(host[n], device=dev) for n in host} for _ in range(2)]
-    out_h = {n: torch.empty(inp[src].shape, dtype=inp[src].dtype).pin_memory()
-             for n, src in (("dq", "q"), ("dk", "k"), ("dv", "v"))}
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+    bufs = [{k: torch.empty_like(t, device=dev) for k, t in host.items()} for _ in range(2)]
+    out_h = {}  # pinned host copies of the outputs, allocated at the first step
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     in_ready = [torch.cuda.Event() for _ in range(2)]  # inputs of buffer b landed
     buf_free = [None, None]                            # last step that read buffer b is done
@@ -924,14 +902,61 @@ def measure_e2e(w, args, dev, stream, inp, step_flops, world):
         with torch.cuda.stream(s_in):
             if buf_free[b] is not None:
                 s_in.wait_event(buf_free[b])
-            for n in host:
-                bufs[b][n].copy_(host[n], non_blocking=True)
+            for k in host:
+                bufs[b][k].copy_(host[k], non_blocking=True)
             in_ready[b].record(s_in)
 
     def compute(i):
         b = i % 2
-        x = bufs[b]
         stream.wait_event(in_ready[b])
+        outs = call(bufs[b])
+        done = torch.cuda.Event()
+        done.record(stream)
+        buf_free[b] = done
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            for k, g in outs.items():
+                if k not in out_h:
+                    out_h[k] = torch.empty(g.shape, dtype=g.dtype).pin_memory()
+                g.record_stream(s_out)  # not reused before the copy has read it
+                out_h[k].copy_(g, non_blocking=True)
+
+    def run(m, start=None):
+        if start is not None:
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+        copy_in(0)
+        for i in range(m):
+            if i + 1 < m:
+                copy_in(i + 1)
+            compute(i)
+        stream.wait_stream(s_out)
+
+    run(2)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    run(n, start=s)
+    e.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+    return s.elapsed_time(e) / n, h2d, d2h
+
+
+E2E_OVERLAP = ("double-buffered inputs; copies on two side streams overlap the compute of the "
+               "neighbouring steps; first copy-in and last copy-out inside the timed region")
+
+
+def measure_e2e(w, args, dev, stream, inp, step_flops, world):
+    """Same metric through the public API with pinned host buffers: every step
+    copies q, k, v, dO host->device and reads dq, dk, dv back (overlapped_e2e)."""
+    from head_dim_flash_gb300 import api
+
+    names = ("q", "k", "v", "dO") + (("cu_seqlens",) if w.varlen else ())
+    host = {n: inp[n].pin_memory() for n in names}
+
+    def call(x):
         if w.varlen:
             cu, mx = x["cu_seqlens"], max(w.seqlens)
             o, lse = api.varlen_fwd(x["q"], x["k"], x["v"], cu, cu, mx, mx, w.causal, w.scale)
@@ -939,41 +964,13 @@ def measure_e2e(w, args, dev, stream, inp, step_flops, world):
         else:
             o, lse = api.fwd(x["q"], x["k"], x["v"], w.causal, w.scale)
             grads = api.bwd(x["q"], x["k"], x["v"], o, lse, x["dO"], w.causal, w.scale)
-        done = torch.cuda.Event()
-        done.record(stream)
-        buf_free[b] = done
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(done)
-            for n, g in zip(("dq", "dk", "dv"), grads):
-                g.record_stream(s_out)  # not reused before the copy has read it
-                out_h[n].copy_(g, non_blocking=True)
+        return dict(zip(("dq", "dk", "dv"), grads))
 
-    def run(n, start=None):
-        if start is not None:
-            s_in.wait_event(start)
-            s_out.wait_event(start)
-        copy_in(0)
-        for i in range(n):
-            if i + 1 < n:
-                copy_in(i + 1)
-            compute(i)
-        stream.wait_stream(s_out)
-
-    run(2)
-    torch.cuda.synchronize()
     # 30 steps: the first copy-in and the last copy-out (a few ms) that no
     # compute overlaps are spread over a run of training-loop length
-    n = max(1, min(args.steps, 30))
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    run(n, start=s)
-    e.record(stream)
-    torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / n
+    ms, h2d, d2h = overlapped_e2e(dev, stream, host, call, max(1, min(args.steps, 30)))
     return {"value": world * step_flops / (ms / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "overlap": "double-buffered inputs; copies on two side streams overlap the compute of the "
-                       "neighbouring steps; first copy-in and last copy-out inside the timed region"}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "overlap": E2E_OVERLAP}
 
 
 def main():

@@ -70,6 +70,7 @@ struct PGeo {
     int nprod;   // producer lanes (ring positions are dealt round-robin)
     int n_rt;    // row tiles of 256 per (batch, head) in the grid (of the longest sequence)
     int n_bz;    // (batch, head) entries in the grid
+    int ostore;  // the output map is valid: whole 128-row tiles leave through shared memory and TMA
 };
 
 template <int OP>
@@ -91,6 +92,7 @@ struct __align__(1024) StaticSmem {
     uint64_t stored[2];      // (dK storing dS) the store of the own Z buffer has read it
     uint64_t p_full[2];      // (dK storing P) the own Z buffer holds the step's P^T
     uint64_t p_read[2];      // (dK storing P) the store of that P^T has read the buffer
+    uint64_t ostage;         // every elementwise thread staged its part of the output tile
 };
 static_assert(sizeof(StaticSmem) == 1024, "static shared block must be exactly 1 KiB");
 
@@ -115,7 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     pair_kernel(const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tA2,
                 const __grid_constant__ CUtensorMap tB1, const __grid_constant__ CUtensorMap tB2,
                 const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tS,
-                const __grid_constant__ CUtensorMap tP, const XArgs a, const PGeo gm)
+                const __grid_constant__ CUtensorMap tP, const __grid_constant__ CUtensorMap tO, const XArgs a,
+                const PGeo gm)
 {
     // the next GEMM kernel of a backward may take SMs as this grid's last CTAs start
     pdl_trigger();
@@ -239,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         mbar_init(&sh.half, 256);
+        mbar_init(&sh.ostage, 256);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.stored[i], 1);
             mbar_init(&sh.p_full[i], 256);
@@ -1113,8 +1117,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t orow = static_cast<size_t>(bco) * ov.sb + static_cast<size_t>(row_head) * ov.sh +
                                 static_cast<size_t>(row_co(row)) * ov.sn;
             uint16_t* dst = reinterpret_cast<uint16_t*>(out) + orow + d0;
+            // Whole 128-row tiles of the 16-bit kernels leave through the idle ring
+            // (after its first KiB, the forward's row-sum scratch) and TMA stores of
+            // 128 rows x 128 columns: one row per thread would make every warp store
+            // touch 32 rows. Columns past the head dim fall outside the map.
+            uint8_t* ostage = sRing + 1024;
+            const bool via_tma = !F8 && gm.ostore && n_steps > 0 && r0 + 128 <= row_len &&
+                                 1024 + 128 * sw * 2 <= gm.stages * kSlot;
+            if (via_tma) {
+                for (int cc = half * (sw / 2); cc < (half + 1) * (sw / 2); cc += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(t_acc + lane_off + cc, v);
+                    tmem_ld_wait(v);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                    // box cc / 128 holds 64-column chunks 2 q, 2 q + 1 of the slab, 16 KiB each
+                    uint8_t* blk = ostage + (cc >> 7) * 32768 + ((cc >> 6) & 1) * 16384;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        *reinterpret_cast<uint4*>(blk + sw128_offset(r, ((cc & 63) >> 3) + e)) =
+                            make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&sh.ostage);
+                if (ew == 0) {
+                    if (mbar_wait(&sh.ostage, 0, abort_flag, status, lim, PS_EPI)) {
+                        for (int q = 0; q < sw / 128; ++q)
+                            tma_store_5d(&tO, ostage + q * 32768, 0, row_co(r0), d0 / 64 + 2 * q, row_head, bco);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                    }
+                }
+            }
             // columns past the output's head dim are not stored
-            const int c_end = min((half + 1) * (sw / 2), (a.d_out > 0 ? a.d_out : pb.D) - d0);
+            const int c_end = via_tma ? 0 : min((half + 1) * (sw / 2), (a.d_out > 0 ? a.d_out : pb.D) - d0);
             for (int cc = half * (sw / 2); cc < c_end; cc += 32) {
                 uint32_t v[32];
                 if (n_steps > 0) {
@@ -1181,7 +1219,8 @@ cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, PGeo gm, int n_rt
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], a, gm);
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], a,
+                              gm);
 }
 
 template <int OP>
@@ -1243,7 +1282,7 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const Src sdo = q_empty ? Src{a.k, pb.vk, true} : (a.dO ? Src{a.dO, pb.vdo, false} : sq);
     const Src sk = kv_empty ? Src{a.q, pb.vq, false} : Src{a.k, pb.vk, true};
     const Src sv = kv_empty ? Src{a.q, pb.vq, false} : Src{a.v, pb.vv, true};
-    CUtensorMap m[7];
+    CUtensorMap m[8];
     bool okm = true;
     auto row = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 128, 2, x.v); };
     auto col = [&](int i, const Src& x) { okm = okm && make_slab_map(&m[i], x.p, pb, x.kv_side, a.bf16, 64, 4, x.v); };
@@ -1262,6 +1301,8 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
         m[3] = m[2];
         m[5] = m[0];
         m[6] = m[0];
+        m[7] = m[0];
+        gm.ostore = 0;
         if (!okm) return cudaErrorInvalidValue;
         const int n_rt8 = (pb.Nq + 255) / 256;
         const int bz8 = pb.B * pb.Hq;
@@ -1294,6 +1335,14 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     if (op == XOP_DK && a.store_p) okm = okm && make_ds_map(&m[6], a.p, pb, a.bf16, 128, ng * (pb.Hq / pb.Hkv));
     else m[6] = m[0];
     if (!okm) return cudaErrorInvalidValue;
+    // the output as 128-row x 2-chunk boxes (the kernel stores whole row tiles
+    // through it; a view the map cannot describe keeps the per-row stores)
+    {
+        const void* out = op == XOP_FWD ? a.o : op == XOP_DQ ? a.dq : op == XOP_DV ? a.dv : a.dk;
+        const View ov = op == XOP_FWD ? pb.vo : op == XOP_DQ ? pb.vdq : op == XOP_DV ? pb.vdv : pb.vdk;
+        gm.ostore = make_slab_map(&m[7], out, pb, !rows_q, a.bf16, 128, 2, ov) ? 1 : 0;
+        if (!gm.ostore) m[7] = m[0];
+    }
     const int n_rt = (n_rows + 255) / 256;
     if (n_rt == 0 || bz == 0) return cudaSuccess;
     switch (op) {

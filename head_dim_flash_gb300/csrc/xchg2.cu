@@ -1125,20 +1125,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool via_tma = !F8 && gm.ostore && n_steps > 0 && r0 + 128 <= row_len &&
                                  1024 + 128 * sw * 2 <= gm.stages * kSlot;
             if (via_tma) {
-                for (int cc = half * (sw / 2); cc < (half + 1) * (sw / 2); cc += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(t_acc + lane_off + cc, v);
-                    tmem_ld_wait(v);
-                    uint32_t w[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                // one 64-column chunk per round: two TMEM loads, one wait
+                for (int cc = half * (sw / 2); cc < (half + 1) * (sw / 2); cc += 64) {
+                    uint32_t va[32], vb[32];
+                    tmem_ld32(t_acc + lane_off + cc, va);
+                    tmem_ld32(t_acc + lane_off + cc + 32, vb);
+                    tmem_ld_wait(va, vb);
                     // box cc / 128 holds 64-column chunks 2 q, 2 q + 1 of the slab, 16 KiB each
                     uint8_t* blk = ostage + (cc >> 7) * 32768 + ((cc >> 6) & 1) * 16384;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        *reinterpret_cast<uint4*>(blk + sw128_offset(r, ((cc & 63) >> 3) + e)) =
-                            make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    for (int p2 = 0; p2 < 2; ++p2) {
+                        const uint32_t (&v)[32] = p2 ? vb : va;
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint4*>(blk + sw128_offset(r, 4 * p2 + e)) =
+                                make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    }
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&sh.ostage);

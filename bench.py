@@ -816,8 +816,8 @@ def run_ours(args):
             "at_clock": at_clock(achieved, clocks.get("sm_mhz"))}
     if dom == "dk" and alone:
         # bytes the dK launch must move (Q, dO, K, V read; dK written), and the
-        # stored-tile writes it adds (a memory-for-FLOPs trade of this build,
-        # not work of the method)
+        # stored-tile writes it adds (the stored-tile backward's trade of memory
+        # for FLOPs, not work of the method)
         e = 2
         roof["algorithmic_bytes"] = e * w.D * (2 * w.B * w.Hq * w.Nq + 3 * w.B * w.Hkv * w.Nkv)
         roof["stored_tile_bytes"] = 2 * e * w.B * w.Hq * w.Nkv * ((w.Nq + 7) // 8 * 8) if ds_path else 0

@@ -55,6 +55,7 @@ struct Geo {
     int res;          // leading 64-wide chunks of the first row operand kept resident in shared memory
     int n_rt;         // row tiles of 128 per (batch, head) in the grid (of the longest sequence)
     int n_bz;         // (batch, head) entries in the grid
+    int ostore;       // the output map is valid: whole 128-row tiles leave through shared memory and TMA
 };
 
 template <int OP>
@@ -76,6 +77,7 @@ struct __align__(1024) StaticSmem {
     int abort_flag;
     // dK storing tiles: the own slot holds P^T / its store read it; the dS store read it
     uint64_t p_full, p_read, stored;
+    uint64_t ostage;  // every elementwise thread staged its part of the output tile
 };
 static_assert(sizeof(StaticSmem) == 1024, "static shared block must be exactly 1 KiB");
 
@@ -95,7 +97,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     xchg_kernel(const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tA2,
                 const __grid_constant__ CUtensorMap tB1, const __grid_constant__ CUtensorMap tB2,
                 const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tS,
-                const __grid_constant__ CUtensorMap tP, const XArgs a, const Geo gm)
+                const __grid_constant__ CUtensorMap tP, const __grid_constant__ CUtensorMap tO, const XArgs a,
+                const Geo gm)
 {
     // the next GEMM kernel of a backward may take SMs as this grid's last CTAs start
     pdl_trigger();
@@ -214,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bar_z_full, 256);
         mbar_init(&bar_half, 256);
+        mbar_init(&sh.ostage, 256);
         mbar_init(&bar_acc, 1);
         for (int i = 0; i < kMaxC; ++i) {
             mbar_init(&bar_zpeer[i], 1);
@@ -846,7 +850,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t orow = static_cast<size_t>(bco) * ov.sb + static_cast<size_t>(row_head) * ov.sh +
                                 static_cast<size_t>(row_co(row)) * ov.sn;
             uint16_t* dst = reinterpret_cast<uint16_t*>(out) + orow + d0;
-            const int c_end = min((half + 1) * (sw / 2), pb.D - d0);  // columns past D are not stored
+            // Whole 128-row tiles leave through the idle ring (after its first KiB,
+            // the forward's row-sum scratch) and one TMA store per 64-column chunk of
+            // the slab: one row per thread would make every warp store touch 32 rows.
+            uint8_t* ostage = sRing + 1024;
+            const bool via_tma = gm.ostore && n_steps > 0 && r0 + 128 <= row_len &&
+                                 1024 + nb * 16384 <= gm.stages * 16384;
+            if (via_tma) {
+                for (int cc = half * (sw / 2); cc < (half + 1) * (sw / 2); cc += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(t_acc + lane_off + cc, v);
+                    tmem_ld_wait(v);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                    uint8_t* blk = ostage + (cc >> 6) * 16384;  // chunk cc / 64: 128 rows x 128 bytes
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        *reinterpret_cast<uint4*>(blk + sw128_offset(r, ((cc & 63) >> 3) + e)) =
+                            make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&sh.ostage);
+                if (ew == 0) {
+                    if (mbar_wait(&sh.ostage, 0, abort_flag, status, lim, XS_EPI)) {
+                        for (int j = 0; j < nb; ++j)
+                            tma_store_5d(&tO, ostage + j * 16384, 0, row_co(r0), c_begin + j, row_head, bco);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                    }
+                }
+            }
+            // columns past D are not stored
+            const int c_end = via_tma ? 0 : min((half + 1) * (sw / 2), pb.D - d0);
             for (int cc = half * (sw / 2); cc < c_end; cc += 32) {
                 uint32_t v[32];
                 if (n_steps > 0) {
@@ -912,7 +949,8 @@ cudaError_t launch_op(const XArgs& a, const CUtensorMap* maps, Geo gm, int n_rt,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], a, gm);
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], a,
+                              gm);
 }
 
 template <int OP>
@@ -965,7 +1003,7 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
     const Src sdo = q_empty ? Src{a.k, pb.vk, true} : (a.dO ? Src{a.dO, pb.vdo, false} : sq);
     const Src sk = kv_empty ? Src{a.q, pb.vq, false} : Src{a.k, pb.vk, true};
     const Src sv = kv_empty ? Src{a.q, pb.vq, false} : Src{a.v, pb.vv, true};
-    CUtensorMap m[7];
+    CUtensorMap m[8];
     bool okm = true;
     auto mk = [&](int i, const Src& x, int rows) {
         // value operand: one box of 32 rows x the slab's chunks, or (D % 64 != 0) a
@@ -1001,6 +1039,15 @@ cudaError_t launch_single(int op, const XArgs& a, cudaStream_t s)
     if (op == XOP_DK && a.store_p) okm = okm && make_ds_map(&m[6], a.p, pb, a.bf16, 128, ng * (pb.Hq / pb.Hkv));
     else m[6] = m[0];
     if (!okm) return cudaErrorInvalidValue;
+    // the output as 128-row x 1-chunk boxes (whole row tiles leave through it;
+    // head dims that are not whole 64-column chunks, and views the map cannot
+    // describe, keep the per-row stores)
+    {
+        const void* out = op == XOP_FWD ? a.o : op == XOP_DQ ? a.dq : op == XOP_DV ? a.dv : a.dk;
+        const View ov = op == XOP_FWD ? pb.vo : op == XOP_DQ ? pb.vdq : op == XOP_DV ? pb.vdv : pb.vdk;
+        gm.ostore = (pb.D % 64 == 0 && make_slab_map(&m[7], out, pb, !rows_q, a.bf16, 128, 1, ov)) ? 1 : 0;
+        if (!gm.ostore) m[7] = m[0];
+    }
     if (n_rt == 0 || bz == 0) return cudaSuccess;
     switch (op) {
     case XOP_FWD: return dispatch<XOP_FWD>(a, m, gm, n_rt, bz, smem, s);

@@ -43,6 +43,7 @@ enum QSite : uint32_t { QS_PROD = 112, QS_RING, QS_ACC, QS_DRAIN };
 
 struct __align__(1024) QStatic {
     uint64_t full[kQStages], empty[kQStages], acc;
+    uint64_t ostage;  // every epilogue thread staged its output row
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -53,12 +54,13 @@ struct QGeo {
     int stage_bytes;  // ring slot per CTA: A (16 KiB) + B (nj_max x 16 KiB)
     int n_rt;         // row tiles of 256 per (batch, head) in the grid (of the longest sequence)
     int n_bz;         // (batch, head) entries in the grid
+    int ostore;       // the output map is valid: whole 128-row tiles leave through shared memory and TMA
 };
 
 template <bool BF16, bool DV>
 __global__ void __launch_bounds__(kQThreads, 1)
-    dsq_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB, const DsqArgs a,
-               const QGeo gm)
+    dsq_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+               const __grid_constant__ CUtensorMap tO, const DsqArgs a, const QGeo gm)
 {
     const Problem& pb = a.pb;
     const int rank = static_cast<int>(cluster_ctarank());
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             mbar_init(&sh.empty[i], 1);
         }
         mbar_init(&sh.acc, 1);
+        mbar_init(&sh.ostage, 128);
         sh.abort_flag = 0;
         // the even rank's full barriers count both CTAs' bytes
         if (leader)
@@ -248,7 +251,44 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const size_t tok = static_cast<size_t>((DV ? tk0 : tq0) + q);  // row (packed: token)
             uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + static_cast<size_t>(bco) * vo.sb +
                             static_cast<size_t>(h) * vo.sh + tok * vo.sn + c0;
-            for (int cc = 0; cc < w; cc += 32) {
+            // Whole 128-row tiles leave through the idle ring and TMA stores of 128
+            // rows x 128 columns (columns past D fall outside the map): one row per
+            // thread would make every warp store touch 32 rows.
+            const bool via_tma = gm.ostore && n_it > 0 && rc + 128 <= n_rows;
+            if (via_tma) {
+                for (int cc = 0; cc < w; cc += 64) {
+                    uint32_t va[32], vb[32];
+                    tmem_ld32(tmem + lane_off + cc, va);
+                    tmem_ld32(tmem + lane_off + cc + 32, vb);
+                    tmem_ld_wait(va, vb);
+                    // box cc / 128 holds 64-column chunks 2 q, 2 q + 1 of the slab, 16 KiB each
+                    uint8_t* blk = smem + (cc >> 7) * 32768 + ((cc >> 6) & 1) * 16384;
+#pragma unroll
+                    for (int p2 = 0; p2 < 2; ++p2) {
+                        const uint32_t (&v)[32] = p2 ? vb : va;
+                        uint32_t wp[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            wp[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint4*>(blk + sw128_offset(r, 4 * p2 + e)) =
+                                make_uint4(wp[4 * e], wp[4 * e + 1], wp[4 * e + 2], wp[4 * e + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&sh.ostage);
+                if (threadIdx.x == 64) {
+                    if (mbar_wait(&sh.ostage, 0, abort_flag, status, lim, QS_ACC)) {
+                        const int row_first = (DV ? tk0 : tq0) + rc;
+                        for (int qb = 0; qb < (w + 127) / 128; ++qb)
+                            tma_store_5d(&tO, smem + qb * 32768, 0, row_first, c0 / 64 + 2 * qb, h, bco);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                    }
+                }
+            }
+            for (int cc = 0; cc < (via_tma ? 0 : w); cc += 32) {
                 uint32_t v[32];
                 if (n_it > 0) {
                     tmem_ld32(tmem + lane_off + cc, v);
@@ -335,12 +375,16 @@ cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s)
     const int G = pb.Hq / pb.Hkv;
     const int ng = a.ng > 0 ? a.ng : pb.Hkv;  // kv groups of this launch (their query heads in the tiles)
     if (a.g0 < 0 || a.g0 + ng > pb.Hkv) return cudaErrorInvalidValue;
+    CUtensorMap tO;
     const bool okm = a.dv ? make_ds_map(&tA, a.tiles, pb, a.bf16, 128, ng * G) &&
                                 make_slab_map(&tB, a.rhs, pb, false, a.bf16, 64, 2, pb.vdo)
                           : make_ds_map(&tA, a.tiles, pb, a.bf16, 64, ng * G) &&
                                 make_slab_map(&tB, a.rhs, pb, true, a.bf16, 64, 2, pb.vk);
     if (!okm) return cudaErrorInvalidValue;
     QGeo gm{};
+    // the output as 128-row x 2-chunk boxes (a view the map cannot describe keeps the row stores)
+    gm.ostore = make_slab_map(&tO, a.out, pb, a.dv != 0, a.bf16, 128, 2, a.dv ? pb.vdv : pb.vdq) ? 1 : 0;
+    if (!gm.ostore) tO = tA;
     gm.nj_max = (min(pb.D, 512) + 255) / 256;
     gm.stage_bytes = 16384 * (1 + gm.nj_max);
     const int n_slab = (pb.D + 511) / 512;
@@ -366,7 +410,7 @@ cudaError_t launch_dsq(const DsqArgs& a, cudaStream_t s)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tA, tB, a, gm);
+    return cudaLaunchKernelEx(&cfg, kern, tA, tB, tO, a, gm);
 }
 
 }  // namespace ffpa

@@ -52,10 +52,23 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdArgs a, lo
         const size_t off_d = bb * pb.vdo.sb + h * pb.vdo.sh + i * pb.vdo.sn;
         const uint4* o4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.o) + off_o);
         const uint4* d4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.dO) + off_d);
+        // every load of the row is issued before the first product (D <= 1024:
+        // at most four 16-byte units of each tensor per lane)
+        constexpr int kMaxUnits = 1024 / 8 / 32;
+        uint4 xo[kMaxUnits], yd[kMaxUnits];
+#pragma unroll
+        for (int k = 0; k < kMaxUnits; ++k) {
+            const int i = lane + lanes * k;
+            if (i < D / 8) {
+                xo[k] = o4[i];
+                yd[k] = d4[i];
+            }
+        }
         float acc = 0.f;
-        for (int i = lane; i < D / 8; i += lanes) {
-            const uint4 x = o4[i], y = d4[i];
-            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int k = 0; k < kMaxUnits; ++k) {
+            if (lane + lanes * k >= D / 8) break;
+            const uint32_t xs[4] = {xo[k].x, xo[k].y, xo[k].z, xo[k].w}, ys[4] = {yd[k].x, yd[k].y, yd[k].z, yd[k].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 p = unpack2<BF16>(xs[e]), q = unpack2<BF16>(ys[e]);
@@ -82,8 +95,13 @@ cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t st)
     cudaError_t e;
     if (!q_empty && (a.stages & 1u)) {
         const int sms = num_sms() > 0 ? num_sms() : 148;
+        // one wave of resident blocks (a grid-stride loop over the rows)
+        static int per_sm = 0;
+        if (per_sm == 0 &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bwd_preprocess_kernel<BF16>, 256, 0) != cudaSuccess)
+            per_sm = 4;
         long blocks = (rows + 7) / 8;
-        const long cap = static_cast<long>(sms) * 8;
+        const long cap = static_cast<long>(sms) * (per_sm > 0 ? per_sm : 4);
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
         bwd_preprocess_kernel<BF16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, rows);

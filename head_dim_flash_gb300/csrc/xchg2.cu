@@ -1117,12 +1117,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t orow = static_cast<size_t>(bco) * ov.sb + static_cast<size_t>(row_head) * ov.sh +
                                 static_cast<size_t>(row_co(row)) * ov.sn;
             uint16_t* dst = reinterpret_cast<uint16_t*>(out) + orow + d0;
-            // Whole 128-row tiles of the 16-bit kernels leave through the idle ring
-            // (after its first KiB, the forward's row-sum scratch) and TMA stores of
-            // 128 rows x 128 columns: one row per thread would make every warp store
-            // touch 32 rows. Columns past the head dim fall outside the map.
+            // Whole 128-row tiles leave through the idle ring (after its first KiB,
+            // the forward's row-sum scratch) and TMA stores of 128 rows x 128
+            // columns: one row per thread would make every warp store touch 32 rows.
+            // Columns past the (real) head dim fall outside the map.
             uint8_t* ostage = sRing + 1024;
-            const bool via_tma = !F8 && gm.ostore && n_steps > 0 && r0 + 128 <= row_len &&
+            const bool via_tma = gm.ostore && n_steps > 0 && r0 + 128 <= row_len &&
                                  1024 + 128 * sw * 2 <= gm.stages * kSlot;
             if (via_tma) {
                 // one 64-column chunk per round: two TMEM loads, one wait
@@ -1307,9 +1307,14 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
         m[3] = m[2];
         m[5] = m[0];
         m[6] = m[0];
-        m[7] = m[0];
-        gm.ostore = 0;
         if (!okm) return cudaErrorInvalidValue;
+        // O (the input dtype, the real head dim) as 128-row x 2-chunk boxes
+        {
+            Problem po = pb;
+            po.D = a.d_out > 0 ? a.d_out : pb.D;
+            gm.ostore = (po.D % 64 == 0 && make_slab_map(&m[7], a.o, po, false, a.bf16, 128, 2, pb.vo)) ? 1 : 0;
+            if (!gm.ostore) m[7] = m[0];
+        }
         const int n_rt8 = (pb.Nq + 255) / 256;
         const int bz8 = pb.B * pb.Hq;
         if (n_rt8 == 0 || bz8 == 0) return cudaSuccess;

@@ -32,6 +32,8 @@ EXPORTS = (
     "ffpa_fp8_quantize",
     "ffpa_fwd_fp8",
     "ffpa_fwd_fp8_quantized",
+    "ffpa_varlen_fp8_workspace_bytes",
+    "ffpa_varlen_fwd_fp8",
     "ffpa_bwd_stages",
     "ffpa_bwd_noalloc",
     "ffpa_varlen_fwd",
@@ -85,6 +87,11 @@ def _declare(lib):
     lib.ffpa_fwd_fp8.restype = _i
     lib.ffpa_fwd_fp8_quantized.argtypes = [_i, View, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _p]
     lib.ffpa_fwd_fp8_quantized.restype = _i
+    lib.ffpa_varlen_fp8_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i]
+    lib.ffpa_varlen_fp8_workspace_bytes.restype = _sz
+    lib.ffpa_varlen_fwd_fp8.argtypes = [_i, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p,
+                                        _sz, _p]
+    lib.ffpa_varlen_fwd_fp8.restype = _i
     lib.ffpa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
     lib.ffpa_decode_workspace_bytes.restype = _sz
     lib.ffpa_decode_fwd.argtypes = [_i, View, View, View, View, _p, _p, _sz, _i, _i, _i, _i, _i, _i, _i, _f, _p]
@@ -199,6 +206,14 @@ def ffpa_fwd_fp8(*args):
 
 def ffpa_fwd_fp8_quantized(*args):
     return load().ffpa_fwd_fp8_quantized(*args)
+
+
+def ffpa_varlen_fp8_workspace_bytes(*args):
+    return load().ffpa_varlen_fp8_workspace_bytes(*args)
+
+
+def ffpa_varlen_fwd_fp8(*args):
+    return load().ffpa_varlen_fwd_fp8(*args)
 
 
 def ffpa_decode_workspace_bytes(*args):

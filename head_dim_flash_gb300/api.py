@@ -346,6 +346,35 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, 
     return o, lse
 
 
+def varlen_fp8_workspace(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k):
+    """Device scratch for varlen_fwd_fp8 (uint8, 256-byte aligned by the allocator)."""
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    batch = cu_seqlens_q.numel() - 1
+    n = int(_ffi.ffpa_varlen_fp8_workspace_bytes(batch, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def varlen_fwd_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False, scale=None,
+                   workspace=None):
+    """Packed FP8 (e4m3) forward through ffpa_varlen_fwd_fp8: each sequence quantized
+    per head as fwd_fp8 quantizes a batch entry. Returns (o [Tq,Hq,D], lse [Hq,Tq])."""
+    q, k, v = _prep(q, k, v)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    cq, ck = _cu(cu_seqlens_q, q.device), _cu(cu_seqlens_k, q.device)
+    batch = cq.numel() - 1
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    ws = varlen_fp8_workspace(q, k, cq, max_seqlen_q, max_seqlen_k) if workspace is None else workspace
+    st = _ffi.ffpa_varlen_fwd_fp8(_dt(q), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                  cq.data_ptr(), ck.data_ptr(), batch, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k),
+                                  Hq, Hkv, D, int(bool(causal)), _scale(scale, D), ws.data_ptr(), ws.numel(),
+                                  _stream())
+    _ffi.raise_for(st, "ffpa_varlen_fwd_fp8")
+    return o, lse
+
+
 def varlen_workspace_bytes(q, k, cu_seqlens_q, max_seqlen_q, max_seqlen_k, causal: bool,
                            budget: int = BWD_WORKSPACE_BUDGET) -> int:
     """Largest useful packed-backward workspace within `budget` bytes

@@ -570,6 +570,50 @@ ffpa_status ffpa_fwd_fp8_quantized(ffpa_dtype dt, ffpa_view o, float* lse, const
                          "fp8 launch");
 }
 
+size_t ffpa_varlen_fp8_workspace_bytes(int batch, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int Hq,
+                                       int Hkv, int D)
+{
+    if (batch <= 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || Hq <= 0 || Hkv <= 0 ||
+        D < 64 || D > 1024 || Hq % Hkv != 0 || D % 32 != 0)
+        return 0;
+    return ffpa::fp8_varlen_layout(batch, Hq, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, D).total;
+}
+
+ffpa_status ffpa_varlen_fwd_fp8(ffpa_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
+                                const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int total_q,
+                                int total_k, int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D, int causal,
+                                float scale, void* workspace, size_t workspace_bytes, ffpa_stream_t stream)
+{
+    FFPA_TRY(check_common(dt, Hq, Hkv, D, scale));
+    FFPA_TRY(check_varlen_sizes(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, cu_seqlens_q, cu_seqlens_k));
+    const long q_rows = batch > 0 ? static_cast<long>(total_q) * Hq : 0;
+    if (q_rows > 0 && total_k < 1) return fail(FFPA_ERR_NOT_SUPPORTED, "fp8 forward: total_k must be >= 1");
+    FFPA_TRY(check_ptr(q, q_rows > 0, "q"));
+    FFPA_TRY(check_ptr(k, q_rows > 0, "k"));
+    FFPA_TRY(check_ptr(v, q_rows > 0, "v"));
+    FFPA_TRY(check_ptr(o, q_rows > 0, "o"));
+    FFPA_TRY(check_ptr(lse, q_rows > 0, "lse"));
+    if (q_rows == 0) return ok();
+    const size_t need =
+        ffpa::fp8_varlen_layout(batch, Hq, Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, D).total;
+    if (workspace_bytes < need)
+        return fail(FFPA_ERR_INVALID_VALUE, "fp8 workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(FFPA_ERR_INVALID_VALUE, "fp8 workspace must be non-NULL and 256-byte aligned");
+    ffpa::FwdArgs a{};
+    a.pb = varlen_problem(batch, total_q, total_k, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, causal, scale, cu_seqlens_q,
+                          cu_seqlens_k);
+    FFPA_TRY(device_ctl(&a.ctl));
+    a.bf16 = dt == FFPA_BF16;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    return launch_result(ffpa::launch_fwd_fp8(a, workspace, reinterpret_cast<cudaStream_t>(stream), true),
+                         "fp8 varlen launch");
+}
+
 size_t ffpa_bwd_workspace_bytes_ds(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal)
 {
     const size_t small = ffpa_bwd_workspace_bytes(dt, B, Hq, Hkv, Nq, Nkv, D);

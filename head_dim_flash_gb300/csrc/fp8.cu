@@ -13,6 +13,12 @@
 // chunks for the tensor maps and the MMAs): the pad holds zero codes, which
 // add nothing to the scores, and the output columns past D are not stored.
 //   sq [B*Hq], sk [B*Hkv], sv [B*Hkv] fp32 dequantization scales
+// Packed (varlen) batches of B sequences are laid out as one batch entry of
+// all tokens: q8 [1, Hq, total_q, Dp], k8 [1, Hkv, total_k, Dp], and v8t
+// [1, Hkv, Dp, ldv] with sequence b's keys from column
+//   vt_col0(b) = 16 ceil(cu_k[b] / 16) + 16 b
+// (tensor-map loads of 8-bit codes start at multiples of 16 columns) and zero
+// codes in the gaps between sequences; the scales are per (sequence, head).
 // One scale per (batch, head) and tensor: amax = max |x| over the head,
 // scale = amax / 448, inv = 448 / amax (fp32, correctly rounded; 1 and 1 for
 // an all-zero head), code = e4m3(fp32(x * inv)) rounded to nearest even with
@@ -36,7 +42,9 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 struct QArgs {
     const void *q, *k, *v;
     View vq, vk, vv;
-    int B, Hq, Hkv, Nq, Nkv, D, ldv;
+    int B, Hq, Hkv, Nq, Nkv, D, ldv;  // packed batches: B sequences, Nq / Nkv their bound
+    const int *cu_q, *cu_k;           // packed batches: sequence offsets (device), else null
+    int total_q, total_k;
     int Dp;                 // code row length: D rounded up to 128 (zero codes past D)
     int nsq, nsk;           // row blocks per q head / per k or v head
     uint8_t *q8, *k8, *v8t;
@@ -56,6 +64,28 @@ __device__ __forceinline__ void tensor_of(const QArgs& a, int y, int& t, int& hi
     if (y < nq) { t = 0; hi = y; }
     else if (y < nq + nk) { t = 1; hi = y - nq; }
     else { t = 2; hi = y - nq - nk; }
+}
+
+// Rows of head hi (b * H + h) of tensor t: the n-th has token tok0 + n, n < len.
+// A packed sequence that breaks its bounds counts as empty here and returns
+// false (the attention kernel reports it).
+__device__ __forceinline__ bool seq_rows(const QArgs& a, int t, int hi, int& tok0, int& len)
+{
+    const int H = t == 0 ? a.Hq : a.Hkv;
+    const int N = t == 0 ? a.Nq : a.Nkv;
+    tok0 = 0;
+    len = N;
+    if (a.cu_q) {
+        const int* cu = t == 0 ? a.cu_q : a.cu_k;
+        const int total = t == 0 ? a.total_q : a.total_k;
+        const int b = hi / H;
+        const int c0 = cu[b], c1 = cu[b + 1];
+        const bool good = c0 >= 0 && c1 >= c0 && c1 <= total && c1 - c0 <= N;
+        tok0 = good ? c0 : 0;
+        len = good ? c1 - c0 : 0;
+        return good;
+    }
+    return true;
 }
 
 __device__ __forceinline__ const uint16_t* row_ptr(const QArgs& a, int t, int hi, int n)
@@ -89,14 +119,15 @@ __global__ void __launch_bounds__(256) amax_kernel(const QArgs a, bool bf16)
     if (y >= static_cast<long long>(a.B) * (a.Hq + 2 * a.Hkv)) return;
     int t, hi;
     tensor_of(a, static_cast<int>(y), t, hi);
-    const int N = t == 0 ? a.Nq : a.Nkv;
+    int tok0, N;
+    seq_rows(a, t, hi, tok0, N);
     const int ns = t == 0 ? a.nsq : a.nsk;
     if (static_cast<int>(blockIdx.x) >= ns) return;
     const int n0 = blockIdx.x * kQRows, n1 = min(N, n0 + kQRows);
     const int units = a.D / 8;  // 16-byte units per row
     float m = 0.f;
     for (int e = threadIdx.x; e < (n1 - n0) * units; e += blockDim.x) {
-        const uint4 w = *reinterpret_cast<const uint4*>(row_ptr(a, t, hi, n0 + e / units) + (e % units) * 8);
+        const uint4 w = *reinterpret_cast<const uint4*>(row_ptr(a, t, hi, tok0 + n0 + e / units) + (e % units) * 8);
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -139,18 +170,23 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const QArgs a, bool bf1
     if (y >= static_cast<long long>(a.B) * (a.Hq + a.Hkv)) return;
     int t, hi;
     tensor_of(a, static_cast<int>(y), t, hi);
-    const int N = t == 0 ? a.Nq : a.Nkv;
+    int tok0, N;
+    seq_rows(a, t, hi, tok0, N);
     const int ns = t == 0 ? a.nsq : a.nsk;
     if (static_cast<int>(blockIdx.x) >= ns) return;
     head_scale(a, t, hi, sm);
     const float inv = sm[1];
     if (blockIdx.x == 0 && threadIdx.x == 0) (t == 0 ? a.sq : a.sk)[hi] = sm[0];
-    uint8_t* out = (t == 0 ? a.q8 : a.k8) + static_cast<size_t>(hi) * N * a.Dp;
+    // codes of row n at out + n * Dp (packed: the head's token rows, from token tok0)
+    const int H = t == 0 ? a.Hq : a.Hkv;
+    const size_t head_rows = a.cu_q ? static_cast<size_t>(hi % H) * (t == 0 ? a.total_q : a.total_k) + tok0
+                                    : static_cast<size_t>(hi) * N;
+    uint8_t* out = (t == 0 ? a.q8 : a.k8) + head_rows * a.Dp;
     const int n0 = blockIdx.x * kQRows, n1 = min(N, n0 + kQRows);
     const int units = a.Dp / 8, in_units = a.D / 8;  // 8 codes per unit; units past D write zero codes
     for (int e = threadIdx.x; e < (n1 - n0) * units; e += blockDim.x) {
         const int n = n0 + e / units, u8 = e % units;
-        const uint4 w = u8 < in_units ? *reinterpret_cast<const uint4*>(row_ptr(a, t, hi, n) + u8 * 8)
+        const uint4 w = u8 < in_units ? *reinterpret_cast<const uint4*>(row_ptr(a, t, hi, tok0 + n) + u8 * 8)
                                       : make_uint4(0, 0, 0, 0);
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[2];
@@ -178,15 +214,33 @@ __global__ void __launch_bounds__(256) quant_vt_kernel(const QArgs a, bool bf16)
     head_scale(a, 2, hi, sm);
     const float inv = sm[1];
     if (blockIdx.x == 0 && threadIdx.x == 0) a.sv[hi] = sm[0];
+    int tok0, Nk;
+    if (!seq_rows(a, 2, hi, tok0, Nk)) return;  // nothing of a malformed sequence is written
     const int k0 = blockIdx.x * kVKeys;
-    const int nk = min(kVKeys, a.Nkv - k0);
+    const int nk = min(kVKeys, Nk - k0);
+    // the head's code rows; packed: the sequence's first column vt_col0(b)
+    int col0 = 0;
     uint8_t* out = a.v8t + static_cast<size_t>(hi) * a.Dp * a.ldv;
+    if (a.cu_q) {
+        const int b = hi / a.Hkv;
+        col0 = 16 * ((tok0 + 15) / 16) + 16 * b;
+        out = a.v8t + static_cast<size_t>(hi % a.Hkv) * a.Dp * a.ldv + col0;
+        if (blockIdx.x == 0) {
+            // zero codes from the sequence's last 16-key group to the next sequence
+            const int b1 = 16 * ((tok0 + Nk + 15) / 16) + 16 * (b + 1);  // cu_k[b + 1] = tok0 + Nk
+            const int z0 = col0 + (Nk + 15) / 16 * 16;
+            const int zn = min(b1, a.ldv) - z0;  // columns
+            for (int e = threadIdx.x; zn > 0 && e < a.Dp * zn; e += blockDim.x)
+                out[static_cast<size_t>(e / zn) * a.ldv + (z0 - col0) + e % zn] = 0;
+        }
+    }
     for (int d0 = 0; d0 < a.Dp; d0 += 64) {
         // load kVKeys x 64 (16-byte units: 8 per row; zeros past the keys and past D)
         for (int e = threadIdx.x; e < kVKeys * 8; e += blockDim.x) {
             const int r = e / 8, u = e % 8;
             uint4 w = make_uint4(0, 0, 0, 0);
-            if (r < nk && d0 + u * 8 < a.D) w = *reinterpret_cast<const uint4*>(row_ptr(a, 2, hi, k0 + r) + d0 + u * 8);
+            if (r < nk && d0 + u * 8 < a.D)
+                w = *reinterpret_cast<const uint4*>(row_ptr(a, 2, hi, tok0 + k0 + r) + d0 + u * 8);
             const uint32_t uu[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -198,7 +252,7 @@ __global__ void __launch_bounds__(256) quant_vt_kernel(const QArgs a, bool bf16)
         // store 64 d-rows x kVKeys keys: each thread 16 keys of one d-row
         {
             const int dr = threadIdx.x / (kVKeys / 16), kq = threadIdx.x % (kVKeys / 16);
-            if (dr < 64 && k0 + kq * 16 < a.Nkv) {
+            if (dr < 64 && k0 + kq * 16 < Nk) {
                 uint32_t o[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -242,10 +296,45 @@ Fp8Layout fp8_layout(int B, int Hq, int Hkv, int Nq, int Nkv, int D)
     return L;
 }
 
+Fp8Layout fp8_varlen_layout(int batch, int Hq, int Hkv, int total_q, int total_k, int max_q, int max_k, int D)
+{
+    Fp8Layout L{};
+    // sequence b's keys from column 16 ceil(cu_k[b] / 16) + 16 b: the last one ends
+    // by 16 ceil(total_k / 16) + 16 (batch - 1) + 16
+    L.ldv = 16 * ((total_k + 15) / 16) + 16 * batch;
+    L.dp = (D + 127) & ~127;
+    const size_t Dp = static_cast<size_t>(L.dp);
+    size_t off = 0;
+    L.q8 = off;
+    off = align256(off + static_cast<size_t>(Hq) * total_q * Dp);
+    L.k8 = off;
+    off = align256(off + static_cast<size_t>(Hkv) * total_k * Dp);
+    L.v8t = off;
+    off = align256(off + static_cast<size_t>(Hkv) * Dp * L.ldv);
+    L.sq = off;
+    off = align256(off + static_cast<size_t>(batch) * Hq * sizeof(float));
+    L.sk = off;
+    off = align256(off + static_cast<size_t>(batch) * Hkv * sizeof(float));
+    L.sv = off;
+    off = align256(off + static_cast<size_t>(batch) * Hkv * sizeof(float));
+    L.part = off;
+    const size_t nsq = (max_q + kQRows - 1) / kQRows, nsk = (max_k + kQRows - 1) / kQRows;
+    off = align256(off + (static_cast<size_t>(batch) * Hq * nsq + 2 * static_cast<size_t>(batch) * Hkv * nsk) *
+                             sizeof(float));
+    L.total = off;
+    return L;
+}
+
+Fp8Layout fp8_layout_of(const Problem& pb)
+{
+    return pb.varlen ? fp8_varlen_layout(pb.B, pb.Hq, pb.Hkv, pb.total_q, pb.total_k, pb.Nq, pb.Nkv, pb.D)
+                     : fp8_layout(pb.B, pb.Hq, pb.Hkv, pb.Nq, pb.Nkv, pb.D);
+}
+
 cudaError_t launch_fp8_quantize(const FwdArgs& f, void* workspace, cudaStream_t s)
 {
     const Problem& pb = f.pb;
-    const Fp8Layout L = fp8_layout(pb.B, pb.Hq, pb.Hkv, pb.Nq, pb.Nkv, pb.D);
+    const Fp8Layout L = fp8_layout_of(pb);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     QArgs a{};
     a.q = f.q;
@@ -259,6 +348,10 @@ cudaError_t launch_fp8_quantize(const FwdArgs& f, void* workspace, cudaStream_t 
     a.Hkv = pb.Hkv;
     a.Nq = pb.Nq;
     a.Nkv = pb.Nkv;
+    a.cu_q = pb.varlen ? pb.cu_q : nullptr;
+    a.cu_k = pb.varlen ? pb.cu_k : nullptr;
+    a.total_q = pb.total_q;
+    a.total_k = pb.total_k;
     a.D = pb.D;
     a.Dp = L.dp;
     a.ldv = L.ldv;
@@ -298,7 +391,7 @@ cudaError_t launch_fwd_fp8(const FwdArgs& f, void* workspace, cudaStream_t s, bo
         const cudaError_t e = launch_fp8_quantize(f, workspace, s);
         if (e != cudaSuccess) return e;
     }
-    const Fp8Layout L = fp8_layout(pb.B, pb.Hq, pb.Hkv, pb.Nq, pb.Nkv, pb.D);
+    const Fp8Layout L = fp8_layout_of(pb);
     const uint8_t* ws = static_cast<const uint8_t*>(workspace);
     XArgs x{};
     x.pb = pb;

@@ -134,6 +134,9 @@ struct Fp8Layout {
     int dp;  // code rows: the head dim rounded up to 128 (zero codes past D)
 };
 Fp8Layout fp8_layout(int B, int Hq, int Hkv, int Nq, int Nkv, int D);
+// packed batches of `batch` sequences (codes of all tokens, per-(sequence, head) scales)
+Fp8Layout fp8_varlen_layout(int batch, int Hq, int Hkv, int total_q, int total_k, int max_q, int max_k, int D);
+Fp8Layout fp8_layout_of(const Problem& pb);
 cudaError_t launch_fp8_quantize(const FwdArgs& a, void* workspace, cudaStream_t s);
 // (quantization pass, then) the CTA-pair forward on the e4m3 operands in `workspace`
 cudaError_t launch_fwd_fp8(const FwdArgs& a, void* workspace, cudaStream_t s, bool quantize);

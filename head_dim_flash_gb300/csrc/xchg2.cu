@@ -384,6 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto load_value = [&](int s) -> bool {
                 if constexpr (F8) {
                     const int vt_row = d0 + rh * (sw / 2);  // my half of the slab's V^T rows
+                    // V^T column of a key row of the sequence (packed: sequence b's keys
+                    // start at column 16 ceil(cu_k[b] / 16) + 16 b)
+                    const int vt0 = VARLEN ? 16 * ((tk0 + 15) / 16) + 16 * b : 0;
                     for (int k = 0; k < C; k += 2) {
                         const int ta = s * C + (c + k) % C;
                         const int tb = s * C + (c + min(k + 1, C - 1)) % C;
@@ -392,9 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             got = mbar_wait(&sh.empty[rp.slot], rp.phase ^ 1u, abort_flag, status, lim, PS_PROD);
                             if (got) {
                                 uint8_t* dst = sRing + rp.slot * kSlot;
-                                tma_load_4d_pair(dst, &tW, lead_full(rp.slot), col_co(col_row0(ta)), vt_row,
+                                tma_load_4d_pair(dst, &tW, lead_full(rp.slot), vt0 + col_row0(ta), vt_row,
                                                  col_head(ta), bco);
-                                tma_load_4d_pair(dst + 16384, &tW, lead_full(rp.slot), col_co(col_row0(tb)), vt_row,
+                                tma_load_4d_pair(dst + 16384, &tW, lead_full(rp.slot), vt0 + col_row0(tb), vt_row,
                                                  col_head(tb), bco);
                             }
                         }
@@ -1248,9 +1251,9 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const bool rows_q = (op == XOP_FWD || op == XOP_DQ);
     if (rows_q ? q_empty : kv_empty) return cudaSuccess;  // no output rows
     if (pb.D % 64 != 0) return cudaErrorInvalidConfiguration;  // chunked 5-D maps need D % 64 == 0
-    // FP8 forward: dense, the head dim padded to whole 128-column chunks (1 to 4 pairs)
+    // FP8 forward: the head dim padded to whole 128-column chunks (1 to 4 pairs)
     const bool f8 = a.f8 != 0;
-    if (f8 && (op != XOP_FWD || pb.varlen || pb.D % 128 != 0 || pb.D > 1024)) return cudaErrorInvalidConfiguration;
+    if (f8 && (op != XOP_FWD || pb.D % 128 != 0 || pb.D > 1024)) return cudaErrorInvalidConfiguration;
     const int nd = f8 ? pb.D / 128 : pb.D / 64;  // 128-byte chunks
     const int zb = f8 ? 16384 : 32768;           // bytes of one Z tile half
     const int d_pad = (pb.D + 127) & ~127;
@@ -1299,10 +1302,13 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
     const int ng = a.ng > 0 ? a.ng : pb.Hkv;
     if (a.g0 < 0 || a.g0 + ng > pb.Hkv) return cudaErrorInvalidValue;
     if (f8) {
-        // e4m3 codes: q8 (rows), k8 (columns), V^T (value operand, 128 head-dim rows per CTA)
-        okm = make_u8_slab_map(&m[0], a.q, pb.B, pb.Hq, pb.Nq, pb.D, 128, 2) &&
-              make_u8_slab_map(&m[2], a.k, pb.B, pb.Hkv, pb.Nkv, pb.D, 64, 4) &&
-              make_vt_map(&m[4], a.v8t, pb.B, pb.Hkv, pb.D, pb.Nkv, a.ldv, 128);
+        // e4m3 codes: q8 (rows), k8 (columns), V^T (value operand, 128 head-dim rows per CTA);
+        // packed batches: one batch entry of all tokens, V^T over all ldv columns
+        // (the gaps between sequences hold zero codes)
+        const int b8 = pb.varlen ? 1 : pb.B;
+        okm = make_u8_slab_map(&m[0], a.q, b8, pb.Hq, pb.varlen ? pb.total_q : pb.Nq, pb.D, 128, 2) &&
+              make_u8_slab_map(&m[2], a.k, b8, pb.Hkv, pb.varlen ? pb.total_k : pb.Nkv, pb.D, 64, 4) &&
+              make_vt_map(&m[4], a.v8t, b8, pb.Hkv, pb.D, pb.varlen ? a.ldv : pb.Nkv, a.ldv, 128);
         m[1] = m[0];
         m[3] = m[2];
         m[5] = m[0];
@@ -1318,6 +1324,9 @@ cudaError_t launch_pair(int op, const XArgs& a, cudaStream_t s)
         const int n_rt8 = (pb.Nq + 255) / 256;
         const int bz8 = pb.B * pb.Hq;
         if (n_rt8 == 0 || bz8 == 0) return cudaSuccess;
+        if (pb.varlen)
+            return a.bf16 ? launch_op<XOP_FWD, true, true, true>(a, m, gm, n_rt8, bz8, smem, s)
+                          : launch_op<XOP_FWD, false, true, true>(a, m, gm, n_rt8, bz8, smem, s);
         return a.bf16 ? launch_op<XOP_FWD, true, false, true>(a, m, gm, n_rt8, bz8, smem, s)
                       : launch_op<XOP_FWD, false, false, true>(a, m, gm, n_rt8, bz8, smem, s);
     }

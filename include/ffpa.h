@@ -147,8 +147,8 @@ FFPA_API ffpa_status ffpa_decode_fwd(ffpa_dtype dt, ffpa_view q, ffpa_view k, ff
  * accumulation; P is rounded to e4m3 for the P V product. O (bf16/fp16 as
  * the inputs) and LSE (fp32 [B, Hq, Nq]) as in ffpa_fwd_strided.
  *   D: any multiple of 32 in [64, 1024] (the pages' FP8 range, "Backends
- *   Overview", capability matrix), and Nkv >= 1 (else FFPA_ERR_NOT_SUPPORTED);
- *   dense views only (the pages' FP8 rows have no packed varlen layout).
+ *   Overview", capability matrix), and Nkv >= 1 (else FFPA_ERR_NOT_SUPPORTED).
+ *   Packed (THD) batches: ffpa_varlen_fwd_fp8 below.
  *   workspace: device scratch of at least ffpa_fp8_workspace_bytes() bytes,
  *   256-byte aligned; it holds the codes and scales afterwards, at the
  *   offsets ffpa_fp8_workspace_layout() gives, with the head dim of the codes
@@ -172,6 +172,29 @@ FFPA_API ffpa_status ffpa_fwd_fp8(ffpa_dtype dt, ffpa_view q, ffpa_view k, ffpa_
 FFPA_API ffpa_status ffpa_fwd_fp8_quantized(ffpa_dtype dt, ffpa_view o, float* lse, const void* workspace,
                                             size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                                             int causal, float scale, ffpa_stream_t stream);
+/* FP8 forward of a packed (THD) batch: the layout, cu_seqlens contract and
+ * device-side checks of ffpa_varlen_fwd ("CuTe-DSL Backend", "Varlen (packed
+ * THD) API"; a sequence that breaks them sets FFPA_ERR_INVALID_VALUE in the
+ * status word), with the quantization of ffpa_fwd_fp8 applied per
+ * (sequence, head) and tensor. The pages' FP8 rows ("Backends Overview",
+ * capability matrix) offer no packed layout; this is the plain extension:
+ * each sequence is quantized and attended as the dense FP8 forward would one
+ * batch entry.
+ *   total_k >= 1 when total_q >= 1 (else FFPA_ERR_NOT_SUPPORTED); D as for
+ *   ffpa_fwd_fp8.
+ *   workspace: device scratch of at least ffpa_varlen_fp8_workspace_bytes()
+ *   bytes, 256-byte aligned (codes of every token, head dim padded to a
+ *   multiple of 128; V transposed with sequence b's keys from column
+ *   16 ceil(cu_k[b] / 16) + 16 b; per-(sequence, head) scales). Its contents
+ *   afterwards are not part of the interface.
+ *   Returns before any launch on invalid arguments; asynchronous on `stream`. */
+FFPA_API size_t ffpa_varlen_fp8_workspace_bytes(int batch, int total_q, int total_k, int max_seqlen_q,
+                                                int max_seqlen_k, int Hq, int Hkv, int D);
+FFPA_API ffpa_status ffpa_varlen_fwd_fp8(ffpa_dtype dt, const void* q, const void* k, const void* v, void* o,
+                                         float* lse, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                                         int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int Hq,
+                                         int Hkv, int D, int causal, float scale, void* workspace,
+                                         size_t workspace_bytes, ffpa_stream_t stream);
 
 /* Workspace bytes ffpa_bwd needs for this problem (fp32 row statistics). */
 FFPA_API size_t ffpa_bwd_workspace_bytes(ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D);

@@ -19,6 +19,10 @@ readings taken here (each one a plain choice the rest of the pages support):
   dequantized inputs code * scale, in fp64. The kernel further rounds the
   softmax numerators P to e4m3 before the P V product (no extra scale);
   ``p_rounding_bound`` bounds what that rounding can change in O.
+* A packed (THD) batch ("CuTe-DSL Backend", "Varlen (packed THD) API") is
+  quantized and attended sequence by sequence, each sequence as one batch
+  entry of the dense FP8 forward (``varlen_attention_fwd_fp8``); the pages'
+  FP8 rows offer no packed layout, so this is the plain extension.
 """
 from __future__ import annotations
 
@@ -103,6 +107,34 @@ def attention_fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None)
     vd = dequantize(*quantize(v))
     o, lse = attention_fwd(qd, kd, vd, causal, scale)
     return o, lse, (qd, kd, vd)
+
+
+def varlen_attention_fwd_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool = False, scale: float | None = None):
+    """Packed FP8 forward: q [Tq, Hq, D], k/v [Tk, Hkv, D], int cu_seqlens [batch + 1].
+    Each sequence is one batch entry of ``attention_fwd_fp8`` (its own per-head
+    scales). Returns (O [Tq, Hq, D], LSE [Hq, Tq], bound [Tq, Hq, D]) with the
+    ``p_rounding_bound`` of each sequence in ``bound``."""
+    q32, k32, v32 = _f32(q), _f32(k), _f32(v)
+    cq = np.asarray(cu_seqlens_q, dtype=np.int64)
+    ck = np.asarray(cu_seqlens_k, dtype=np.int64)
+    Tq, Hq, D = q32.shape
+    o = np.zeros((Tq, Hq, D))
+    lse = np.full((Hq, Tq), -np.inf)
+    bound = np.zeros((Tq, Hq, D))
+    sc = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+        if q1 == q0:
+            continue
+        qb = q32[q0:q1].transpose(1, 0, 2)[None]  # [1, Hq, Lq, D]
+        kb = k32[k0:k1].transpose(1, 0, 2)[None]
+        vb = v32[k0:k1].transpose(1, 0, 2)[None]
+        ob, lb, (qd, kd, vd) = attention_fwd_fp8(qb, kb, vb, causal, sc)
+        o[q0:q1] = ob[0].transpose(1, 0, 2)
+        lse[:, q0:q1] = lb[0]
+        if k1 > k0:  # no keys: no P to round (O = 0 exactly)
+            bound[q0:q1] = p_rounding_bound(qd, kd, vd, causal, sc)[0].transpose(1, 0, 2)
+    return o, lse, bound
 
 
 def p_rounding_bound(qd, kd, vd, causal: bool = False, scale: float | None = None) -> np.ndarray:

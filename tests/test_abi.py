@@ -355,3 +355,22 @@ def test_backward_workspace_budget_plan(lib):
     vgroup = 2 * (700 + 3 * 256) * 304 * 2
     assert lib.ffpa_varlen_bwd_workspace_bytes_budget(0, 3, 600, 700, 300, 400, 4, 2, 512, 0,
                                                       vsmall + 2 * vgroup + 512) == vsmall + a256(vgroup) + vgroup
+
+
+def test_packed_fp8_validates_before_any_launch(lib):
+    n = lib.ffpa_varlen_fp8_workspace_bytes(2, 30, 40, 20, 25, 4, 2, 512)
+    assert n > 0
+
+    def call(cu_k=FAKE, total_k=40, ws=FAKE, ws_bytes=n, D=512, lse=FAKE):
+        return lib.ffpa_varlen_fwd_fp8(0, FAKE, FAKE, FAKE, FAKE, lse, FAKE, cu_k, 2, 30, total_k, 20, 25, 4, 2, D,
+                                       1, 0.05, ws, ws_bytes, None)
+
+    assert call(cu_k=None) == 1 and "one-sided" in lib.ffpa_last_error().decode()
+    assert call(ws_bytes=n - 1) == 1 and "too small" in lib.ffpa_last_error().decode()
+    assert call(ws=FAKE + 32) == 1 and "256-byte" in lib.ffpa_last_error().decode()
+    assert call(total_k=0, ws_bytes=lib.ffpa_varlen_fp8_workspace_bytes(2, 30, 0, 20, 25, 4, 2, 512)) == 2
+    assert call(D=48) == 2
+    assert call(lse=0) == 1
+    # sizes: V^T columns for 16-aligned sequence starts, per-(sequence, head) scales
+    assert lib.ffpa_varlen_fp8_workspace_bytes(2, 30, 40, 20, 25, 4, 2, 48) == 0
+    assert lib.ffpa_varlen_fp8_workspace_bytes(3, 30, 40, 20, 25, 4, 2, 512) > n

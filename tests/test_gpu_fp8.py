@@ -184,3 +184,53 @@ def test_fp8_all_zero_heads():
     assert np.all(np.abs(o.float().cpu().numpy() - o_ref) <= tol)
     assert np.all(o[:, 2:4].float().cpu().numpy() == 0.0)   # heads of the zero V head
     assert np.all(np.abs(lse.cpu().numpy() - lse_ref) <= 1e-3)
+
+
+def run_fp8_varlen(lq, lk, Hq, Hkv, D, causal, dtype=torch.bfloat16, seed=0):
+    """Packed FP8 forward against the oracle's per-sequence FP8 reference, with
+    the tolerance of run_fp8 (derived P-rounding bound per sequence, output
+    rounding, the stated margin)."""
+    inp = workloads.random_varlen(lq, lk, Hq, Hkv, D, dtype, seed=seed)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    cq, ck = inp["cu_seqlens_q"], inp["cu_seqlens_k"]
+    scale = 1.0 / math.sqrt(D)
+    o, lse = api.varlen_fwd_fp8(q, k, v, cq.cuda(), ck.cuda(), max(lq), max(lk), causal, scale)
+    api.get_status()
+    o_ref, lse_ref, bound = ofp8.varlen_attention_fwd_fp8(inp["q"], inp["k"], inp["v"], cq.numpy(), ck.numpy(),
+                                                          causal, scale)
+    og = o.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(og))
+    vmax = float(np.abs(inp["v"].float().numpy()).max())
+    tol = bound + 2.0 ** -8 * np.abs(o_ref) + 1e-3 * vmax
+    err = np.abs(og - o_ref)
+    assert np.all(err <= tol), f"O: max err {err.max():.3e}, max err/tol {float((err / tol).max()):.3f}"
+    lg = lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.abs(lg[fin] - lse_ref[fin]) <= 1e-3), f"LSE max err {np.abs(lg[fin] - lse_ref[fin]).max():.3e}"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_varlen_d512(causal):
+    # ragged lengths (several row and key tiles, tails), a zero-length query
+    # sequence, and a sequence whose keys start off a 16-column boundary
+    run_fp8_varlen([300, 0, 129, 517], [300, 37, 400, 517], 4, 2, 512, causal, seed=21)
+
+
+@pytest.mark.parametrize("D", [64, 96, 320, 1024])
+def test_fp8_varlen_head_dims(D):
+    run_fp8_varlen([70, 200, 33], [150, 5, 260], 2, 2, D, True, seed=D + 3)
+
+
+def test_fp8_varlen_keyless_sequence_and_fp16():
+    # a sequence without keys gives O = 0, LSE = -inf
+    run_fp8_varlen([40, 90, 17], [0, 300, 64], 8, 2, 512, False, dtype=torch.float16, seed=33)
+
+
+def test_fp8_varlen_bound_below_longest_sequence_is_an_error():
+    inp = workloads.random_varlen([100, 300], [100, 300], 2, 2, 512, torch.bfloat16, seed=5)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    cq, ck = inp["cu_seqlens_q"].cuda(), inp["cu_seqlens_k"].cuda()
+    api.varlen_fwd_fp8(q, k, v, cq, ck, 299, 300, False, 0.05)
+    with pytest.raises(ValueError, match="varlen contract"):
+        api.get_status()

@@ -130,3 +130,40 @@ def test_fp8_reference_is_the_plain_definition_of_dequantized_inputs():
     ref_lse = torch.logsumexp(s, dim=-1)
     assert np.allclose(o, ref_o.numpy(), atol=1e-12)
     assert np.allclose(lse, ref_lse.numpy(), atol=1e-12)
+
+
+def test_packed_fp8_single_sequence_is_the_dense_reference():
+    # a packed batch of one sequence is one batch entry of the dense FP8 forward
+    oracle.build()
+    g = torch.Generator().manual_seed(11)
+    q = torch.randn(1, 4, 13, 64, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 2, 21, 64, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 2, 21, 64, generator=g).to(torch.bfloat16)
+    o, lse, (qd, kd, vd) = fp8.attention_fwd_fp8(q, k, v, True, 0.11)
+    bound = fp8.p_rounding_bound(qd, kd, vd, True, 0.11)
+    op, lp, bp = fp8.varlen_attention_fwd_fp8(q[0].transpose(0, 1), k[0].transpose(0, 1), v[0].transpose(0, 1),
+                                              [0, 13], [0, 21], True, 0.11)
+    assert np.array_equal(op, o[0].transpose(1, 0, 2))
+    assert np.array_equal(lp, lse[0])
+    assert np.array_equal(bp, bound[0].transpose(1, 0, 2))
+
+
+def test_packed_fp8_scales_are_per_sequence():
+    # scaling one sequence's inputs by a power of two changes nothing in the
+    # other sequences (their scales are their own), and an empty-key sequence
+    # gives O = 0 and LSE = -inf
+    oracle.build()
+    g = torch.Generator().manual_seed(12)
+    cq, ck = [0, 9, 20, 26], [0, 11, 30, 30]
+    q = torch.randn(26, 2, 64, generator=g).to(torch.bfloat16)
+    k = torch.randn(30, 1, 64, generator=g).to(torch.bfloat16)
+    v = torch.randn(30, 1, 64, generator=g).to(torch.bfloat16)
+    o1, l1, _ = fp8.varlen_attention_fwd_fp8(q, k, v, cq, ck, False, 0.125)
+    q2, k2, v2 = q.clone(), k.clone(), v.clone()
+    q2[9:20] *= 1024.0
+    k2[11:30] *= 1024.0
+    v2[11:30] *= 1024.0
+    o2, l2, _ = fp8.varlen_attention_fwd_fp8(q2, k2, v2, cq, ck, False, 0.125)
+    assert np.array_equal(o1[:9], o2[:9]) and np.array_equal(l1[:, :9], l2[:, :9])
+    assert not np.allclose(o1[9:20], o2[9:20])
+    assert np.all(o1[20:] == 0.0) and np.all(np.isneginf(l1[:, 20:]))
